@@ -1,0 +1,253 @@
+"""Plain fp64 definitions of the quantised MoE expert block (test oracle).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the product library.
+
+Sources (page title, then section):
+  [FM]  "flash-moe: C/Metal engine running a 397B MoE on an M3 Max"
+        (discuss.pytorch.kr): sections "FMA-optimised dequant kernel",
+        "hand-written Metal compute shaders", "per-layer pipeline",
+        "Qwen3.5-397B-A17B model architecture".
+  [GN]  "Flash-MoE - running a 397B-parameter model on a laptop" (GeekNews
+        topic 27758), sections "Model architecture", "Metal Compute Shaders".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 64          # quantisation group: 64 consecutive input columns of a row
+_ALIGN = 256        # every plane of a blob starts on a 256-byte boundary
+
+
+# ---------------------------------------------------------------------------
+# packed expert blob
+# ---------------------------------------------------------------------------
+def layout(bits: int, hidden: int, inter: int) -> tuple:
+    """Byte offset, row count and 32-bit words per row of the six planes.
+
+    Order: gate codes, gate (scale,bias), up codes, up (scale,bias), down
+    codes, down (scale,bias).  Gate/up rows are the I intermediate rows of
+    H inputs; down rows are the H output rows of I inputs.  Returns
+    (dict name -> (offset, rows, words_per_row), blob_bytes).
+    Pinned by the expert-size pin (6.75 MiB per 4-bit expert of the
+    397B model, [FM] "SSD expert streaming").
+    """
+    if bits not in (2, 4):
+        raise ValueError("bits must be 2 or 4")
+    per_word = 32 // bits
+    planes = [
+        ("gate_q", inter, hidden // per_word),
+        ("gate_sb", inter, hidden // GROUP),
+        ("up_q", inter, hidden // per_word),
+        ("up_sb", inter, hidden // GROUP),
+        ("down_q", hidden, inter // per_word),
+        ("down_sb", hidden, inter // GROUP),
+    ]
+    out, pos = {}, 0
+    for name, rows, wpr in planes:
+        pos = -(-pos // _ALIGN) * _ALIGN
+        out[name] = (pos, rows, wpr)
+        pos += rows * wpr * 4
+    return out, -(-pos // _ALIGN) * _ALIGN
+
+
+def unpack_codes(words: np.ndarray, bits: int) -> np.ndarray:
+    """Integer codes of packed rows: uint32 [rows][wpr] -> int64 [rows][wpr*32/bits].
+
+    Code c sits at bit (c mod (32/bits))*bits of word c div (32/bits), lowest
+    bits first.  Pinned by hand-worked words (tests/golden/unpack_examples.txt).
+    """
+    w = np.asarray(words, dtype=np.uint64)
+    per_word = 32 // bits
+    mask = (1 << bits) - 1
+    codes = np.empty(w.shape[:-1] + (w.shape[-1], per_word), dtype=np.int64)
+    for i in range(per_word):
+        codes[..., i] = ((w >> np.uint64(bits * i)) & np.uint64(mask)).astype(np.int64)
+    return codes.reshape(w.shape[:-1] + (w.shape[-1] * per_word,))
+
+
+def bf16_to_f64(b16: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values (bf16 is the top half of fp32)."""
+    u = (np.asarray(b16, dtype=np.uint32) & 0xFFFF) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def dequantize(q_words: np.ndarray, sb_words: np.ndarray, bits: int) -> np.ndarray:
+    """W[r, c] = q[r, c] * s[r, c//64] + b[r, c//64] in fp64.
+
+    [FM] "FMA-optimised dequant kernel": the weight is nibble*scale+bias.
+    sb word g of a row holds scale (low 16 bits, bf16) and bias (high 16).
+    Pinned by hand-worked dequant examples and the FMA identity.
+    """
+    q = unpack_codes(q_words, bits).astype(np.float64)
+    sb = np.asarray(sb_words, dtype=np.uint32)
+    s = bf16_to_f64(sb & 0xFFFF)
+    b = bf16_to_f64(sb >> 16)
+    n = q.shape[-1]
+    if n != sb.shape[-1] * GROUP:
+        raise ValueError("codes and (scale,bias) groups disagree")
+    g = np.arange(n) // GROUP
+    return q * s[..., g] + b[..., g]
+
+
+def expert_weights(blob: np.ndarray, bits: int, hidden: int, inter: int) -> tuple:
+    """(Wg [I][H], Wu [I][H], Wd [H][I]) dequantised from one blob (fp64)."""
+    words = np.ascontiguousarray(blob).view(np.uint32).reshape(-1)
+    planes, nbytes = layout(bits, hidden, inter)
+    if words.size * 4 < nbytes:
+        raise ValueError("blob too small")
+
+    def plane(name):
+        off, rows, wpr = planes[name]
+        return words[off // 4: off // 4 + rows * wpr].reshape(rows, wpr)
+
+    wg = dequantize(plane("gate_q"), plane("gate_sb"), bits)
+    wu = dequantize(plane("up_q"), plane("up_sb"), bits)
+    wd = dequantize(plane("down_q"), plane("down_sb"), bits)
+    return wg, wu, wd
+
+
+# ---------------------------------------------------------------------------
+# expert FFN
+# ---------------------------------------------------------------------------
+def silu(a):
+    """a * sigmoid(a) = a / (1 + exp(-a))."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+def sigmoid(z):
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def expert_ffn(weights: tuple, x: np.ndarray) -> np.ndarray:
+    """y = Wd (silu(Wg x) * (Wu x)).
+
+    [FM] shader list: dequant matvec for gate/up/down and fused SwiGLU
+    (gate branch through SiLU, multiplied by the up branch).
+    Pinned by the constant-row closed form.
+    """
+    wg, wu, wd = weights
+    x = np.asarray(x, dtype=np.float64)
+    a = wg @ x
+    u = wu @ x
+    h = silu(a) * u
+    return wd @ h
+
+
+# ---------------------------------------------------------------------------
+# routing, shared gate, combine
+# ---------------------------------------------------------------------------
+def route(logits: np.ndarray, k: int) -> tuple:
+    """(ids [K] int, weights [K] fp64) for one token.
+
+    [FM] "per-layer pipeline": softmax + top-K on the router logits.  The K
+    largest logits are taken by value, ties broken towards the lower expert
+    id, in descending order; the weights are the softmax of the K selected
+    logits (equal to full softmax -> top-K -> renormalise).
+    Pinned by brute force over all K-subsets and the sum-to-one invariant.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    if not np.all(np.isfinite(l)):
+        raise ValueError("router logits must be finite")
+    if not 1 <= k <= l.size:
+        raise ValueError("need 1 <= K <= number of experts")
+    order = np.argsort(-l, kind="stable")       # stable: equal logits keep id order
+    ids = order[:k]
+    sel = l[ids]
+    e = np.exp(sel - sel.max())
+    return ids.astype(np.int64), e / e.sum()
+
+
+def shared_gate(wsg_bf16: np.ndarray, x: np.ndarray) -> float:
+    """g = sigmoid(w_sg . x) with w_sg given as bf16 bit patterns.
+
+    [FM] shader list "MoE combine + residual + sigmoid gate" and model
+    section "plus one shared expert".  Pinned by closed-form gate values.
+    """
+    w = bf16_to_f64(wsg_bf16)
+    return float(sigmoid(w @ np.asarray(x, dtype=np.float64)))
+
+
+def combine(residual, routed_y, weights, shared_y=None, g=None):
+    """out = residual + sum_k w_k y_k (+ g * y_shared)."""
+    out = np.asarray(residual, dtype=np.float64).copy()
+    for wk, yk in zip(weights, routed_y):
+        out += wk * yk
+    if shared_y is not None:
+        out += g * shared_y
+    return out
+
+
+def moe_block(get_expert, x, logits, residual, k, shared=None, wsg=None):
+    """One MoE block for T independent tokens.
+
+    get_expert(e) -> (Wg, Wu, Wd) of routed expert e;  shared -> the shared
+    expert's weights or None.  x, residual: [T][H]; logits: [T][E].
+    Returns dict(out [T][H], ids [T][K], weights [T][K], gate [T] or None,
+    y [T][K(+1)][H] unweighted expert outputs).
+    """
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    residual = np.atleast_2d(np.asarray(residual, dtype=np.float64))
+    logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    T = x.shape[0]
+    cache = {}
+    outs, all_ids, all_w, gates, ys = [], [], [], [], []
+    for t in range(T):
+        ids, w = route(logits[t], k)
+        y_t = []
+        for e in ids:
+            e = int(e)
+            if e not in cache:
+                cache[e] = get_expert(e)
+            y_t.append(expert_ffn(cache[e], x[t]))
+        ysh, g = None, None
+        if shared is not None:
+            ysh = expert_ffn(shared, x[t])
+            g = shared_gate(wsg, x[t])
+        outs.append(combine(residual[t], y_t, w, ysh, g))
+        all_ids.append(ids)
+        all_w.append(w)
+        gates.append(g)
+        ys.append(np.stack(y_t + ([ysh] if ysh is not None else [])))
+    return {
+        "out": np.stack(outs),
+        "ids": np.stack(all_ids),
+        "weights": np.stack(all_w),
+        "gate": None if shared is None else np.array(gates),
+        "y": np.stack(ys),
+    }
+
+
+# ---------------------------------------------------------------------------
+# stacked decode
+# ---------------------------------------------------------------------------
+def rms_norm(h, eps: float):
+    """h / sqrt(mean(h^2) + eps), unit weight ([FM] shader list: RMSNorm)."""
+    h = np.asarray(h, dtype=np.float64)
+    return h / np.sqrt(np.mean(h * h) + eps)
+
+
+def stack_decode(get_expert_l, h0, logits, k, eps, shared_l=None, wsg_l=None):
+    """One token through L pre-norm MoE blocks.
+
+    h_{l+1} = h_l + MoE_l(rms_norm(h_l)), the residual being h_l itself
+    ([FM] "deferred CMD3": combine, residual and norm stay on the GPU and
+    feed the next layer).  get_expert_l(l, e) -> weights of expert e of layer
+    l; logits [L][E].  Returns (h_L, ids [L][K]).
+    """
+    h = np.asarray(h0, dtype=np.float64).copy()
+    logits = np.asarray(logits, dtype=np.float64)
+    all_ids = []
+    for l in range(logits.shape[0]):
+        xn = rms_norm(h, eps)
+        sh = None if shared_l is None else shared_l(l)
+        wsg = None if wsg_l is None else wsg_l(l)
+        r = moe_block(lambda e, l=l: get_expert_l(l, e), xn[None], logits[l][None],
+                      h[None], k, sh, wsg)
+        h = r["out"][0]
+        all_ids.append(r["ids"][0])
+    return h, np.stack(all_ids)
