@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Throughput of the batch-1 quantised MoE expert block on B300.
+
+Default workload (the one the headline metric is quoted on): the Qwen-shaped
+4-bit block (H 4096, 512 routed experts, top-4 + 1 shared, I 1024, group-64
+bf16 scale/bias), run as a decode chain: one step = one token through 64 such
+blocks, each with its own shared expert and fresh router logits, RMSNorm +
+residual between blocks, all in ONE launch of the persistent kernel
+(fmoe_stack_decode).  No block's weights are requested before the previous
+block's output exists.
+
+value     active-expert bytes (5 experts x 7,077,888 B per block) per second,
+          inputs resident in HBM, CUDA events on the launching stream
+e2e       the same metric through the C-ABI call with the step's inputs copied
+          from pinned host memory and the result copied back, per step
+roofline  the fused kernel's algorithmic bytes per launch / its event time,
+          against the measured HBM copy bandwidth (MEASURED_PEAKS.json)
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload.  --gpus N (torchrun) runs N independent replicas (the path has no
+exchange step); value sums the bytes of all ranks over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "active-expert GB/s and % of HBM peak; MoE-block tokens/s at batch 1"
+CHAIN = 64
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fmoe", choices=["fmoe", "reference"])
+    ap.add_argument("--workload", default="qwen_q4",
+                    choices=["qwen_q4", "qwen_q2", "stack48", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="run only this many steps (for an ncu launch list); prints no JSON")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def workload_desc(name):
+    import synth
+    if name == "qwen_q4":
+        return synth.QWEN_Q4, CHAIN
+    if name == "qwen_q2":
+        return synth.QWEN_Q2, CHAIN
+    if name == "stack48":
+        return synth.STACK48, synth.STACK48.n_layers
+    if name == "tiny":
+        return synth.TINY, CHAIN
+    raise ValueError(name)
+
+
+def bytes_per_token(shape, n_layers):
+    import synth
+    blob = synth.blob_bytes(shape.bits, shape.hidden, shape.inter)
+    return n_layers * (shape.top_k + (1 if shape.has_shared else 0)) * blob
+
+
+def workload_name(shape, n_layers):
+    if shape.n_layers > 1:
+        return (f"{shape.name}: decode step = 1 token through {n_layers} layers "
+                f"(RMSNorm eps {shape.eps} + residual between layers), one persistent launch")
+    return (f"{shape.name}: decode step = 1 token through a chain of {n_layers} such blocks "
+            f"(own shared expert and fresh logits per block, RMSNorm + residual between blocks), "
+            f"one persistent launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region (NVML, 5 ms period)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, device_index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self._ok = True
+        except Exception as e:  # noqa: BLE001
+            self.error = str(e)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self._ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self._ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "error", "")}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(self.reasons - {"gpu_idle"})}
+
+
+# ---------------------------------------------------------------------------
+# committed ncu traffic summary (null when the kernel sources changed since)
+# ---------------------------------------------------------------------------
+KERNEL_SOURCES = ["quantized_moe_expert_05_b300/csrc/fmoe_fused.cu",
+                  "quantized_moe_expert_05_b300/csrc/fmoe_internal.cuh",
+                  "quantized_moe_expert_05_b300/csrc/fmoe_kernels.cuh"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """Per-launch DRAM bytes from profiles/ncu_traffic.txt for this workload, if
+    the kernel sources still hash to the value recorded there."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload:
+            if parts[2] == want:
+                return float(parts[1])
+    return None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_sample(shape, n_blocks, seed_tag=0):
+    """Time the fp64 oracle on `n_blocks` blocks of the workload (inputs made first).
+    Returns (seconds per block, threads used, description)."""
+    import numpy as np
+    import oracle
+    import synth
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        threads = 1
+    K = shape.top_k
+    inp = synth.block_inputs(shape, n_blocks, tag=1000 + seed_tag)
+    blobs = []
+    for b in range(n_blocks):
+        ids, _ = oracle.route(inp.logits[b].numpy(), K)
+        ex = {int(e): synth.expert_blob(shape, 0, int(e)).numpy().view(np.uint8) for e in ids}
+        sh = synth.expert_blob(shape, 0, shape.n_experts + b).numpy().view(np.uint8) if shape.has_shared else None
+        blobs.append((ex, sh))
+    wsg = synth.shared_gate_vector(shape).numpy().view(np.uint16) if shape.has_shared else None
+    t0 = time.perf_counter()
+    for b in range(n_blocks):
+        ex, sh = blobs[b]
+        get = lambda e, ex=ex: oracle.expert_weights(ex[e], shape.bits, shape.hidden, shape.inter)
+        shw = oracle.expert_weights(sh, shape.bits, shape.hidden, shape.inter) if sh is not None else None
+        oracle.moe_block(get, inp.x[b].numpy(), inp.logits[b].numpy(), inp.residual[b].numpy(), K, shw, wsg)
+    dt = (time.perf_counter() - t0) / n_blocks
+    desc = (f"{n_blocks} block(s) of {shape.name}: dequantise the {K + (1 if shape.has_shared else 0)} "
+            f"active experts + fp64 matvecs + combine (numpy/OpenBLAS), inputs prepared beforehand")
+    return dt, threads, desc
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step dequantises one active expert of
+    a block and runs its fp64 forward (the block's dominant work), cycling over the
+    block's experts; value = that expert's packed bytes per second."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import synth
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        threads = 1
+    shape, n_layers = workload_desc(args.workload)
+    inp = synth.block_inputs(shape, 1, tag=500)
+    ids, _ = oracle.route(inp.logits[0].numpy(), shape.top_k)
+    experts = [int(e) for e in ids] + ([shape.n_experts] if shape.has_shared else [])
+    blobs = [synth.expert_blob(shape, 0, e).numpy().view(np.uint8) for e in experts]
+    H, I, bits = shape.hidden, shape.inter, shape.bits
+    x = inp.x[0].numpy().astype(np.float64)
+    planes, _ = oracle.layout(bits, H, I)
+
+    def rows(blob, name, n):
+        off, r, wpr = planes[name]
+        return blob.view(np.uint32)[off // 4: off // 4 + n * wpr].reshape(n, wpr)
+
+    def one(i, frac):
+        # the first frac of the rows of one expert's gate, up and down matrices
+        blob = blobs[i % len(blobs)]
+        ni, nh = max(1, int(I * frac)), max(1, int(H * frac))
+        wg = oracle.dequantize(rows(blob, "gate_q", ni), rows(blob, "gate_sb", ni), bits)
+        wu = oracle.dequantize(rows(blob, "up_q", ni), rows(blob, "up_sb", ni), bits)
+        h = oracle.silu(wg @ x) * (wu @ x)
+        wd = oracle.dequantize(rows(blob, "down_q", nh), rows(blob, "down_sb", nh), bits)
+        wd[:, :ni] @ h
+        return (2 * ni * (H * bits // 8 + H // 16) + nh * (I * bits // 8 + I // 16))
+
+    # size the per-step sample so that warm-up + steps take about 90 s
+    t0 = time.perf_counter()
+    one(0, 1.0)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, 90.0 / max(args.steps + args.warmup, 1) / t_full)
+    for i in range(args.warmup):
+        one(i, frac)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        nbytes += one(i, frac)
+    el = time.perf_counter() - t0
+    dt = el / max(args.steps, 1)
+    gbs = nbytes / el / 1e9
+    desc = (f"per step the first {frac:.3f} of the rows of one active expert of a {shape.name} block "
+            f"(dequantise + fp64 gate/up/down matvecs + SwiGLU, numpy/OpenBLAS), cycling over the "
+            f"block's {len(blobs)} experts; value = packed bytes processed per second")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(shape, n_layers), "step": "one expert forward (bounded CPU sample)"},
+        "tokens_per_s_per_block": gbs * 1e9 / (len(blobs) * synth.blob_bytes(bits, H, I)),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# CUDA path
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from quantized_moe_expert_05_b300 import build
+    build.build()
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    shape, n_layers = workload_desc(args.workload)
+    K = shape.top_k
+    S = 1 if shape.has_shared else 0
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+
+    # expert pools: a stack has its own routed pool per layer; a chain shares
+    # one routed pool and gives every block its own shared expert
+    layers = []
+    if shape.n_layers > 1:
+        for l in range(n_layers):
+            pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
+            synth.fill_pool(pool, shape, l, 0, shape.n_experts)
+            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool))
+    else:
+        pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
+        synth.fill_pool(pool, shape, 0, 0, shape.n_experts)
+        shared = None
+        if S:
+            shared = torch.empty(n_layers * nw, dtype=torch.int32, device=dev)
+            synth.fill_pool(shared, shape, 0, shape.n_experts, n_layers)
+        for l in range(n_layers):
+            sh = shared[l * nw:(l + 1) * nw] if S else None
+            wsg = synth.shared_gate_vector(shape, l).to(dev) if S else None
+            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool, sh, wsg))
+    ws = fm.new_workspace(layers[0], 1, K, n_layers)
+
+    # per-step inputs: NSETS distinct (h0, logits) sets, cycled
+    NSETS = 8
+    import dataclasses
+    h0, logits = synth.stack_inputs(
+        dataclasses.replace(shape, seed=shape.seed + 1000 * rank, n_layers=n_layers), NSETS)
+    h0_d, lg_d = h0.to(dev), logits.to(dev)
+    h = torch.empty(shape.hidden, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        h.copy_(h0_d[i % NSETS])
+        fm.stack_decode(layers, lg_d[i % NSETS], h, K, shape.eps, ws)
+
+    if args.profile_launches:
+        for i in range(args.profile_launches):
+            step(i)
+        torch.cuda.synchronize()
+        assert fm.last_device_error(ws) == fm.OK
+        return 0
+
+    # graph of NSETS steps (one persistent launch + one 16 KB copy each)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(NSETS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(i)
+        graphs.append(g)
+
+    for i in range(args.warmup):
+        graphs[i % NSETS].replay()
+    torch.cuda.synchronize()
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # kernel-only timing: events around K graph replays on the launching stream
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % NSETS].replay()
+        ev1.record(stream)
+        ev1.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device-side wait timed out in the timed region")
+
+    # end-to-end through the C ABI: pinned host inputs in, result out, every step
+    h0_host = h0.pin_memory()
+    lg_host = logits.pin_memory()
+    out_host = torch.empty((args.steps, shape.hidden), dtype=torch.float32).pin_memory()
+    lg_step = torch.empty_like(lg_d[0])
+    for i in range(3):
+        h.copy_(h0_host[i % NSETS], non_blocking=True)
+        lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
+        fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
+        out_host[i].copy_(h, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        h.copy_(h0_host[i % NSETS], non_blocking=True)
+        lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
+        fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
+        out_host[i].copy_(h, non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = h0_host[0].numel() * 4 + lg_host[0].numel() * 4
+    d2h = shape.hidden * 4
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    per_step = bytes_per_token(shape, n_layers)
+    total_bytes = per_step * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    ms_step = ms / args.steps
+    # the fused kernel is the only kernel of the timed region besides a 16 KB
+    # device copy per step (torch's), so its launch time is the step time
+    achieved = per_step / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = committed_traffic(args.workload)
+    clk = clocks.summary()
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": workload_name(shape, n_layers),
+            "active_bytes_per_step": per_step,
+            "weights": f"{shape.bits}-bit codes, group 64, bf16 scale+bias; random-init (seeded)",
+            "l2": "inputs larger than L2: each step streams "
+                  f"{per_step / 1e9:.2f} GB of expert weights (L2 126 MB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s_per_block": n_layers * args.steps * world / (ms * 1e-3),
+        "tokens_per_s_stack": args.steps * world / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)",
+                     "traffic": traffic, "kernel": f"fused_moe_kernel<{shape.bits}>",
+                     "algorithmic_bytes_per_launch": per_step},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n = 2 if shape.hidden >= 4096 else 4
+        dt, threads, desc = oracle_sample(shape, n)
+        line["cpu_baseline"] = {"value": bytes_per_token(shape, 1) / dt / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * fmoe.h -- C ABI of the batch-1 quantised MoE expert block for B300 (sm_103a).
+ *
+ * The operations follow the flash-moe write-ups (discuss.pytorch.kr post
+ * "flash-moe: C/Metal engine running a 397B MoE on an M3 Max" and GeekNews
+ * topic 27758 "Flash-MoE - running a 397B-parameter model on a laptop"):
+ *   - "per-layer pipeline": router logits -> softmax + top-K -> expert forward
+ *     -> combine + residual (+ norm) feeding the next layer;
+ *   - "FMA-optimised dequant kernel": expert weights are 4-bit (or 2-bit)
+ *     codes dequantised as code * scale + bias;
+ *   - "hand-written Metal compute shaders": dequant matvec, fused SwiGLU,
+ *     two-stage RMSNorm, and one fused "MoE combine + residual + sigmoid gate";
+ *   - "Qwen3.5-397B-A17B model architecture": K routed experts out of E plus
+ *     one always-on shared expert.
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer unless its comment says
+ *     "host".  The caller owns all memory; the library allocates nothing and
+ *     keeps no state between calls except inside the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising, except
+ *     fmoe_last_device_error, which synchronises `stream`.
+ *   - Host-side argument checks return FMOE_ERR_INVALID_ARG (null or
+ *     misaligned pointer, inconsistent sizes) or FMOE_ERR_UNSUPPORTED (a
+ *     shape or bit width this build does not implement) and enqueue nothing.
+ *     A failed launch returns FMOE_ERR_CUDA.  Device-side waits that run out
+ *     of time set an error word in the workspace and return; the host reads
+ *     it with fmoe_last_device_error (FMOE_ERR_TIMEOUT).
+ *   - fp32 activations are read and written as IEEE binary32.  Router logits
+ *     must be finite (NaN/inf logits give unspecified ids).  Activations must
+ *     stay below 2^40 in magnitude (the dot products pre-scale x by powers of
+ *     two; larger values overflow to inf).
+ *
+ * Packed expert blob (one per expert, contiguous, 256-byte aligned planes):
+ *     gate_q  [I][H*bits/32] uint32   codes, code c at bits (c mod 32/bits)*bits
+ *                                     of word c/(32/bits) (lowest bits first)
+ *     gate_sb [I][H/64]      uint32   bits 0..15 scale (bf16), 16..31 bias (bf16)
+ *     up_q    [I][H*bits/32] uint32
+ *     up_sb   [I][H/64]      uint32
+ *     down_q  [H][I*bits/32] uint32
+ *     down_sb [H][I/64]      uint32
+ *   The dequantised weight of row r, column c is q * scale[r][c/64] +
+ *   bias[r][c/64]; gate/up rows have H columns, down rows have I columns.
+ *   Blob size: fmoe_expert_bytes(); the routed experts of a layer sit at
+ *   stride fmoe_expert_bytes() from `experts`.
+ */
+#ifndef FMOE_H
+#define FMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FMOE_OK = 0,
+  FMOE_ERR_INVALID_ARG = 1,
+  FMOE_ERR_UNSUPPORTED = 2,
+  FMOE_ERR_CUDA = 3,
+  FMOE_ERR_TIMEOUT = 4
+} fmoe_status;
+
+/* Largest sizes this build accepts. */
+#define FMOE_MAX_TOKENS 16      /* T per call                                  */
+#define FMOE_MAX_TOPK 16        /* K routed experts per token                  */
+#define FMOE_MAX_EXPERTS 1024   /* E routed experts per layer                  */
+#define FMOE_MAX_HIDDEN 8192    /* H                                           */
+#define FMOE_MAX_INTER 4096     /* I                                           */
+#define FMOE_MAX_LAYERS 1024    /* L of fmoe_stack_decode                      */
+
+/*
+ * One MoE layer: describes caller-owned device memory (no ownership passes).
+ *   bits          4 or 2
+ *   group         quantisation group; must be 64
+ *   hidden, inter H and I; multiples of 64 (H also a multiple of 128, I a
+ *                 multiple of 128 for the fused single-launch path)
+ *   n_experts     E routed experts stored at `experts`
+ *   has_shared    0 or 1
+ *   experts       E blobs at stride fmoe_expert_bytes(); 256-byte aligned
+ *   shared        the shared expert's blob (256-byte aligned) or NULL
+ *   shared_gate_w bf16[H] gate vector w_sg (bit patterns), or NULL if no shared
+ */
+typedef struct fmoe_layer {
+  int32_t bits;
+  int32_t group;
+  int32_t hidden;
+  int32_t inter;
+  int32_t n_experts;
+  int32_t has_shared;
+  const void* experts;
+  const void* shared;
+  const uint16_t* shared_gate_w;
+} fmoe_layer;
+
+/* Bytes of one packed expert blob (0 for an unsupported shape). */
+size_t fmoe_expert_bytes(int bits, int hidden, int inter, int group);
+
+/*
+ * Bytes of workspace a call needs for `layer`, T tokens, K routed experts and
+ * L stacked layers (L = 1 for the single-block calls).  The workspace holds
+ * intermediate activations, routing results, device-wide counters and the
+ * device error word.  It must be 256-byte aligned and zeroed once before its
+ * first use (fmoe_workspace_init); afterwards the library keeps it
+ * consistent.  Calls that share a workspace must not overlap in time.
+ */
+size_t fmoe_workspace_bytes(const fmoe_layer* layer /* host */, int T, int K, int L);
+
+/* Zero a workspace of `bytes` bytes (async on `stream`). */
+fmoe_status fmoe_workspace_init(void* ws, size_t bytes, void* stream);
+
+/*
+ * Route T tokens: the flash-moe "softmax + top-K" step ("per-layer pipeline").
+ *   logits  fp32 [T][E]   router logits (finite)
+ *   ids     int32 [T][K]  out: the K largest logits per token in descending
+ *                         order; equal logits rank the lower expert id first
+ *                         (-0 and +0 are equal)
+ *   weights fp32 [T][K]   out: softmax over the K selected logits (sums to 1)
+ * 1 <= T <= FMOE_MAX_TOKENS, 1 <= K <= min(E, FMOE_MAX_TOPK), E <= FMOE_MAX_EXPERTS.
+ */
+fmoe_status fmoe_route(const float* logits, int T, int E, int K,
+                       int32_t* ids, float* weights, void* stream);
+
+/*
+ * Expert forward for given ids (flash-moe CMD3 "expert forward", without the
+ * combine): for token t and slot k < K, y[t][k] = Wd (silu(Wg x_t) * (Wu x_t))
+ * of routed expert ids[t][k]; if layer->has_shared, slot K holds the shared
+ * expert's output for x_t.
+ *   ids  int32 [T][K]         expert ids in [0, E)
+ *   x    fp32  [T][H]
+ *   y    fp32  [T][K+S][H]    out, unweighted (S = has_shared)
+ *   ws   workspace of fmoe_workspace_bytes(layer, T, K, 1) bytes
+ */
+fmoe_status fmoe_expert_ffn(const fmoe_layer* layer /* host */, const int32_t* ids,
+                            int T, int K, const float* x, float* y,
+                            void* ws, void* stream);
+
+/*
+ * One MoE block (flash-moe: routing, expert forward, and the fused "MoE
+ * combine + residual + sigmoid gate"):
+ *   out[t] = residual[t] + sum_k w[t][k] * y[t][k] + sigmoid(w_sg . x[t]) * y_shared[t]
+ * with (ids, w) = fmoe_route(router_logits[t]) and y as in fmoe_expert_ffn
+ * (the sigmoid term only if layer->has_shared).
+ *   x, residual, out  fp32 [T][H];  router_logits fp32 [T][E]
+ *   out may alias residual; it must not overlap x or router_logits.
+ * With T > 1 each distinct expert among the T*K picks is read once.  The
+ * routing result is left in the workspace (see fmoe_ws_routing).
+ */
+fmoe_status fmoe_moe_block(const fmoe_layer* layer /* host */, const float* x,
+                           const float* router_logits, const float* residual,
+                           float* out, int T, int K, void* ws, void* stream);
+
+/*
+ * One decode token through L pre-norm MoE blocks (flash-moe "deferred CMD3":
+ * combine, residual and normalisation stay on the GPU and feed the next
+ * layer; the RMSNorm is the write-ups' two-stage RMS normalisation with unit
+ * weight):
+ *   for l in 0..L-1:  h <- h + MoE_l(h / sqrt(mean(h^2) + eps))
+ * where MoE_l routes with logits[l] and uses residual 0 (the block's
+ * residual is h itself).
+ *   layers  host array of L layer descriptors, all with the same bits,
+ *           hidden, inter, n_experts and has_shared
+ *   logits  fp32 [L][E];  h fp32 [H] in/out
+ *   ws      workspace of fmoe_workspace_bytes(&layers[0], 1, K, L) bytes
+ * No layer's weights are read before the previous layer's output is complete.
+ */
+fmoe_status fmoe_stack_decode(const fmoe_layer* layers /* host */, int L,
+                              const float* logits, float* h, int K, float eps,
+                              void* ws, void* stream);
+
+/*
+ * Device pointers, inside a workspace, to the routing result of the last
+ * fmoe_moe_block call (ids int32 [T][K], weights fp32 [T][K], gate fp32 [T]
+ * = sigmoid(w_sg . x) or 0 without a shared expert) and to the
+ * intermediate activations h fp32 [T][K+S][I].  Host function; no sync.
+ */
+fmoe_status fmoe_ws_routing(void* ws, const fmoe_layer* layer /* host */, int T, int K,
+                            int32_t** ids, float** weights, float** gate, float** h);
+
+/* Static description of a status code (host). */
+const char* fmoe_status_string(fmoe_status s);
+
+/*
+ * Synchronise `stream`, then read and clear the workspace's device error
+ * word: FMOE_OK, or FMOE_ERR_TIMEOUT if a device-side wait gave up since the
+ * last call.  After a timeout the workspace must be re-initialised with
+ * fmoe_workspace_init before reuse.
+ */
+fmoe_status fmoe_last_device_error(void* ws, void* stream);
+
+/*
+ * Test hook for the bounded device-side waits: launches `n_blocks` blocks
+ * that arrive at a workspace counter and wait for `expected` arrivals for at
+ * most `timeout_us` microseconds.  With expected > n_blocks the wait runs
+ * out and the error word is set (no trap, no hang); with expected ==
+ * n_blocks it completes.  1 <= n_blocks <= 148 * 4.
+ */
+fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected,
+                                 int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FMOE_H */

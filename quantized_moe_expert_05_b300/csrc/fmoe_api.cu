@@ -1,0 +1,319 @@
+// extern "C" entry points of libfmoe: argument checks, workspace carving and
+// dispatch to the kernels.  See include/fmoe.h for the contract of each call.
+#include <cstdio>
+#include <cstring>
+
+#include "fmoe_kernels.cuh"
+
+using namespace fmoe;
+
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 200ull * 1000 * 1000;   // 200 ms per device-side wait
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fmoe_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return FMOE_OK;
+  cudaGetLastError();   // clear a sticky launch error so later calls start clean
+  return FMOE_ERR_CUDA;
+}
+
+// Shape checks common to every call that reads expert blobs.
+fmoe_status check_layer(const fmoe_layer* L, bool need_ptrs) {
+  if (L == nullptr) return FMOE_ERR_INVALID_ARG;
+  if (L->bits != 4 && L->bits != 2) return FMOE_ERR_UNSUPPORTED;
+  if (L->group != kGroup) return FMOE_ERR_UNSUPPORTED;
+  if (L->hidden <= 0 || L->inter <= 0 || L->hidden % kGroup || L->inter % kGroup) return FMOE_ERR_INVALID_ARG;
+  if (L->hidden > FMOE_MAX_HIDDEN || L->inter > FMOE_MAX_INTER) return FMOE_ERR_UNSUPPORTED;
+  if (L->n_experts <= 0 || L->n_experts > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
+  if (L->has_shared != 0 && L->has_shared != 1) return FMOE_ERR_INVALID_ARG;
+  if (need_ptrs) {
+    if (L->experts == nullptr || !aligned(L->experts, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
+    if (L->has_shared) {
+      if (L->shared == nullptr || !aligned(L->shared, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
+      if (L->shared_gate_w == nullptr || !aligned(L->shared_gate_w, 16)) return FMOE_ERR_INVALID_ARG;
+    }
+  }
+  return FMOE_OK;
+}
+
+bool vec_ok(const void* p) { return p != nullptr && aligned(p, 16); }
+
+struct Ws {
+  WsLayout lay;
+  uint8_t* base;
+  uint32_t* err() const { return reinterpret_cast<uint32_t*>(base + lay.err); }
+  uint32_t* counters() const { return reinterpret_cast<uint32_t*>(base + lay.counters); }
+  int32_t* ids() const { return reinterpret_cast<int32_t*>(base + lay.ids); }
+  float* weights() const { return reinterpret_cast<float*>(base + lay.weights); }
+  float* gate() const { return reinterpret_cast<float*>(base + lay.gate); }
+  float* h() const { return reinterpret_cast<float*>(base + lay.h); }
+  float* hbuf() const { return reinterpret_cast<float*>(base + lay.hbuf); }
+};
+
+Ws carve(void* ws, const fmoe_layer* L, int T, int K, int n_layers) {
+  Ws w;
+  w.lay = ws_layout(L->hidden, L->inter, L->has_shared, T > n_layers ? T : n_layers, K, n_layers);
+  w.base = static_cast<uint8_t*>(ws);
+  return w;
+}
+
+GenericArgs generic_args(const fmoe_layer* L, int T, int K, const Ws& w) {
+  GenericArgs a{};
+  a.bits = L->bits;
+  a.H = L->hidden;
+  a.I = L->inter;
+  a.E = L->n_experts;
+  a.K = K;
+  a.S = L->has_shared;
+  a.T = T;
+  a.lay = blob_layout(L->bits, L->hidden, L->inter);
+  a.blob = a.lay.bytes;
+  a.experts = static_cast<const uint8_t*>(L->experts);
+  a.shared = static_cast<const uint8_t*>(L->shared);
+  a.h = w.h();
+  a.err = w.err();
+  return a;
+}
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fmoe_expert_bytes(int bits, int hidden, int inter, int group) {
+  if ((bits != 4 && bits != 2) || group != kGroup) return 0;
+  if (hidden <= 0 || inter <= 0 || hidden % kGroup || inter % kGroup) return 0;
+  return blob_layout(bits, hidden, inter).bytes;
+}
+
+size_t fmoe_workspace_bytes(const fmoe_layer* layer, int T, int K, int L) {
+  if (layer == nullptr || T < 1 || K < 1 || L < 1) return 0;
+  if (check_layer(layer, false) != FMOE_OK) return 0;
+  return ws_layout(layer->hidden, layer->inter, layer->has_shared, T > L ? T : L, K, L).bytes;
+}
+
+fmoe_status fmoe_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (ws == nullptr || !aligned(ws, 256) || bytes == 0) return FMOE_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+fmoe_status fmoe_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, void* stream) {
+  if (!vec_ok(logits) || ids == nullptr || weights == nullptr) return FMOE_ERR_INVALID_ARG;
+  if (!aligned(ids, 4) || !aligned(weights, 4)) return FMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > FMOE_MAX_TOKENS || E < 1 || E > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
+  if (K < 1 || K > E || K > FMOE_MAX_TOPK) return FMOE_ERR_INVALID_ARG;
+  return from_cuda(launch_route(logits, T, E, K, ids, weights, nullptr, nullptr, 0, nullptr,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+fmoe_status fmoe_expert_ffn(const fmoe_layer* layer, const int32_t* ids, int T, int K, const float* x, float* y,
+                            void* ws, void* stream) {
+  fmoe_status s = check_layer(layer, true);
+  if (s != FMOE_OK) return s;
+  if (T < 1 || T > FMOE_MAX_TOKENS || K < 1 || K > FMOE_MAX_TOPK || K > layer->n_experts)
+    return FMOE_ERR_INVALID_ARG;
+  if (ids == nullptr || !aligned(ids, 4) || !vec_ok(x) || !vec_ok(y) || ws == nullptr || !aligned(ws, 256))
+    return FMOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ws w = carve(ws, layer, T, K, 1);
+  GenericArgs a = generic_args(layer, T, K, w);
+  a.ids = ids;
+  a.x = x;
+  cudaError_t e = launch_gateup_generic(a, st);
+  if (e == cudaSuccess) e = launch_down_y(a, y, st);
+  return from_cuda(e);
+}
+
+fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float* router_logits,
+                           const float* residual, float* out, int T, int K, void* ws, void* stream) {
+  fmoe_status s = check_layer(layer, true);
+  if (s != FMOE_OK) return s;
+  if (T < 1 || T > FMOE_MAX_TOKENS || K < 1 || K > FMOE_MAX_TOPK || K > layer->n_experts)
+    return FMOE_ERR_INVALID_ARG;
+  if (!vec_ok(x) || !vec_ok(router_logits) || !vec_ok(residual) || !vec_ok(out) || ws == nullptr ||
+      !aligned(ws, 256))
+    return FMOE_ERR_INVALID_ARG;
+  const size_t H = layer->hidden;
+  // out may alias residual but must not overlap x or the logits
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    return pa < pb + nb && pb < pa + na;
+  };
+  if (overlap(out, T * H * 4, x, T * H * 4) ||
+      overlap(out, T * H * 4, router_logits, (size_t)T * layer->n_experts * 4))
+    return FMOE_ERR_INVALID_ARG;
+  if (out != residual && overlap(out, T * H * 4, residual, T * H * 4)) return FMOE_ERR_INVALID_ARG;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ws w = carve(ws, layer, T, K, 1);
+  const int S = layer->has_shared;
+
+  if (T == 1) {
+    FusedPlan pl = fused_plan(layer->bits, layer->hidden, layer->inter, K, S, current_device());
+    if (pl.ok) {
+      FusedParams p{};
+      p.bits = layer->bits;
+      p.H = layer->hidden;
+      p.I = layer->inter;
+      p.E = layer->n_experts;
+      p.K = K;
+      p.S = S;
+      p.L = 1;
+      p.norm = 0;
+      p.eps = 0.f;
+      p.lay = blob_layout(layer->bits, layer->hidden, layer->inter);
+      p.blob = p.lay.bytes;
+      p.x = x;
+      p.residual = residual;
+      p.out = out;
+      p.logits = router_logits;
+      p.hmid = w.h();
+      p.hbuf = w.hbuf();
+      p.ids_out = w.ids();
+      p.w_out = w.weights();
+      p.gate_out = w.gate();
+      p.counters = w.counters();
+      p.err = w.err();
+      p.timeout_ns = kTimeoutNs;
+      p.copy_back = 0;
+      p.layer[0].experts = static_cast<const uint8_t*>(layer->experts);
+      p.layer[0].shared = static_cast<const uint8_t*>(layer->shared);
+      p.layer[0].wsg = layer->shared_gate_w;
+      return from_cuda(launch_fused(p, pl, st));
+    }
+  }
+  // general path: route (+ gate), gate/up + SwiGLU, down + combine
+  GenericArgs a = generic_args(layer, T, K, w);
+  a.ids = w.ids();
+  a.weights = w.weights();
+  a.gate = w.gate();
+  a.x = x;
+  a.residual = residual;
+  a.out = out;
+  cudaError_t e = launch_route(router_logits, T, layer->n_experts, K, w.ids(), w.weights(),
+                               S ? layer->shared_gate_w : nullptr, x, layer->hidden, w.gate(), st);
+  if (e == cudaSuccess) e = launch_gateup_generic(a, st);
+  if (e == cudaSuccess) e = launch_down_combine(a, st);
+  return from_cuda(e);
+}
+
+fmoe_status fmoe_stack_decode(const fmoe_layer* layers, int L, const float* logits, float* h, int K, float eps,
+                              void* ws, void* stream) {
+  if (layers == nullptr || L < 1 || L > FMOE_MAX_LAYERS) return FMOE_ERR_INVALID_ARG;
+  fmoe_status s = check_layer(&layers[0], true);
+  if (s != FMOE_OK) return s;
+  for (int l = 1; l < L; ++l) {
+    s = check_layer(&layers[l], true);
+    if (s != FMOE_OK) return s;
+    if (layers[l].bits != layers[0].bits || layers[l].hidden != layers[0].hidden ||
+        layers[l].inter != layers[0].inter || layers[l].n_experts != layers[0].n_experts ||
+        layers[l].has_shared != layers[0].has_shared)
+      return FMOE_ERR_INVALID_ARG;
+  }
+  if (K < 1 || K > FMOE_MAX_TOPK || K > layers[0].n_experts) return FMOE_ERR_INVALID_ARG;
+  if (!vec_ok(logits) || !vec_ok(h) || ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
+  if (!(eps >= 0.f)) return FMOE_ERR_INVALID_ARG;
+  const fmoe_layer& L0 = layers[0];
+  const int S = L0.has_shared;
+  FusedPlan pl = fused_plan(L0.bits, L0.hidden, L0.inter, K, S, current_device());
+  if (!pl.ok) return FMOE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ws w = carve(ws, &L0, 1, K, L);
+  for (int l0 = 0; l0 < L; l0 += kMaxFusedLayers) {
+    const int n = (L - l0) < kMaxFusedLayers ? (L - l0) : kMaxFusedLayers;
+    FusedParams p{};
+    p.bits = L0.bits;
+    p.H = L0.hidden;
+    p.I = L0.inter;
+    p.E = L0.n_experts;
+    p.K = K;
+    p.S = S;
+    p.L = n;
+    p.norm = 1;
+    p.eps = eps;
+    p.lay = blob_layout(L0.bits, L0.hidden, L0.inter);
+    p.blob = p.lay.bytes;
+    p.x = nullptr;
+    p.residual = nullptr;
+    p.out = h;
+    p.logits = logits + (size_t)l0 * L0.n_experts;
+    p.hmid = w.h();
+    p.hbuf = w.hbuf();
+    p.ids_out = w.ids() + (size_t)l0 * K;
+    p.w_out = w.weights() + (size_t)l0 * K;
+    p.gate_out = w.gate() + l0;
+    p.counters = w.counters();
+    p.err = w.err();
+    p.timeout_ns = kTimeoutNs;
+    p.copy_back = (n == 1) ? 1 : 0;
+    for (int i = 0; i < n; ++i) {
+      p.layer[i].experts = static_cast<const uint8_t*>(layers[l0 + i].experts);
+      p.layer[i].shared = static_cast<const uint8_t*>(layers[l0 + i].shared);
+      p.layer[i].wsg = layers[l0 + i].shared_gate_w;
+    }
+    cudaError_t e = launch_fused(p, pl, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return FMOE_OK;
+}
+
+fmoe_status fmoe_ws_routing(void* ws, const fmoe_layer* layer, int T, int K, int32_t** ids, float** weights,
+                            float** gate, float** h) {
+  if (ws == nullptr || layer == nullptr || T < 1 || K < 1) return FMOE_ERR_INVALID_ARG;
+  if (check_layer(layer, false) != FMOE_OK) return FMOE_ERR_INVALID_ARG;
+  Ws w = carve(ws, layer, T, K, 1);
+  if (ids) *ids = w.ids();
+  if (weights) *weights = w.weights();
+  if (gate) *gate = w.gate();
+  if (h) *h = w.h();
+  return FMOE_OK;
+}
+
+const char* fmoe_status_string(fmoe_status s) {
+  switch (s) {
+    case FMOE_OK: return "ok";
+    case FMOE_ERR_INVALID_ARG: return "invalid argument";
+    case FMOE_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case FMOE_ERR_CUDA: return "CUDA launch or runtime error";
+    case FMOE_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+fmoe_status fmoe_last_device_error(void* ws, void* stream) {
+  if (ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (word != 0) {
+    e = cudaMemsetAsync(ws, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (word & (kErrWaitTimeout | kErrCopyTimeout)) return FMOE_ERR_TIMEOUT;
+  if (word & kErrBadExpert) return FMOE_ERR_INVALID_ARG;
+  return FMOE_OK;
+}
+
+fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected, int timeout_us, void* stream) {
+  if (ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
+  if (n_blocks < 1 || n_blocks > 148 * 4 || expected < 1 || timeout_us < 1 || timeout_us > 10 * 1000 * 1000)
+    return FMOE_ERR_INVALID_ARG;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(base);
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(base + 64);   // inside the 256-byte header
+  return from_cuda(launch_wait_test(ctr, err, n_blocks, expected, (unsigned long long)timeout_us * 1000ull,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+"""ctypes binding of libfmoe.so (argument marshalling only).
+
+Every step of the MoE block runs in the library's CUDA kernels; this module
+turns torch tensors into device pointers, passes the current CUDA stream and
+raises on a non-OK status.  There is no CPU fallback: if the library cannot
+be loaded, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfmoe.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+MAX_TOKENS, MAX_TOPK, MAX_EXPERTS, MAX_LAYERS = 16, 16, 1024, 1024
+
+
+class FmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class fmoe_layer(ctypes.Structure):
+    _fields_ = [
+        ("bits", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("hidden", ctypes.c_int32),
+        ("inter", ctypes.c_int32),
+        ("n_experts", ctypes.c_int32),
+        ("has_shared", ctypes.c_int32),
+        ("experts", ctypes.c_void_p),
+        ("shared", ctypes.c_void_p),
+        ("shared_gate_w", ctypes.c_void_p),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m quantized_moe_expert_05_b300.build` "
+            "(the library has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    LP = ctypes.POINTER(fmoe_layer)
+    sig = {
+        "fmoe_expert_bytes": (Z, [I, I, I, I]),
+        "fmoe_workspace_bytes": (Z, [LP, I, I, I]),
+        "fmoe_workspace_init": (I, [P, Z, P]),
+        "fmoe_route": (I, [P, I, I, I, P, P, P]),
+        "fmoe_expert_ffn": (I, [LP, P, I, I, P, P, P, P]),
+        "fmoe_moe_block": (I, [LP, P, P, P, P, I, I, P, P]),
+        "fmoe_stack_decode": (I, [LP, I, P, P, I, F, P, P]),
+        "fmoe_ws_routing": (I, [P, LP, I, I, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P),
+                                ctypes.POINTER(P)]),
+        "fmoe_status_string": (ctypes.c_char_p, [I]),
+        "fmoe_last_device_error": (I, [P, P]),
+        "fmoe_debug_wait_test": (I, [P, I, I, I, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.fmoe_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise FmoeError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def expert_bytes(bits: int, hidden: int, inter: int, group: int = 64) -> int:
+    return int(lib.fmoe_expert_bytes(bits, hidden, inter, group))
+
+
+@dataclass
+class Layer:
+    """One MoE layer: packed routed experts, optional shared expert and gate."""
+
+    bits: int
+    hidden: int
+    inter: int
+    n_experts: int
+    experts: torch.Tensor                      # flat int32/uint8 device tensor, E blobs
+    shared: Optional[torch.Tensor] = None      # one blob
+    shared_gate_w: Optional[torch.Tensor] = None  # int16/bfloat16 [H]
+
+    def c(self) -> fmoe_layer:
+        s = fmoe_layer()
+        s.bits, s.group, s.hidden, s.inter = self.bits, 64, self.hidden, self.inter
+        s.n_experts = self.n_experts
+        s.has_shared = 1 if self.shared is not None else 0
+        s.experts = _ptr(self.experts)
+        s.shared = _ptr(self.shared)
+        s.shared_gate_w = _ptr(self.shared_gate_w)
+        return s
+
+
+def workspace_bytes(layer: Layer, T: int, K: int, L: int = 1) -> int:
+    n = int(lib.fmoe_workspace_bytes(ctypes.byref(layer.c()), T, K, L))
+    if n == 0:
+        raise FmoeError(ERR_INVALID_ARG, "fmoe_workspace_bytes")
+    return n
+
+
+def new_workspace(layer: Layer, T: int, K: int, L: int = 1, device=None, stream=None) -> torch.Tensor:
+    """Allocate (through torch) and zero a workspace for the given sizes."""
+    n = workspace_bytes(layer, T, K, L)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or layer.experts.device)
+    _check(lib.fmoe_workspace_init(_ptr(ws), n, _stream(stream)), "fmoe_workspace_init")
+    return ws
+
+
+def route(logits: torch.Tensor, K: int, ids: Optional[torch.Tensor] = None,
+          weights: Optional[torch.Tensor] = None, stream=None):
+    T, E = logits.shape
+    if ids is None:
+        ids = torch.empty((T, K), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    _check(lib.fmoe_route(_ptr(logits), T, E, K, _ptr(ids), _ptr(weights), _stream(stream)), "fmoe_route")
+    return ids, weights
+
+
+def expert_ffn(layer: Layer, ids: torch.Tensor, x: torch.Tensor, ws: torch.Tensor,
+               y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    T, K = ids.shape
+    S = 1 if layer.shared is not None else 0
+    if y is None:
+        y = torch.empty((T, K + S, layer.hidden), dtype=torch.float32, device=x.device)
+    _check(lib.fmoe_expert_ffn(ctypes.byref(layer.c()), _ptr(ids), T, K, _ptr(x), _ptr(y), _ptr(ws),
+                               _stream(stream)), "fmoe_expert_ffn")
+    return y
+
+
+def moe_block(layer: Layer, x: torch.Tensor, logits: torch.Tensor, residual: torch.Tensor, K: int,
+              ws: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty_like(residual)
+    _check(lib.fmoe_moe_block(ctypes.byref(layer.c()), _ptr(x), _ptr(logits), _ptr(residual), _ptr(out), T, K,
+                              _ptr(ws), _stream(stream)), "fmoe_moe_block")
+    return out
+
+
+def stack_decode(layers: Sequence[Layer], logits: torch.Tensor, h: torch.Tensor, K: int, eps: float,
+                 ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """In place: h <- h + MoE_l(RMSNorm(h)) for every layer."""
+    arr = (fmoe_layer * len(layers))(*[l.c() for l in layers])
+    _check(lib.fmoe_stack_decode(arr, len(layers), _ptr(logits), _ptr(h), K, float(eps), _ptr(ws),
+                                 _stream(stream)), "fmoe_stack_decode")
+    return h
+
+
+def ws_routing(ws: torch.Tensor, layer: Layer, T: int, K: int) -> dict:
+    """Views of the routing result and h left in a workspace by moe_block."""
+    P = ctypes.c_void_p
+    ids, w, g, h = P(), P(), P(), P()
+    _check(lib.fmoe_ws_routing(_ptr(ws), ctypes.byref(layer.c()), T, K, ctypes.byref(ids), ctypes.byref(w),
+                               ctypes.byref(g), ctypes.byref(h)), "fmoe_ws_routing")
+    base = ws.data_ptr()
+    S = 1 if layer.shared is not None else 0
+
+    def view(p, dtype, n):
+        off = p.value - base
+        return ws[off: off + 4 * n].view(dtype)
+
+    return {
+        "ids": view(ids, torch.int32, T * K).view(T, K),
+        "weights": view(w, torch.float32, T * K).view(T, K),
+        "gate": view(g, torch.float32, T),
+        "h": view(h, torch.float32, T * (K + S) * layer.inter).view(T, K + S, layer.inter),
+    }
+
+
+def last_device_error(ws: torch.Tensor, stream=None) -> int:
+    return int(lib.fmoe_last_device_error(_ptr(ws), _stream(stream)))
+
+
+def debug_wait_test(ws: torch.Tensor, n_blocks: int, expected: int, timeout_us: int, stream=None) -> None:
+    _check(lib.fmoe_debug_wait_test(_ptr(ws), n_blocks, expected, timeout_us, _stream(stream)),
+           "fmoe_debug_wait_test")

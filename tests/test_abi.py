@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every declared symbol (no GPU needed).
+
+Only host-side calls run here: sizes, status strings and argument checks that
+return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_moe_expert_05_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fm():
+    build.build()
+    from quantized_moe_expert_05_b300 import fmoe
+    return fmoe
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fmoe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(fm):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(fm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/fmoe.h but not exported"
+
+
+def test_library_is_sm103a_build():
+    # the build flags name the B300 architecture only
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.NVCC_FLAGS)
+
+
+@pytest.mark.parametrize("bits,H,I", [(4, 512, 128), (4, 4096, 1024), (2, 4096, 1024), (4, 2048, 512),
+                                      (2, 192, 320), (4, 64, 64)])
+def test_expert_bytes_matches_oracle_layout(fm, bits, H, I):
+    assert fm.expert_bytes(bits, H, I) == oracle.layout(bits, H, I)[1]
+
+
+def test_expert_bytes_rejects_bad_shapes(fm):
+    assert fm.expert_bytes(3, 512, 128) == 0
+    assert fm.expert_bytes(4, 500, 128) == 0
+    assert fm.expert_bytes(4, 512, 128, group=32) == 0
+
+
+def test_status_strings(fm):
+    for s in range(5):
+        assert fm.status_string(s)
+    assert fm.status_string(fm.ERR_TIMEOUT) == "device-side wait timed out"
+
+
+def test_argument_checks_before_any_launch(fm):
+    lib = fm.lib
+    L = fm.fmoe_layer()
+    L.bits, L.group, L.hidden, L.inter, L.n_experts, L.has_shared = 4, 64, 512, 128, 8, 0
+    L.experts = None
+    assert lib.fmoe_moe_block(ctypes.byref(L), None, None, None, None, 1, 2, None, None) == fm.ERR_INVALID_ARG
+    L.experts = 4096 * 16
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 16, 1, 2, None, None) == fm.ERR_INVALID_ARG
+    L.bits = 3
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 32, 1, 2, 256, None) == fm.ERR_UNSUPPORTED
+    L.bits, L.group = 4, 32
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 32, 1, 2, 256, None) == fm.ERR_UNSUPPORTED
+    L.group = 64
+    # K > E, T > 16, misaligned workspace
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 4096, 1, 9, 256, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 4096, 17, 2, 256, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_moe_block(ctypes.byref(L), 16, 16, 16, 4096, 1, 2, 128, None) == fm.ERR_INVALID_ARG
+    # out overlapping x
+    assert lib.fmoe_moe_block(ctypes.byref(L), 4096, 1 << 20, 1 << 21, 4096 + 512, 1, 2, 256,
+                              None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_route(None, 1, 8, 2, 16, 16, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_route(16, 1, 8, 9, 16, 16, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_route(16, 1, 2000, 2, 16, 16, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_stack_decode(None, 1, 16, 16, 2, 1e-6, 256, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_debug_wait_test(256, 0, 1, 10, None) == fm.ERR_INVALID_ARG
+
+
+def test_workspace_bytes(fm):
+    L = fm.fmoe_layer()
+    L.bits, L.group, L.hidden, L.inter, L.n_experts, L.has_shared = 4, 64, 4096, 1024, 512, 1
+    a = fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 1, 4, 1)
+    b = fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 16, 4, 1)
+    c = fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 1, 4, 64)
+    assert 0 < a < b and a < c and a % 256 == 0
+    # h for T tokens x (K+1) slots x I floats fits
+    assert b >= 16 * 5 * 1024 * 4
+    assert fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 0, 4, 1) == 0

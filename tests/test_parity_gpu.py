@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Workloads: the tiny block (H 512, 8 experts, top-2), the Qwen-shaped block
+(H 4096, 512 experts, top-4 + shared, I 1024) in 4-bit and 2-bit, the same
+block at batch 1..16 with Zipf(1.1) routing, and the 48-layer stack (H 2048,
+512 experts, top-10, I 512).  Expert ids must match exactly; outputs within
+max relative error 2e-3 (both the max-normalised and the elementwise form).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from fmoe_testlib import TOL, assert_close, gpu_pool, make_layer, oracle_block, oracle_expert, rel_errors
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU only with -m gpu
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module")
+def fm():
+    from quantized_moe_expert_05_b300 import build
+    build.build()
+    from quantized_moe_expert_05_b300 import fmoe
+    return fmoe
+
+
+def run_block(fm, layer, shape, inp, K, ws):
+    x = inp.x.cuda()
+    lg = inp.logits.cuda()
+    res = inp.residual.cuda()
+    out = fm.moe_block(layer, x, lg, res, K, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    return out.cpu().numpy()
+
+
+def check_block(fm, layer, shape, inp, K, ws, shared_index=0):
+    got = run_block(fm, layer, shape, inp, K, ws)
+    T = inp.x.shape[0]
+    ref = oracle_block(shape, 0, inp.x.numpy(), inp.logits.numpy(), inp.residual.numpy(), K, shared_index)
+    info = fm.ws_routing(ws, layer, T, K)
+    ids = info["ids"].cpu().numpy()
+    assert np.array_equal(ids, ref["ids"]), (ids, ref["ids"])
+    assert_close(info["weights"].cpu().numpy(), ref["weights"], what="routing weights")
+    if ref["gate"] is not None:
+        assert_close(info["gate"].cpu().numpy(), ref["gate"], what="shared gate")
+    errs = [assert_close(got[t], ref["out"][t], what=f"out token {t}") for t in range(T)]
+    return max(e[0] for e in errs)
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("E,K", [(8, 2), (8, 8), (5, 3), (33, 1), (512, 4), (512, 10), (1000, 16), (1024, 16)])
+def test_route_matches_oracle(fm, E, K):
+    g = torch.Generator().manual_seed(E * 100 + K)
+    cases = [torch.randn((16, E), generator=g),
+             torch.randint(-3, 4, (16, E), generator=g).float()]          # many ties
+    z = torch.zeros((3, E))
+    z[0, ::2] = -0.0
+    z[1, : E // 2] = -0.0
+    cases.append(z)                                                        # -0 == +0
+    for lg in cases:
+        ids, w = fm.route(lg.cuda(), K)
+        torch.cuda.synchronize()
+        for t in range(lg.shape[0]):
+            rid, rw = oracle.route(lg[t].numpy(), K)
+            assert ids[t].cpu().tolist() == rid.tolist(), (t, lg[t])
+            assert_close(w[t].cpu().numpy(), rw, what="weights")
+
+
+# ---------------------------------------------------------------------------
+# tiny block (every output, several draws, fused single-launch path)
+# ---------------------------------------------------------------------------
+def test_tiny_block_all_outputs(fm):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 16, shape.top_k)
+    for tag in range(6):
+        inp = synth.block_inputs(shape, 1, tag=tag)
+        check_block(fm, layer, shape, inp, shape.top_k, ws)
+
+
+@pytest.mark.parametrize("K", [1, 2, 8])
+def test_tiny_block_k_extremes(fm, K):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 16, K)
+    for T in (1, 3, 16):
+        inp = synth.block_inputs(shape, T, tag=7 + T)
+        check_block(fm, layer, shape, inp, K, ws)
+
+
+def test_tiny_block_ties_and_signed_zero(fm):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 1, 2)
+    inp = synth.block_inputs(shape, 1, tag=20)
+    inp.logits[:] = torch.tensor([[0.5, -0.0, 0.5, 0.0, 0.5, -1.0, 0.25, 0.5]])
+    check_block(fm, layer, shape, inp, 2, ws)
+    inp.logits[:] = torch.tensor([[-0.0, -1.0, 0.0, -2.0, -0.0, -3.0, -1.0, -0.0]])
+    check_block(fm, layer, shape, inp, 2, ws)
+
+
+def test_expert_ffn_tiny_and_qwen(fm):
+    for shape, T, K in ((synth.TINY, 3, 2), (synth.QWEN_Q4, 2, 4)):
+        layer = make_layer(fm, shape)
+        ws = fm.new_workspace(layer, T, K)
+        g = torch.Generator().manual_seed(5)
+        ids = torch.stack([torch.randperm(shape.n_experts, generator=g)[:K] for _ in range(T)]).int()
+        x = synth.normal(shape.seed, 77, (T, shape.hidden))
+        y = fm.expert_ffn(layer, ids.cuda(), x.cuda(), ws)
+        torch.cuda.synchronize()
+        assert fm.last_device_error(ws) == fm.OK
+        y = y.cpu().numpy()
+        for t in range(T):
+            for k in range(K):
+                ref = oracle.expert_ffn(oracle_expert(shape, 0, int(ids[t, k])), x[t].numpy())
+                assert_close(y[t, k], ref, what=f"y[{t},{k}]")
+            if shape.has_shared:
+                ref = oracle.expert_ffn(oracle_expert(shape, 0, shape.n_experts), x[t].numpy())
+                assert_close(y[t, K], ref, what=f"shared y[{t}]")
+
+
+def test_expert_ffn_bad_id_is_reported_not_faulted(fm):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 1, 2)
+    ids = torch.tensor([[1, 99]], dtype=torch.int32, device="cuda")
+    x = synth.normal(0, 5, (1, shape.hidden)).cuda()
+    y = fm.expert_ffn(layer, ids, x, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.ERR_INVALID_ARG
+    assert torch.all(y[0, 1] == 0)
+    # the context is still usable and the error word was cleared
+    y = fm.expert_ffn(layer, ids[:, :1].contiguous(), x, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+
+
+def test_zero_weight_invariance_on_gpu(fm):
+    shape = synth.TINY
+    pool = gpu_pool(shape, 0, shape.n_experts)
+    layer = make_layer(fm, shape, pool=pool)
+    ws = fm.new_workspace(layer, 1, 3)
+    inp = synth.block_inputs(shape, 1, tag=30)
+    inp.logits[0] = torch.tensor([1.0, 0.5, 1.0 - 1e4, -2e4, -2e4, -2e4, -2e4, -2e4])
+    a = run_block(fm, layer, shape, inp, 3, ws)
+    nw = pool.numel() // shape.n_experts
+    pool2 = pool.clone()
+    pool2[2 * nw:3 * nw] = torch.randint(-2 ** 31, 2 ** 31 - 1, (nw,), dtype=torch.int32, device="cuda") & 0x0F0F0F0F
+    b = run_block(fm, make_layer(fm, shape, pool=pool2), shape, inp, 3, ws)
+    assert np.array_equal(a, b)
+
+
+def test_out_aliases_residual(fm):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 1, 2)
+    inp = synth.block_inputs(shape, 1, tag=40)
+    ref = oracle_block(shape, 0, inp.x.numpy(), inp.logits.numpy(), inp.residual.numpy(), 2)
+    res = inp.residual.cuda()
+    fm.moe_block(layer, inp.x.cuda(), inp.logits.cuda(), res, 2, ws, out=res)
+    torch.cuda.synchronize()
+    assert_close(res.cpu().numpy()[0], ref["out"][0], what="in-place out")
+
+
+def test_ragged_shape_general_path(fm):
+    # H and I that are not powers of two: 6 and 10 lane slices per row
+    shape = synth.BlockShape("ragged_h192_e6_top3_i320_q4", 192, 320, 6, 3, True, 4,
+                             0.002, 0.02, -0.1, 0.0, seed=11)
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 5, 3)
+    for T in (1, 5):
+        check_block(fm, layer, shape, synth.block_inputs(shape, T, tag=T), 3, ws)
+    shape2 = synth.BlockShape("ragged_h192_e6_top3_i320_q2", 192, 320, 6, 3, True, 2,
+                              0.01, 0.05, -0.1, 0.0, seed=12)
+    layer2 = make_layer(fm, shape2)
+    check_block(fm, layer2, shape2, synth.block_inputs(shape2, 2, tag=1), 3, ws)
+
+
+# ---------------------------------------------------------------------------
+# Qwen-shaped block, 4-bit and 2-bit, full size
+# ---------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def qwen_pools():
+    return {s.name: gpu_pool(s, 0, s.n_experts) for s in (synth.QWEN_Q4, synth.QWEN_Q2)}
+
+
+@pytest.mark.parametrize("shape", [synth.QWEN_Q4, synth.QWEN_Q2], ids=lambda s: s.name)
+def test_qwen_block_batch1(fm, qwen_pools, shape):
+    layer = make_layer(fm, shape, pool=qwen_pools[shape.name])
+    ws = fm.new_workspace(layer, 1, 4)
+    worst = 0.0
+    for tag in range(3):
+        worst = max(worst, check_block(fm, layer, shape, synth.block_inputs(shape, 1, tag=tag), 4, ws))
+    print(f"{shape.name}: worst max-rel err {worst:.2e}")
+
+
+def test_qwen_block_graph_replay_matches_eager(fm, qwen_pools):
+    shape = synth.QWEN_Q4
+    layer = make_layer(fm, shape, pool=qwen_pools[shape.name])
+    ws = fm.new_workspace(layer, 1, 4)
+    inp = synth.block_inputs(shape, 1, tag=5)
+    x, lg, res = inp.x.cuda(), inp.logits.cuda(), inp.residual.cuda()
+    eager = fm.moe_block(layer, x, lg, res, 4, ws).clone()
+    out = torch.empty_like(res)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fm.moe_block(layer, x, lg, res, 4, ws, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fm.moe_block(layer, x, lg, res, 4, ws, out=out)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
+# ---------------------------------------------------------------------------
+# batch 1..16 with Zipf routing (unique experts read once)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16])
+def test_qwen_batch_zipf(fm, qwen_pools, T):
+    shape = synth.QWEN_Q4_BATCH
+    layer = make_layer(fm, shape, pool=_zipf_pool(shape))
+    ws = fm.new_workspace(layer, 16, 4)
+    check_block(fm, layer, shape, synth.block_inputs(shape, T, tag=T), 4, ws)
+
+
+_ZP = {}
+
+
+def _zipf_pool(shape):
+    if shape.name not in _ZP:
+        _ZP[shape.name] = gpu_pool(shape, 0, shape.n_experts)
+    return _ZP[shape.name]
+
+
+# ---------------------------------------------------------------------------
+# stacks
+# ---------------------------------------------------------------------------
+def _oracle_stack(shape, h0, logits, K, shared=False):
+    return oracle.stack_decode(lambda l, e: oracle_expert(shape, l, e), h0, logits, K, shape.eps,
+                               (lambda l: oracle_expert(shape, l, shape.n_experts)) if shared else None,
+                               (lambda l: synth.shared_gate_vector(shape, l).numpy().view(np.uint16))
+                               if shared else None)
+
+
+@pytest.mark.parametrize("L", [1, 2, 5, 70])
+def test_tiny_stack(fm, L):
+    shape = synth.BlockShape("tiny_stack", 512, 128, 8, 2, True, 4, 0.002, 0.02, -0.1, 0.0, seed=21,
+                             n_layers=L)
+    layers = [make_layer(fm, shape, layer=l) for l in range(L)]
+    ws = fm.new_workspace(layers[0], 1, 2, L)
+    h0, logits = synth.stack_inputs(shape, 1)
+    h = h0[0].clone().cuda()
+    fm.stack_decode(layers, logits[0].cuda(), h, 2, shape.eps, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    ref, _ = _oracle_stack(shape, h0[0].numpy(), logits[0].numpy(), 2, shared=True)
+    assert_close(h.cpu().numpy(), ref, what=f"tiny stack L={L}")
+
+
+@pytest.fixture(scope="module")
+def stack48_layers(fm):
+    shape = synth.STACK48
+    return [make_layer(fm, shape, layer=l) for l in range(shape.n_layers)]
+
+
+def test_stack48_tokens(fm, stack48_layers):
+    shape = synth.STACK48
+    ws = fm.new_workspace(stack48_layers[0], 1, shape.top_k, shape.n_layers)
+    h0, logits = synth.stack_inputs(shape, 1)
+    for t in range(1):
+        h = h0[t].clone().cuda()
+        fm.stack_decode(stack48_layers, logits[t].cuda(), h, shape.top_k, shape.eps, ws)
+        torch.cuda.synchronize()
+        assert fm.last_device_error(ws) == fm.OK
+        ref, ids = _oracle_stack(shape, h0[t].numpy(), logits[t].numpy(), shape.top_k)
+        assert_close(h.cpu().numpy(), ref, what=f"stack48 token {t}")
+
+
+def test_generator_cpu_gpu_identical():
+    for shape, e in ((synth.QWEN_Q4, 7), (synth.QWEN_Q2, 300), (synth.STACK48, 511)):
+        a = synth.expert_blob(shape, 3, e, device="cpu")
+        b = synth.expert_blob(shape, 3, e, device="cuda").cpu()
+        assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# bounded device-side waits
+# ---------------------------------------------------------------------------
+def test_bounded_wait_times_out_and_reports(fm):
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 1, 2)
+    fm.debug_wait_test(ws, 8, 8, 1_000_000)          # all arrive: completes
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    fm.debug_wait_test(ws, 4, 5, 20_000)             # one arrival short: 20 ms time-out
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.ERR_TIMEOUT
+    assert fm.last_device_error(ws) == fm.OK         # cleared
+    # the context stays usable
+    check_block(fm, layer, shape, synth.block_inputs(shape, 1, tag=3), 2, fm.new_workspace(layer, 1, 2))
