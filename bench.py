@@ -87,55 +87,83 @@ def workload_name(shape, n_layers):
 # clocks sampled during the timed region (NVML, 5 ms period)
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """SM clock and clock-event reasons sampled while the timed region runs:
+    NVML every 5 ms when pynvml imports, else `nvidia-smi -lms 20`."""
+
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
         0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
 
-    def __init__(self, device_index):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
+    def __init__(self, local_index):
+        self.samples, self.reasons, self.max_mhz, self.source = [], set(), None, None
         self._stop = threading.Event()
-        self._ok = False
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        self.index = int(ids[local_index]) if len(ids) > local_index and ids[local_index].isdigit() else local_index
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._ok = True
-        except Exception as e:  # noqa: BLE001
-            self.error = str(e)
+            self.source = "nvml"
+        except Exception:  # noqa: BLE001
+            self.source = "nvidia-smi"
 
-    def _run(self):
+    def _add_mask(self, mask):
+        for bit, name in self.REASONS.items():
+            if mask & bit:
+                self.reasons.add(name)
+
+    def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for bit, name in self.REASONS.items():
-                    if mask & bit:
-                        self.reasons.add(name)
+                self._add_mask(nv.nvmlDeviceGetCurrentClocksEventReasons(self._h))
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(0.005)
 
     def __enter__(self):
-        if self._ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self.source == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        else:
+            import subprocess
+            try:
+                self._p = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.05)
+            except Exception:  # noqa: BLE001
+                self._p = None
         return self
 
     def __exit__(self, *a):
-        if self._ok:
+        if self.source == "nvml":
             self._stop.set()
             self._t.join()
+        elif getattr(self, "_p", None) is not None:
+            self._p.terminate()
+            out, _ = self._p.communicate(timeout=10)
+            for line in out.splitlines():
+                f = [v.strip() for v in line.split(",")]
+                if len(f) >= 3 and f[0].isdigit():
+                    self.samples.append(int(f[0]))
+                    self.max_mhz = int(f[1]) if f[1].isdigit() else self.max_mhz
+                    try:
+                        self._add_mask(int(f[2], 16))
+                    except ValueError:
+                        pass
 
     def summary(self):
-        if not self._ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "error", "")}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "source": self.source,
                 "reasons": sorted(self.reasons - {"gpu_idle"})}
 
 

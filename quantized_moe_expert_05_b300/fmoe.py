@@ -142,6 +142,8 @@ def new_workspace(layer: Layer, T: int, K: int, L: int = 1, device=None, stream=
 def route(logits: torch.Tensor, K: int, ids: Optional[torch.Tensor] = None,
           weights: Optional[torch.Tensor] = None, stream=None):
     T, E = logits.shape
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
     if ids is None:
         ids = torch.empty((T, K), dtype=torch.int32, device=logits.device)
     if weights is None:
@@ -164,6 +166,8 @@ def expert_ffn(layer: Layer, ids: torch.Tensor, x: torch.Tensor, ws: torch.Tenso
 def moe_block(layer: Layer, x: torch.Tensor, logits: torch.Tensor, residual: torch.Tensor, K: int,
               ws: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     T = x.shape[0]
+    if x.shape != (T, layer.hidden) or logits.shape != (T, layer.n_experts) or residual.shape != x.shape:
+        raise ValueError("x, residual must be [T][H] and logits [T][E]")
     if out is None:
         out = torch.empty_like(residual)
     _check(lib.fmoe_moe_block(ctypes.byref(layer.c()), _ptr(x), _ptr(logits), _ptr(residual), _ptr(out), T, K,
@@ -174,6 +178,8 @@ def moe_block(layer: Layer, x: torch.Tensor, logits: torch.Tensor, residual: tor
 def stack_decode(layers: Sequence[Layer], logits: torch.Tensor, h: torch.Tensor, K: int, eps: float,
                  ws: torch.Tensor, stream=None) -> torch.Tensor:
     """In place: h <- h + MoE_l(RMSNorm(h)) for every layer."""
+    if logits.numel() != len(layers) * layers[0].n_experts or h.numel() != layers[0].hidden:
+        raise ValueError("logits must be [L][E] and h [H]")
     arr = (fmoe_layer * len(layers))(*[l.c() for l in layers])
     _check(lib.fmoe_stack_decode(arr, len(layers), _ptr(logits), _ptr(h), K, float(eps), _ptr(ws),
                                  _stream(stream)), "fmoe_stack_decode")
