@@ -199,6 +199,49 @@ fmoe_status fmoe_last_device_error(void* ws, void* stream);
 fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected,
                                  int timeout_us, void* stream);
 
+/*
+ * Bytes of the library's own scratch array used by fmoe_moe_block_noalloc.
+ * Every GPU that loads the library holds this much device memory for it
+ * until the process exits.
+ */
+#define FMOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+/*
+ * fmoe_moe_block for one token (T = 1) without a caller workspace.
+ *
+ * The flash-moe write-ups have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory (code running inside an
+ * allocator or memory-pool callback, plugins whose host framework owns all
+ * device allocations, real-time loops that must not block in cudaMalloc).
+ * Instead of a workspace it uses a fixed array of FMOE_NOALLOC_SCRATCH_BYTES
+ * bytes that the library declares in device memory.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   layer, x, router_logits, residual, out, K
+ *                 as fmoe_moe_block with T = 1 (out may alias residual)
+ *   device_error  device pointer to one uint32, or NULL: after the block, the
+ *                 call copies the kernel's error word there (0 = no error;
+ *                 nonzero = a device-side wait timed out and `out` is not
+ *                 valid).  Written asynchronously on `stream`.
+ *
+ * Returns FMOE_ERR_INVALID_ARG (and enqueues nothing) for the argument
+ * errors of fmoe_moe_block and when the shape's scratch
+ * (fmoe_workspace_bytes(layer, 1, K, 1)) exceeds FMOE_NOALLOC_SCRATCH_BYTES;
+ * FMOE_ERR_UNSUPPORTED for shapes the single-launch kernel does not cover;
+ * FMOE_ERR_CUDA if the set-up or a launch fails.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the device current at the call); make that first call before any
+ * stream capture.  Every call on a device uses the same array, and each call
+ * clears its error word and counters first: calls that overlap on the GPU
+ * (other streams, or other host threads) race on it and must be serialised
+ * by the caller.  The routing result is not kept.
+ */
+fmoe_status fmoe_moe_block_noalloc(const fmoe_layer* layer /* host */, const float* x,
+                                   const float* router_logits, const float* residual,
+                                   float* out, int K, uint32_t* device_error,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

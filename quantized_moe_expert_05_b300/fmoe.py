@@ -62,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "fmoe_status_string": (ctypes.c_char_p, [I]),
         "fmoe_last_device_error": (I, [P, P]),
         "fmoe_debug_wait_test": (I, [P, I, I, I, P]),
+        "fmoe_moe_block_noalloc": (I, [LP, P, P, P, P, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,3 +215,21 @@ def last_device_error(ws: torch.Tensor, stream=None) -> int:
 def debug_wait_test(ws: torch.Tensor, n_blocks: int, expected: int, timeout_us: int, stream=None) -> None:
     _check(lib.fmoe_debug_wait_test(_ptr(ws), n_blocks, expected, timeout_us, _stream(stream)),
            "fmoe_debug_wait_test")
+
+
+NOALLOC_SCRATCH_BYTES = 256 * 1024
+
+
+def moe_block_noalloc(layer: Layer, x: torch.Tensor, logits: torch.Tensor, residual: torch.Tensor, K: int,
+                      out: Optional[torch.Tensor] = None, device_error: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """One token through fmoe_moe_block_noalloc (no workspace; the library's own
+    fixed device scratch).  For callers that cannot allocate device memory the
+    output (and the optional int32 error word) must be preallocated."""
+    if x.shape != (1, layer.hidden) or logits.shape != (1, layer.n_experts) or residual.shape != x.shape:
+        raise ValueError("x, residual must be [1][H] and logits [1][E]")
+    if out is None:
+        out = torch.empty_like(residual)
+    _check(lib.fmoe_moe_block_noalloc(ctypes.byref(layer.c()), _ptr(x), _ptr(logits), _ptr(residual), _ptr(out),
+                                      K, _ptr(device_error), _stream(stream)), "fmoe_moe_block_noalloc")
+    return out
