@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="fmoe", choices=["fmoe", "reference"])
     ap.add_argument("--workload", default="qwen_q4",
                     choices=["qwen_q4", "qwen_q2", "stack48", "tiny"])
+    ap.add_argument("--chain", type=int, default=CHAIN,
+                    help="blocks per step for the single-block workloads (1..64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="run only this many steps (for an ncu launch list); prints no JSON")
@@ -55,16 +57,18 @@ def parse():
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def workload_desc(name):
+def workload_desc(name, chain=CHAIN):
     import synth
+    if not 1 <= chain <= 64:
+        raise ValueError("--chain must be in 1..64")
     if name == "qwen_q4":
-        return synth.QWEN_Q4, CHAIN
+        return synth.QWEN_Q4, chain
     if name == "qwen_q2":
-        return synth.QWEN_Q2, CHAIN
+        return synth.QWEN_Q2, chain
     if name == "stack48":
         return synth.STACK48, synth.STACK48.n_layers
     if name == "tiny":
-        return synth.TINY, CHAIN
+        return synth.TINY, chain
     raise ValueError(name)
 
 
@@ -257,18 +261,15 @@ def run_reference(args):
         threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:  # noqa: BLE001
         threads = 1
-    shape, n_layers = workload_desc(args.workload)
+    shape, n_layers = workload_desc(args.workload, args.chain)
     inp = synth.block_inputs(shape, 1, tag=500)
     ids, _ = oracle.route(inp.logits[0].numpy(), shape.top_k)
     experts = [int(e) for e in ids] + ([shape.n_experts] if shape.has_shared else [])
     blobs = [synth.expert_blob(shape, 0, e).numpy().view(np.uint8) for e in experts]
     H, I, bits = shape.hidden, shape.inter, shape.bits
     x = inp.x[0].numpy().astype(np.float64)
-    planes, _ = oracle.layout(bits, H, I)
-
     def rows(blob, name, n):
-        off, r, wpr = planes[name]
-        return blob.view(np.uint32)[off // 4: off // 4 + n * wpr].reshape(n, wpr)
+        return oracle.part_rows(blob, bits, H, I, name, n)
 
     def one(i, frac):
         # the first frac of the rows of one expert's gate, up and down matrices
@@ -335,7 +336,7 @@ def main():
     from quantized_moe_expert_05_b300 import fmoe as fm
     import synth
 
-    shape, n_layers = workload_desc(args.workload)
+    shape, n_layers = workload_desc(args.workload, args.chain)
     K = shape.top_k
     S = 1 if shape.has_shared else 0
     nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4

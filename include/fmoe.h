@@ -31,18 +31,23 @@
  *     stay below 2^40 in magnitude (the dot products pre-scale x by powers of
  *     two; larger values overflow to inf).
  *
- * Packed expert blob (one per expert, contiguous, 256-byte aligned planes):
- *     gate_q  [I][H*bits/32] uint32   codes, code c at bits (c mod 32/bits)*bits
- *                                     of word c/(32/bits) (lowest bits first)
- *     gate_sb [I][H/64]      uint32   bits 0..15 scale (bf16), 16..31 bias (bf16)
- *     up_q    [I][H*bits/32] uint32
- *     up_sb   [I][H/64]      uint32
- *     down_q  [H][I*bits/32] uint32
- *     down_sb [H][I/64]      uint32
+ * Packed expert blob (one per expert, contiguous, 256-byte aligned):
+ *   gate/up records, r = 0..I-1, each padded to a multiple of 16 bytes:
+ *     gate_q  [H*bits/32] uint32   codes of gate row r; code c at bits
+ *                                  (c mod 32/bits)*bits of word c/(32/bits)
+ *                                  (lowest bits first)
+ *     up_q    [H*bits/32] uint32   codes of up row r
+ *     gate_sb [H/64]      uint32   bits 0..15 scale (bf16), 16..31 bias (bf16)
+ *     up_sb   [H/64]      uint32
+ *   down records, j = 0..H-1, from the next 256-byte boundary, each padded
+ *   to a multiple of 16 bytes:
+ *     down_q  [I*bits/32] uint32
+ *     down_sb [I/64]      uint32
  *   The dequantised weight of row r, column c is q * scale[r][c/64] +
  *   bias[r][c/64]; gate/up rows have H columns, down rows have I columns.
- *   Blob size: fmoe_expert_bytes(); the routed experts of a layer sit at
- *   stride fmoe_expert_bytes() from `experts`.
+ *   A range of rows of a matrix, with its scales, is one contiguous byte
+ *   range.  Blob size: fmoe_expert_bytes() (a multiple of 256); the routed
+ *   experts of a layer sit at stride fmoe_expert_bytes() from `experts`.
  */
 #ifndef FMOE_H
 #define FMOE_H

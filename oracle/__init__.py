@@ -33,6 +33,7 @@ docstring of each function for the pin that covers it.
 from .moe import (  # noqa: F401
     GROUP,
     layout,
+    part_rows,
     unpack_codes,
     bf16_to_f64,
     dequantize,

@@ -23,32 +23,35 @@ _ALIGN = 256        # every plane of a blob starts on a 256-byte boundary
 # packed expert blob
 # ---------------------------------------------------------------------------
 def layout(bits: int, hidden: int, inter: int) -> tuple:
-    """Byte offset, row count and 32-bit words per row of the six planes.
+    """Where the six parts of an expert blob live.
 
-    Order: gate codes, gate (scale,bias), up codes, up (scale,bias), down
-    codes, down (scale,bias).  Gate/up rows are the I intermediate rows of
-    H inputs; down rows are the H output rows of I inputs.  Returns
-    (dict name -> (offset, rows, words_per_row), blob_bytes).
+    Gate/up row r (r < I) is one record of gate codes, up codes, gate
+    (scale,bias) words and up (scale,bias) words, padded to a multiple of 16
+    bytes; the H down rows follow from the next 256-byte boundary, each a
+    record of down codes then down (scale,bias) words, padded to 16 bytes; the
+    blob is padded to a multiple of 256 bytes.  Returns
+    (dict name -> (offset of row 0, row stride, rows, 32-bit words per row),
+    blob_bytes), all in bytes except the word count.
     Pinned by the expert-size pin (6.75 MiB per 4-bit expert of the
     397B model, [FM] "SSD expert streaming").
     """
     if bits not in (2, 4):
         raise ValueError("bits must be 2 or 4")
     per_word = 32 // bits
-    planes = [
-        ("gate_q", inter, hidden // per_word),
-        ("gate_sb", inter, hidden // GROUP),
-        ("up_q", inter, hidden // per_word),
-        ("up_sb", inter, hidden // GROUP),
-        ("down_q", hidden, inter // per_word),
-        ("down_sb", hidden, inter // GROUP),
-    ]
-    out, pos = {}, 0
-    for name, rows, wpr in planes:
-        pos = -(-pos // _ALIGN) * _ALIGN
-        out[name] = (pos, rows, wpr)
-        pos += rows * wpr * 4
-    return out, -(-pos // _ALIGN) * _ALIGN
+    qh, sh = hidden // per_word * 4, hidden // GROUP * 4       # bytes of one gate/up row's parts
+    qi, si = inter // per_word * 4, inter // GROUP * 4         # bytes of one down row's parts
+    gu_stride = -(-(2 * qh + 2 * sh) // 16) * 16
+    d_stride = -(-(qi + si) // 16) * 16
+    d_base = -(-(inter * gu_stride) // _ALIGN) * _ALIGN
+    out = {
+        "gate_q": (0, gu_stride, inter, qh // 4),
+        "up_q": (qh, gu_stride, inter, qh // 4),
+        "gate_sb": (2 * qh, gu_stride, inter, sh // 4),
+        "up_sb": (2 * qh + sh, gu_stride, inter, sh // 4),
+        "down_q": (d_base, d_stride, hidden, qi // 4),
+        "down_sb": (d_base + qi, d_stride, hidden, si // 4),
+    }
+    return out, -(-(d_base + hidden * d_stride) // _ALIGN) * _ALIGN
 
 
 def unpack_codes(words: np.ndarray, bits: int) -> np.ndarray:
@@ -90,16 +93,22 @@ def dequantize(q_words: np.ndarray, sb_words: np.ndarray, bits: int) -> np.ndarr
     return q * s[..., g] + b[..., g]
 
 
-def expert_weights(blob: np.ndarray, bits: int, hidden: int, inter: int) -> tuple:
-    """(Wg [I][H], Wu [I][H], Wd [H][I]) dequantised from one blob (fp64)."""
+def part_rows(blob: np.ndarray, bits: int, hidden: int, inter: int, name: str, n=None) -> np.ndarray:
+    """The first n (default: all) rows of one part of a blob, uint32 [n][words per row]."""
     words = np.ascontiguousarray(blob).view(np.uint32).reshape(-1)
-    planes, nbytes = layout(bits, hidden, inter)
+    parts, nbytes = layout(bits, hidden, inter)
     if words.size * 4 < nbytes:
         raise ValueError("blob too small")
+    off, stride, rows, wpr = parts[name]
+    n = rows if n is None else n
+    return np.stack([words[(off + r * stride) // 4: (off + r * stride) // 4 + wpr] for r in range(n)])
+
+
+def expert_weights(blob: np.ndarray, bits: int, hidden: int, inter: int) -> tuple:
+    """(Wg [I][H], Wu [I][H], Wd [H][I]) dequantised from one blob (fp64)."""
 
     def plane(name):
-        off, rows, wpr = planes[name]
-        return words[off // 4: off // 4 + rows * wpr].reshape(rows, wpr)
+        return part_rows(blob, bits, hidden, inter, name)
 
     wg = dequantize(plane("gate_q"), plane("gate_sb"), bits)
     wu = dequantize(plane("up_q"), plane("up_sb"), bits)

@@ -44,12 +44,14 @@ struct Ws {
   WsLayout lay;
   uint8_t* base;
   uint32_t* err() const { return reinterpret_cast<uint32_t*>(base + lay.err); }
-  uint32_t* counters() const { return reinterpret_cast<uint32_t*>(base + lay.counters); }
+  uint32_t* exit_ctr() const { return reinterpret_cast<uint32_t*>(base + lay.exit_ctr); }
+  uint32_t* epoch() const { return reinterpret_cast<uint32_t*>(base + lay.epoch); }
+  unsigned long long* hll() const { return reinterpret_cast<unsigned long long*>(base + lay.hll); }
+  unsigned long long* hbufll() const { return reinterpret_cast<unsigned long long*>(base + lay.hbufll); }
   int32_t* ids() const { return reinterpret_cast<int32_t*>(base + lay.ids); }
   float* weights() const { return reinterpret_cast<float*>(base + lay.weights); }
   float* gate() const { return reinterpret_cast<float*>(base + lay.gate); }
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
-  float* hbuf() const { return reinterpret_cast<float*>(base + lay.hbuf); }
 };
 
 Ws carve(void* ws, const fmoe_layer* L, int T, int K, int n_layers) {
@@ -176,14 +178,15 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float*
       p.out = out;
       p.logits = router_logits;
       p.hmid = w.h();
-      p.hbuf = w.hbuf();
+      p.hll = w.hll();
+      p.hbufll = w.hbufll();
       p.ids_out = w.ids();
       p.w_out = w.weights();
       p.gate_out = w.gate();
-      p.counters = w.counters();
+      p.exit_ctr = w.exit_ctr();
+      p.epoch = w.epoch();
       p.err = w.err();
       p.timeout_ns = kTimeoutNs;
-      p.copy_back = 0;
       p.layer[0].experts = static_cast<const uint8_t*>(layer->experts);
       p.layer[0].shared = static_cast<const uint8_t*>(layer->shared);
       p.layer[0].wsg = layer->shared_gate_w;
@@ -246,14 +249,15 @@ fmoe_status fmoe_stack_decode(const fmoe_layer* layers, int L, const float* logi
     p.out = h;
     p.logits = logits + (size_t)l0 * L0.n_experts;
     p.hmid = w.h();
-    p.hbuf = w.hbuf();
+    p.hll = w.hll();
+    p.hbufll = w.hbufll();
     p.ids_out = w.ids() + (size_t)l0 * K;
     p.w_out = w.weights() + (size_t)l0 * K;
     p.gate_out = w.gate() + l0;
-    p.counters = w.counters();
+    p.exit_ctr = w.exit_ctr();
+    p.epoch = w.epoch();
     p.err = w.err();
     p.timeout_ns = kTimeoutNs;
-    p.copy_back = (n == 1) ? 1 : 0;
     for (int i = 0; i < n; ++i) {
       p.layer[i].experts = static_cast<const uint8_t*>(layers[l0 + i].experts);
       p.layer[i].shared = static_cast<const uint8_t*>(layers[l0 + i].shared);

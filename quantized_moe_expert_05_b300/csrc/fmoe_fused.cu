@@ -3,37 +3,46 @@
 // flash-moe (discuss.pytorch.kr write-up, "per-layer pipeline" and "deferred
 // CMD3") runs routing, the expert forward and the combine + residual + norm
 // per layer as GPU command buffers submitted without waiting; the slotstream
-// write-up (simpler24.com) measured batch-1 quantised matmuls at 20 % of
-// memory bandwidth because of dispatch cost.  Here one cooperative launch
-// (one 512-thread block per SM) runs, for each layer:
+// write-up (simpler24.com, "the disk was not the slow part") measured batch-1
+// quantised matmuls at 20 % of memory bandwidth because of dispatch cost.
+// Here one cooperative launch (one block per SM) runs every layer, with three
+// warp roles per block:
 //
-//   prologue   every block: RMSNorm statistics of the input (stacks), top-K +
-//              softmax of the router logits, sigmoid shared-expert gate, and
-//              its pre-scaled input slice in registers
-//   gate/up    block c owns intermediate rows [I*c/n, I*(c+1)/n) of every
-//              selected expert ("slot"); their packed rows stream from HBM into
-//              a shared-memory ring with bulk asynchronous copies (TMA engine,
-//              mbarrier completion); SwiGLU is applied in the epilogue and h
-//              goes to global memory (L2)
-//   down       block c owns output rows [H*c/n, H*(c+1)/n); their packed rows
-//              of every slot are copied into shared memory while gate/up runs.
-//              After a slot's h is complete device-wide (a per-slot counter,
-//              bounded wait) the block folds w_slot * (down_row . h_slot) into
-//              per-row accumulators, one slot behind the gate/up stream, so
-//              only the last slot's down work trails the last weight byte.
-//   combine    out[j] = residual[j] + sum over slots, written by the row's owner
+//   producer warp  issues bulk asynchronous copies (TMA engine, mbarrier
+//                  completion) of the block's packed rows: for every selected
+//                  expert ("slot") the gate/up rows [I*c/n, I*(c+1)/n) into a
+//                  shared-memory ring, and the down rows [H*c/n, H*(c+1)/n)
+//                  into a per-slot area.  The shared expert needs no routing,
+//                  so its rows are requested first; a routed slot's rows are
+//                  requested as soon as its id is known.
+//   final warp     turns the consumers' partial sums into h = silu(gate) * up
+//                  for the block's rows and publishes them to L2
+//   exchange warp  gathers each slot's full h from L2 into shared memory,
+//                  pre-scaled for the down projection
+//   16 consumer    route (each warp takes the top-K of its share of the
+//   warps          logits, one warp merges and publishes the ids one by one),
+//                  hold a pre-scaled slice of the input in registers, compute
+//                  dequantised gate/up dot products stage by stage (no block
+//                  barrier per stage: each warp releases a stage through an
+//                  mbarrier), and fold w_slot * (down_row . h_slot) into
+//                  per-row accumulators a slot or two behind the gate/up
+//                  stream; finally out[j] = residual[j] + sum over slots.
 //
-// Weight bytes of a layer are requested only after the previous layer's
-// output is complete (a device-wide counter), as a real decoder would have
-// to.  Every wait is bounded (%globaltimer) and records a time-out in the
-// workspace error word instead of hanging.
+// Blocks exchange data without counters or barriers: every value published
+// to another block (h rows, and the layer outputs of a stack) is stored as
+// one 64-bit (value, tag) word whose tag names the launch and layer, so a
+// reader knows a value is current from the load that fetches it (the
+// low-latency protocol idea of NCCL's LL transport).  A layer's routed
+// experts are requested only after routing on its complete input; the shared
+// expert, which needs no routing, may be requested as soon as this block has
+// finished the previous layer.  Every wait is bounded (%globaltimer); a wait
+// that runs out records the time-out in the workspace error word, and every
+// later wait of the block returns at once, so the launch always ends.
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
 
 namespace {
-
-constexpr int kCtrlBytes = 6144;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -41,6 +50,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -60,364 +73,666 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase; records a time-out and returns.
-__device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                          uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) {
-      atomicOr(err, kErrCopyTimeout);
-      return;
-    }
-  }
-}
-
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
-// A byte range rounded out to 16-byte boundaries for the bulk-copy engine.
-struct Span {
-  const uint8_t* src;   // 16-byte aligned start
-  uint32_t off;         // offset of the wanted bytes inside the copy
-  uint32_t len;         // multiple of 16
-};
-
-__device__ __forceinline__ Span span_of(const uint8_t* p, uint32_t bytes) {
-  Span s;
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)15;
-  s.src = reinterpret_cast<const uint8_t*>(a);
-  s.off = (uint32_t)(reinterpret_cast<uintptr_t>(p) - a);
-  s.len = (s.off + bytes + 15u) & ~15u;
-  return s;
+// Wait for an mbarrier phase, suspended (not spinning) for up to hint_ns.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
 }
 
-// Offset of the wanted bytes inside a rounded copy (consumer side).
-__device__ __forceinline__ uint32_t span_off(size_t byte_offset) { return (uint32_t)(byte_offset & 15); }
+// Bounded wait on an mbarrier phase.  The waiting warp sleeps in the
+// barrier unit rather than spinning, so it takes no issue slots from the
+// warps doing the arithmetic.  Returns false (and sets the abort flag and
+// the error word on a time-out) if the block has given up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
+                                          uint32_t* err, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 50000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      atomicOr(err, kErrCopyTimeout);
+      *abort = 1;
+      return false;
+    }
+  }
+}
 
-struct Geo {
-  int tl_gu, teams_gu, team, sl, wpt, wit, red_w;   // gate/up teams (one row per team)
-  int tl_d, teams_d, dteam, dsl;                     // down teams
-  int ra, nr, nch, ja, nd;                           // this block's rows
-  size_t qbh, sbbh, qbi, sbbi;                        // row bytes
-};
+// (value, tag) words: a float and the tag of the launch and layer that wrote
+// it, stored and loaded as one 64-bit access so that a reader sees either the
+// old pair or the new one, never a mix.
+__device__ __forceinline__ void ll_store(unsigned long long* p, float v, uint32_t tag) {
+  const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ll_load(const unsigned long long* p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
+__device__ __forceinline__ float ll_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ bool ll_is(unsigned long long w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+
+// Eight consecutive (value, tag) words (16-byte aligned) once all carry
+// `tag` (one thread, bounded wait).
+__device__ __forceinline__ void ll_wait8(const unsigned long long* p, uint32_t tag, float4& v0, float4& v1,
+                                         unsigned long long timeout_ns, uint32_t* err, volatile int* abort) {
+  uint64_t t0 = 0;
+  bool started = false;
+  while (true) {
+    unsigned long long w[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) ll_load2(p + i, w[i], w[i + 1]);
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ok = ok && ll_is(w[i], tag);
+    v0 = make_float4(ll_value(w[0]), ll_value(w[1]), ll_value(w[2]), ll_value(w[3]));
+    v1 = make_float4(ll_value(w[4]), ll_value(w[5]), ll_value(w[6]), ll_value(w[7]));
+    if (ok || *abort) return;
+    const uint64_t t = global_timer_ns();
+    if (!started) {
+      t0 = t;
+      started = true;
+    } else if (t - t0 > timeout_ns) {
+      atomicOr(err, kErrWaitTimeout);
+      *abort = 1;
+      return;
+    }
+    __nanosleep(32);
+  }
+}
+
+// 16-byte global -> shared copy that holds no registers (completion by
+// cp.async.wait_all).  Each 8-byte (value, tag) word of the pair is copied
+// whole: an aligned 16-byte read returns every 8-byte half as it was at one
+// time.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// named barrier over the consumer warps only
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Top-K key: larger key = larger logit, and among equal logits the lower
+// expert id (-0 and +0 compare equal).  Valid keys are never 0.
+__device__ __forceinline__ uint64_t route_key(float v, int id) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)id);
+}
+
+__device__ __forceinline__ float key_value(uint64_t k) {
+  const uint32_t ord = (uint32_t)(k >> 32);
+  const uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+  return __uint_as_float(b);
+}
+
+
+
+// Reduce four values over `width` consecutive lanes (a power of two, 4..32)
+// with a transposed butterfly: on return the group's lane 0 holds sum(a),
+// lane width/4 sum(b), lane width/2 sum(c) and lane 3*width/4 sum(d).
+__device__ __forceinline__ float quad_reduce(float a, float b, float c, float d, int width, int lane) {
+  const int half = width >> 1, quarter = width >> 2;
+  const bool lo = (lane & half) == 0;
+  const float s0 = __shfl_xor_sync(0xFFFFFFFFu, lo ? c : a, half);
+  const float s1 = __shfl_xor_sync(0xFFFFFFFFu, lo ? d : b, half);
+  const float x0 = (lo ? a : c) + s0;
+  const float x1 = (lo ? b : d) + s1;
+  const bool lq = (lane & quarter) == 0;
+  float y = (lq ? x0 : x1) + __shfl_xor_sync(0xFFFFFFFFu, lq ? x1 : x0, quarter);
+  for (int o = quarter >> 1; o >= 1; o >>= 1) y += __shfl_xor_sync(0xFFFFFFFFu, y, o);
+  return y;
+}
 
 }  // namespace
 
 template <int BITS>
-__global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __grid_constant__ FusedParams p) {
+__global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* mbar_ring = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* mbar_d = mbar_ring + kMaxStages;
-  int* s_ids = reinterpret_cast<int*>(mbar_d + kMaxSlots);
-  float* s_w = reinterpret_cast<float*>(s_ids + kMaxSlots);
-  float* s_red = s_w + kMaxSlots;            // 64 floats
-  float* s_part = s_red + 64;                // [2][32][2][8] floats
-  uint8_t* ring = smem + kCtrlBytes;
-  uint8_t* darea = ring + (size_t)p.nstage * p.stage_bytes;
+  const FusedPlan& pl = p.plan;
+  const BlobLayout& lay = p.lay;
+  // control area
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem);          // ring stage filled (count 1 + bytes)
+  uint64_t* bar_empty = bar_full + kMaxStages;                      // ring stage released (one per consumer warp)
+  uint64_t* bar_dfull = bar_empty + kMaxStages;                     // slot's down records filled
+  uint64_t* bar_routed = bar_dfull + kMaxSlots;                     // slot's expert id known
+  uint64_t* bar_slot = bar_routed + kMaxSlots;                      // slot's partial sums written
+  uint64_t* bar_hready = bar_slot + kMaxSlots;                      // slot's full h staged
+  uint64_t* bar_xready = bar_hready + kMaxSlots;                    // layer input complete (consumers)
+  int* s_ids = reinterpret_cast<int*>(smem + 832);                  // [kMaxSlots]
+  float* s_w = reinterpret_cast<float*>(smem + 960);                // [kMaxSlots] routing weights, shared gate
+  float* s_red = reinterpret_cast<float*>(smem + 1088);             // [kConsumerWarps][2]
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 1280);
+  float* s_part = reinterpret_cast<float*>(smem + pl.part_off);    // [slot][row][part][2]
+  unsigned long long* s_stage = reinterpret_cast<unsigned long long*>(smem + pl.stage_off);  // one slot's h words
+  uint8_t* s_hs = smem + pl.hs_off;                                // [slot] h slices + slice sums
+  float4* s_x4 = reinterpret_cast<float4*>(smem + pl.xs_off);      // layer input, slice-major
+  uint8_t* darea = smem + pl.darea_off;                            // [slot] down records
+  uint8_t* ring = smem + pl.ring_off;                              // [stage] gate/up records
 
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
+  const int warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, n = gridDim.x;
   const int NS = p.K + p.S;
   const int H = p.H, I = p.I;
 
-  Geo g;
-  g.tl_gu = H / kSlice;
-  g.teams_gu = kFusedThreads / g.tl_gu;
-  g.team = tid / g.tl_gu;
-  g.sl = tid % g.tl_gu;
-  g.wpt = g.tl_gu >= 32 ? g.tl_gu / 32 : 1;
-  g.wit = g.tl_gu >= 32 ? g.sl / 32 : 0;
-  g.red_w = g.tl_gu >= 32 ? 32 : g.tl_gu;
-  g.tl_d = I / kSlice;
-  g.teams_d = kFusedThreads / g.tl_d;
-  g.dteam = tid / g.tl_d;
-  g.dsl = tid % g.tl_d;
-  g.ra = (int)((long long)I * c / n);
-  g.nr = (int)((long long)I * (c + 1) / n) - g.ra;
-  g.nch = (g.nr + g.teams_gu - 1) / g.teams_gu;
-  g.ja = (int)((long long)H * c / n);
-  g.nd = (int)((long long)H * (c + 1) / n) - g.ja;
-  g.qbh = (size_t)H * BITS / 8;
-  g.sbbh = (size_t)H / kGroup * 4;
-  g.qbi = (size_t)I * BITS / 8;
-  g.sbbi = (size_t)I / kGroup * 4;
+  // Gate/up: this block owns rows [ra, ra+nr) of every slot.  The rows of
+  // all slots form one sequence of NS*nr "virtual rows" (slot-major) that
+  // the ring carries R at a time; a consumer warp handles rows rs0 and rs1
+  // of each stage (its slice range `sl` of H).
+  const int tl = H / kSlice;
+  const int R = pl.rows_per_stage;
+  const int nparts = pl.nparts;
+  const int gw = tl < 32 ? tl : 32;                                // reduction width
+  const int ra = (int)((long long)I * c / n);
+  const int nr = (int)((long long)I * (c + 1) / n) - ra;
+  const int V = NS * nr;
+  const int nstg = (V + R - 1) / R;
+  int rs0, sl, pi;
+  if (tl >= 32) {
+    rs0 = warp / nparts;
+    pi = warp % nparts;
+    sl = pi * 32 + lane;
+  } else {
+    rs0 = warp * (32 / tl) + lane / tl;
+    pi = 0;
+    sl = lane % tl;
+  }
+  const int rs1 = rs0 + R / 2;
+  // Down: this block owns output rows [ja, ja+nd); a row has tld slices;
+  // lpr lanes per row, rpp rows per warp pass.  Staged h: float4 j of slice
+  // s at j*(tld+1) + s (the padding keeps the exchanger's stores free of
+  // bank conflicts), then the tld slice sums.
+  const int ja = (int)((long long)H * c / n);
+  const int nd = (int)((long long)H * (c + 1) / n) - ja;
+  const int tld = I / kSlice;
+  const int hstride = tld + 1;
+  const int lpr = tld < 32 ? tld : 32;
+  const int rpp = 32 / lpr;
+  const int spl = tld > 32 ? tld / 32 : 1;
+  const int ngroups = (nd + rpp - 1) / rpp;
+  const int dlag = pl.dlag;
 
   if (tid == 0) {
-    for (int i = 0; i < kMaxStages; ++i) mbar_init(&mbar_ring[i], 1);
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&mbar_d[i], 1);
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kMaxSlots; ++i) {
+      mbar_init(&bar_dfull[i], 1);
+      mbar_init(&bar_routed[i], 1);
+      mbar_init(&bar_slot[i], kConsumerWarps);
+      mbar_init(&bar_hready[i], 1);
+    }
+    mbar_init(bar_xready, 1);
+    *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // producer state (meaningful in thread 0 only)
-  int pr_slot = 0, pr_chunk = 0;
-  bool pr_routed = false;
-  uint32_t g_issue = 0;
-  uint32_t g_cons = 0;          // GU chunks consumed (uniform over the block)
-
-  float accd[kMaxRowsPerTeam];
+  uint32_t g_issue = 0;   // gate/up stages issued (producer lane 0)
+  uint32_t g_cons = 0;    // gate/up stages consumed (consumer warps)
+  const unsigned long long tmo = p.timeout_ns;
+  // tags of this launch: layer l publishes with epoch * 64 + l + 1 (never 0,
+  // the value of a freshly zeroed workspace)
+  const uint32_t tag0 = *reinterpret_cast<volatile uint32_t*>(p.epoch) * (uint32_t)kMaxFusedLayers + 1u;
 
   for (int l = 0; l < p.L; ++l) {
     const FusedLayerPtrs lp = p.layer[l];
-    uint32_t* ctr = p.counters + (size_t)l * (NS + 1);
-
-    auto slot_blob = [&](int ps) -> const uint8_t* {
-      if (p.S && ps == 0) return lp.shared;
-      return lp.experts + (size_t)s_ids[ps] * p.blob;
-    };
+    const uint32_t lpar = (uint32_t)(l & 1);
+    const uint32_t tag = tag0 + (uint32_t)l;
+    // input: x (block), the stack input h (layer 0), or the previous layer's
+    // published output; residual likewise; output: out, or published words
+    const bool in_ll = p.norm && l > 0;
+    const bool out_ll = p.norm && l < p.L - 1;
+    const float* hin = p.norm ? p.out : p.x;
+    const unsigned long long* hin_ll = p.hbufll + (size_t)((l - 1) & 1) * H;
+    unsigned long long* out_llp = p.hbufll + (size_t)(l & 1) * H;
+    // slot ps: 0 is the shared expert when there is one; its h goes to index K
     auto hidx = [&](int ps) -> int { return p.S ? (ps == 0 ? p.K : ps - 1) : ps; };
 
-    // ---- producer: issue copies in consumption order, as far as allowed ----
-    auto issue_gu = [&](int ps, int pc) {
-      const uint8_t* blob = slot_blob(ps);
-      const int r0 = g.ra + pc * g.teams_gu;
-      const int rn = min(g.teams_gu, g.ra + g.nr - r0);
-      const uint32_t st = g_issue % p.nstage;
-      uint8_t* buf = ring + (size_t)st * p.stage_bytes;
-      const Span a = span_of(blob + p.lay.gate_q + (size_t)r0 * g.qbh, (uint32_t)(rn * g.qbh));
-      const Span b = span_of(blob + p.lay.gate_sb + (size_t)r0 * g.sbbh, (uint32_t)(rn * g.sbbh));
-      const Span cc = span_of(blob + p.lay.up_q + (size_t)r0 * g.qbh, (uint32_t)(rn * g.qbh));
-      const Span d = span_of(blob + p.lay.up_sb + (size_t)r0 * g.sbbh, (uint32_t)(rn * g.sbbh));
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&mbar_ring[st], a.len + b.len + cc.len + d.len);
-      bulk_g2s(buf, a.src, a.len, &mbar_ring[st]);
-      bulk_g2s(buf + p.gu_cap_q, b.src, b.len, &mbar_ring[st]);
-      bulk_g2s(buf + p.gu_cap_q + p.gu_cap_sb, cc.src, cc.len, &mbar_ring[st]);
-      bulk_g2s(buf + 2 * p.gu_cap_q + p.gu_cap_sb, d.src, d.len, &mbar_ring[st]);
-      ++g_issue;
-    };
-    auto issue_d = [&](int ps) {
-      uint8_t* buf = darea + (size_t)ps * p.dslot_bytes;
-      if (g.nd == 0) {
-        mbar_arrive_expect_tx(&mbar_d[ps], 0);
-        return;
-      }
-      const uint8_t* blob = slot_blob(ps);
-      const Span a = span_of(blob + p.lay.down_q + (size_t)g.ja * g.qbi, (uint32_t)(g.nd * g.qbi));
-      const Span b = span_of(blob + p.lay.down_sb + (size_t)g.ja * g.sbbi, (uint32_t)(g.nd * g.sbbi));
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&mbar_d[ps], a.len + b.len);
-      bulk_g2s(buf, a.src, a.len, &mbar_d[ps]);
-      bulk_g2s(buf + p.d_cap_q, b.src, b.len, &mbar_d[ps]);
-    };
-    // job order per slot: its gate/up chunks, then the previous slot's down rows
-    auto pump = [&](uint32_t limit) {
-      while (pr_slot <= NS) {
-        if (pr_slot == NS) {
-          if (NS - 1 >= p.S && !pr_routed) return;
-          issue_d(NS - 1);
-          ++pr_slot;
-          return;
-        }
-        if (pr_slot >= p.S && !pr_routed) return;
-        if (pr_chunk < g.nch) {
-          if (g_issue >= limit) return;
-          issue_gu(pr_slot, pr_chunk);
-          ++pr_chunk;
-          continue;
-        }
-        if (pr_slot >= 1) issue_d(pr_slot - 1);
-        ++pr_slot;
-        pr_chunk = 0;
-      }
-    };
-
-    // ---- prologue ----
-    if (tid == 0) {
-      pr_slot = 0;
-      pr_chunk = 0;
-      pr_routed = false;
-      pump(g_cons + p.nstage);          // shared-expert rows need no routing
-    }
-    const float* hin = p.norm ? (l == 0 ? p.out : p.hbuf + (size_t)((l - 1) & 1) * H) : p.x;
-    const float* res = p.norm ? hin : p.residual;
-    float* outp = p.norm ? ((l == p.L - 1 && !p.copy_back) ? p.out : p.hbuf + (size_t)(l & 1) * H) : p.out;
-
-    if (tid < 32) {
-      int id; float w;
-      warp_route(p.logits + (size_t)l * p.E, p.E, p.K, id, w);
-      if (lane < p.K) {
-        s_ids[p.S + lane] = id;
-        s_w[p.S + lane] = w;
-        if (c == 0 && p.ids_out != nullptr) {
-          p.ids_out[(size_t)l * p.K + lane] = id;
-          p.w_out[(size_t)l * p.K + lane] = w;
-        }
-      }
-    }
-    {
-      float ss = 0.f, wg = 0.f;
-      for (int e = tid * 4; e < H; e += kFusedThreads * 4) {
-        const float4 v = p.norm ? __ldcg(reinterpret_cast<const float4*>(hin + e))
-                                : __ldg(reinterpret_cast<const float4*>(hin + e));
-        ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-        if (p.S) {
-          const uint2 wb = __ldg(reinterpret_cast<const uint2*>(lp.wsg + e));
-          wg += (bf16lo(wb.x) * v.x + bf16hi(wb.x) * v.y) + (bf16lo(wb.y) * v.z + bf16hi(wb.y) * v.w);
-        }
-      }
-      ss = warp_sum(ss);
-      wg = warp_sum(wg);
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------------
+      // producer: one lane issues every copy of the layer in consumption order
+      // ------------------------------------------------------------------
       if (lane == 0) {
-        s_red[2 * (tid >> 5)] = ss;
-        s_red[2 * (tid >> 5) + 1] = wg;
+        auto slot_blob = [&](int ps) -> const uint8_t* {
+          if (p.S && ps == 0) return lp.shared;
+          return lp.experts + (size_t)s_ids[ps] * p.blob;
+        };
+        bool routed = false;       // routed ids are published all at once
+        auto ensure_routed = [&](int ps) {
+          if (ps >= p.S && !routed) {
+            mbar_wait(&bar_routed[0], lpar, tmo, p.err, s_abort);
+            routed = true;
+          }
+        };
+        auto issue_down = [&](int ps) {
+          if (nd == 0 || *s_abort) {
+            mbar_arrive_expect_tx(&bar_dfull[ps], 0);
+            return;
+          }
+          ensure_routed(ps);
+          const uint32_t bytes = (uint32_t)(nd * lay.d_row);
+          mbar_arrive_expect_tx(&bar_dfull[ps], bytes);
+          bulk_g2s(darea + (size_t)ps * pl.dslot_bytes, slot_blob(ps) + lay.d_off + (size_t)ja * lay.d_row, bytes,
+                   &bar_dfull[ps]);
+        };
+        int dnext = 0;
+        for (int k = 0; k < nstg; ++k) {
+          const uint32_t st = g_issue % pl.nstage;
+          const uint32_t use = g_issue / pl.nstage;
+          ++g_issue;
+          if (use >= 1) mbar_wait(&bar_empty[st], (use - 1) & 1u, tmo, p.err, s_abort);
+          const int v0 = k * R, v1 = min(V, v0 + R);
+          if (*s_abort) {
+            mbar_arrive_expect_tx(&bar_full[st], 0);
+          } else {
+            // the stage's bytes are expected up front; the shared expert's
+            // segment goes out at once, routed segments once ids are known
+            mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((v1 - v0) * lay.gu_row));
+            uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
+            for (int v = v0; v < v1;) {           // one copy per slot segment
+              const int ps = v / nr, r = v % nr;
+              const int cnt = min(v1 - v, nr - r);
+              ensure_routed(ps);
+              if (!*s_abort)
+                bulk_g2s(buf + (size_t)(v - v0) * lay.gu_row, slot_blob(ps) + (size_t)(ra + r) * lay.gu_row,
+                         (uint32_t)(cnt * lay.gu_row), &bar_full[st]);
+              v += cnt;
+            }
+          }
+          // down records of slots whose gate/up is dlag slots behind
+          const int slots_issued = v1 / nr;
+          while (dnext < slots_issued - dlag) issue_down(dnext++);
+        }
+        while (dnext < NS) issue_down(dnext++);
       }
-    }
-    __syncthreads();
-    float SS = 0.f, WG = 0.f;
-#pragma unroll
-    for (int w = 0; w < kFusedThreads / 32; ++w) {
-      SS += s_red[2 * w];
-      WG += s_red[2 * w + 1];
-    }
-    const float rinv = p.norm ? 1.0f / sqrtf(SS / (float)H + p.eps) : 1.0f;
-    const float gate = p.S ? sigmoid_f(WG * rinv) : 0.f;
-    if (tid == 0 && p.S) {
-      s_ids[0] = -1;
-      s_w[0] = gate;
-      if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
-    } else if (tid == 0 && c == 0 && p.gate_out != nullptr) {
-      p.gate_out[l] = 0.f;
-    }
-    float xs[kSlice];
-    float xsum;
-    if (p.norm) xsum = load_slice_x<BITS, true>(hin, g.sl, rinv, xs);
-    else xsum = load_slice_x<BITS, false>(hin, g.sl, 1.0f, xs);
-    __syncthreads();
-    if (tid == 0) {
-      pr_routed = true;
-      pump(g_cons + p.nstage);
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxRowsPerTeam; ++i) accd[i] = 0.f;
-
-    // ---- down rows of one slot, folded into the accumulators ----
-    auto do_down = [&](int ps) {
-      if (tid == 0) wait_counter(&ctr[ps], (uint32_t)n, p.timeout_ns, p.err);
-      mbar_wait(&mbar_d[ps], (uint32_t)(l & 1), p.timeout_ns, p.err);
-      __syncthreads();
-      float hs[kSlice];
-      const float hsum = load_slice_x<BITS, true>(p.hmid + (size_t)hidx(ps) * I, g.dsl, 1.0f, hs);
-      const float wk = s_w[ps];
-      const uint8_t* buf = darea + (size_t)ps * p.dslot_bytes;
-      const uint8_t* q0 = buf + span_off((size_t)g.ja * g.qbi);
-      const uint8_t* sb0 = buf + p.d_cap_q + span_off((size_t)g.ja * g.sbbi);
-#pragma unroll
-      for (int i = 0; i < kMaxRowsPerTeam; ++i) {
-        const int jj = g.dteam + i * g.teams_d;
-        if (jj < g.nd) {
-          SliceCodes<BITS> q;
-          if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(q0 + (size_t)jj * g.qbi + g.dsl * 16);
-          else q.v = *reinterpret_cast<const uint2*>(q0 + (size_t)jj * g.qbi + g.dsl * 8);
-          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(sb0 + (size_t)jj * g.sbbi + (g.dsl >> 1) * 4);
-          accd[i] = fmaf(wk, slice_term<BITS>(q, sbw, hs, hsum), accd[i]);
+      __syncwarp();
+    } else if (warp == kFinalWarp) {
+      // ------------------------------------------------------------------
+      // finaliser: h = silu(gate . x) * (up . x) for this block's rows, to L2
+      // ------------------------------------------------------------------
+      for (int ps = 0; ps < NS; ++ps) {
+        mbar_wait(&bar_slot[ps], lpar, tmo, p.err, s_abort);
+        float* hdst = p.hmid + (size_t)hidx(ps) * I + ra;
+        unsigned long long* hll = p.hll + (size_t)hidx(ps) * I + ra;
+        const float* part = s_part + (size_t)ps * pl.nrmax * nparts * 2;
+        for (int r = lane; r < nr; r += 32) {
+          float a = 0.f, u = 0.f;
+          for (int q = 0; q < nparts; ++q) {
+            a += part[(r * nparts + q) * 2];
+            u += part[(r * nparts + q) * 2 + 1];
+          }
+          const float hv = silu_f(a) * u;
+          ll_store(hll + r, hv, tag);
+          if (l == p.L - 1) hdst[r] = hv;
         }
       }
-    };
+    } else if (warp == kExchangeWarp) {
+      // ------------------------------------------------------------------
+      // exchanger: routing, then each slot's full h from L2 into shared memory
+      // ------------------------------------------------------------------
+      {
+        // top-K by repeated warp-wide max: each lane keeps the largest of its
+        // logits (ties: lowest id); a round takes the warp maximum, the lowest
+        // id holding it, and that lane rescans
+        const float* lg = p.logits + (size_t)l * p.E;
+        const int nv = (p.E + 31) >> 5;
+        uint32_t ord[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int id = lane + 32 * j;
+          ord[j] = (j < nv && id < p.E) ? (uint32_t)(route_key(__ldg(lg + id), id) >> 32) : 0u;
+        }
+        uint32_t bo = 0u;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (ord[j] > bo) {
+            bo = ord[j];
+            bj = j;
+          }
+        float my_l = 0.f;
+        int my_id = -1;
+        for (int k = 0; k < p.K; ++k) {
+          const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bo);
+          const uint32_t cid = __reduce_min_sync(0xFFFFFFFFu, bo == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+          if (lane == k) {
+            my_l = key_value((uint64_t)m << 32);
+            my_id = (int)cid;
+          }
+          if ((int)(cid & 31u) == lane) {
+            const int jr = (int)(cid >> 5);
+            bo = 0u;
+            bj = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j == jr) ord[j] = 0u;
+              if (ord[j] > bo) {
+                bo = ord[j];
+                bj = j;
+              }
+            }
+          }
+        }
+        const float lmax = __shfl_sync(0xFFFFFFFFu, my_l, 0);
+        const float e = lane < p.K ? expf(my_l - lmax) : 0.f;
+        const float etot = warp_sum(e);
+        // publish once the consumers hold the whole layer input
+        mbar_wait(bar_xready, lpar, tmo, p.err, s_abort);
+        if (lane < p.K) {
+          s_ids[p.S + lane] = my_id;
+          s_w[p.S + lane] = e / etot;
+          if (c == 0 && p.ids_out != nullptr) {
+            p.ids_out[(size_t)l * p.K + lane] = my_id;
+            p.w_out[(size_t)l * p.K + lane] = e / etot;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_routed[0]);
+      }
+      for (int q = 0; q < NS; ++q) {
+        const unsigned long long* hsrc = p.hll + (size_t)hidx(q) * I;
+        float* hsf = reinterpret_cast<float*>(s_hs + (size_t)q * pl.hs_slot_bytes);
+        float* hsum = hsf + (size_t)8 * hstride * 4;
+        // fetch all I words of the slot, then re-fetch until every tag is current
+        uint64_t t0 = 0;
+        bool started = false;
+        while (true) {
+          for (int c2 = lane; c2 < I / 2; c2 += 32) cp_async16(s_stage + 2 * c2, hsrc + 2 * c2);
+          cp_async_wait_all();
+          __syncwarp();
+          bool ok = true;
+          for (int i = lane; i < I; i += 32) ok = ok && ll_is(s_stage[i], tag);
+          if (__all_sync(0xFFFFFFFFu, ok)) break;
+          if (*s_abort) break;
+          const uint64_t t = global_timer_ns();
+          if (!started) {
+            t0 = t;
+            started = true;
+          } else if (t - t0 > tmo) {
+            atomicOr(p.err, kErrWaitTimeout);
+            *s_abort = 1;
+            break;
+          }
+          __nanosleep(32);
+        }
+        // pre-scale into the padded slice-major layout; lane = position in
+        // the slice, 32 slices at a time, then a transposed reduction leaves
+        // slice g+lane's sum in lane `lane`
+        const float ps_l = pos_scale<BITS>(lane);
+        const int fo = ((lane >> 2) * hstride) * 4 + (lane & 3);
+        for (int g = 0; g < tld; g += 32) {
+          float v[32];
+#pragma unroll
+          for (int mm = 0; mm < 32; ++mm) {
+            const int m = g + mm;
+            v[mm] = 0.f;
+            if (m < tld) {
+              v[mm] = ll_value(s_stage[(size_t)m * kSlice + lane]);
+              hsf[fo + m * 4] = v[mm] * ps_l;
+            }
+          }
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? v[i] : v[i + w];
+              const float keep = up ? v[i + w] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+            }
+          }
+          if (g + lane < tld) hsum[g + lane] = v[0];
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_hready[q]);
+      }
+    } else {
+      // ------------------------------------------------------------------
+      // consumers
+      // ------------------------------------------------------------------
+      SliceX xs;
+      float xsum;
+      float resv[kMaxDownGroups];
+      {
+        // The layer input goes through shared memory, slice-major (float4 j of
+        // slice s at j*tl + s), so that each lane then reads its slice without
+        // bank conflicts.  Every consumer thread fetches 8 consecutive elements
+        // (plain, or published words of the previous layer) and adds up their
+        // squares and their products with the shared-expert gate vector.
+        float ss = 0.f, wg = 0.f;
+        for (int e = tid * 8; e < H; e += kConsumerWarps * 32 * 8) {
+          float4 v0, v1;
+          if (in_ll) {
+            ll_wait8(hin_ll + e, tag - 1u, v0, v1, tmo, p.err, s_abort);
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(hin + e);
+            v0 = p.norm ? __ldcg(src) : __ldg(src);
+            v1 = p.norm ? __ldcg(src + 1) : __ldg(src + 1);
+          }
+          s_x4[((e & 31) >> 2) * tl + (e >> 5)] = v0;
+          s_x4[(((e + 4) & 31) >> 2) * tl + (e >> 5)] = v1;
+          ss += (v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w);
+          ss += (v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w);
+          if (p.S) {
+            const uint4 wb = __ldg(reinterpret_cast<const uint4*>(lp.wsg + e));
+            wg += (bf16lo(wb.x) * v0.x + bf16hi(wb.x) * v0.y) + (bf16lo(wb.y) * v0.z + bf16hi(wb.y) * v0.w);
+            wg += (bf16lo(wb.z) * v1.x + bf16hi(wb.z) * v1.y) + (bf16lo(wb.w) * v1.z + bf16hi(wb.w) * v1.w);
+          }
+        }
+        ss = warp_sum(ss);
+        wg = warp_sum(wg);
+        if (lane == 0) {
+          s_red[2 * warp] = ss;
+          s_red[2 * warp + 1] = wg;
+        }
+        consumer_sync();
+        float tot = 0.f, wgt = 0.f;
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) {
+          tot += s_red[2 * q];
+          wgt += s_red[2 * q + 1];
+        }
+        const float rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
+        if (warp == 0 && lane == 0) {
+          const float gate = p.S ? sigmoid_f(wgt * rinv) : 0.f;
+          if (p.S) s_w[0] = gate;
+          if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
+          mbar_arrive(bar_xready);
+        }
+        xsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kSlice / 4; ++j) {
+          const float4 v = s_x4[j * tl + sl];
+          xsum += put_x4<BITS>(xs, j, make_float4(v.x * rinv, v.y * rinv, v.z * rinv, v.w * rinv));
+        }
+#pragma unroll
+        for (int gi = 0; gi < kMaxDownGroups; ++gi) {
+          const int r = (warp + kConsumerWarps * gi) * rpp + lane / lpr;
+          resv[gi] = 0.f;
+          if ((warp + kConsumerWarps * gi) < ngroups && r < nd && (lane % lpr) == 0) {
+            if (p.norm) {
+              const int e = ja + r;
+              resv[gi] = reinterpret_cast<const float*>(s_x4)[(((e & 31) >> 2) * tl + (e >> 5)) * 4 + (e & 3)];
+            } else {
+              resv[gi] = __ldg(p.residual + ja + r);
+            }
+          }
+        }
+      }
+      float acc[kMaxDownGroups];
+#pragma unroll
+      for (int i = 0; i < kMaxDownGroups; ++i) acc[i] = 0.f;
 
-    // ---- gate/up stream ----
-    for (int ps = 0; ps < NS; ++ps) {
-      for (int pc = 0; pc < g.nch; ++pc) {
-        const uint32_t st = g_cons % p.nstage;
-        mbar_wait(&mbar_ring[st], (g_cons / p.nstage) & 1u, p.timeout_ns, p.err);
-        const int r0 = g.ra + pc * g.teams_gu;
-        const int rn = min(g.teams_gu, g.ra + g.nr - r0);
-        const uint8_t* buf = ring + (size_t)st * p.stage_bytes;
-        float ga = 0.f, ua = 0.f;
-        if (g.team < rn) {
-          const uint8_t* gq = buf + span_off((size_t)r0 * g.qbh) + (size_t)g.team * g.qbh;
-          const uint8_t* gsb = buf + p.gu_cap_q + span_off((size_t)r0 * g.sbbh) + (size_t)g.team * g.sbbh;
-          const uint8_t* uq = buf + p.gu_cap_q + p.gu_cap_sb + span_off((size_t)r0 * g.qbh) + (size_t)g.team * g.qbh;
-          const uint8_t* usb =
-              buf + 2 * p.gu_cap_q + p.gu_cap_sb + span_off((size_t)r0 * g.sbbh) + (size_t)g.team * g.sbbh;
+      auto down = [&](int ps) {
+        mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
+        mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
+        const float wk = s_w[ps];
+        const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
+        const float* hsum = reinterpret_cast<const float*>(s_hs + (size_t)ps * pl.hs_slot_bytes) + (size_t)8 * hstride * 4;
+        const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
+        for (int k = 0; k < spl; ++k) {
+          const int s = (lane % lpr) + 32 * k;
+          SliceX hs;
+#pragma unroll
+          for (int j = 0; j < kSlice / 4; ++j) {
+            const float4 v = hs4[(size_t)j * hstride + s];
+            hs[2 * j] = make_float2(v.x, v.y);
+            hs[2 * j + 1] = make_float2(v.z, v.w);
+          }
+          const float hsm = hsum[s];
+#pragma unroll
+          for (int gi = 0; gi < kMaxDownGroups; ++gi) {
+            const int grp = warp + kConsumerWarps * gi;
+            const int r = grp * rpp + lane / lpr;
+            if (grp < ngroups && r < nd) {
+              const uint8_t* rec = buf + (size_t)r * lay.d_row;
+              SliceCodes<BITS> q;
+              if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
+              else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
+              const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
+              acc[gi] = fmaf(wk, slice_term<BITS>(q, sbw, hs, hsm), acc[gi]);
+            }
+          }
+        }
+      };
+
+      int next_done = 0, next_down = 0;
+      if (nr == 0) {                 // no gate/up rows here: every slot is complete at once
+        __syncwarp();
+        if (lane == 0)
+          for (int ps = 0; ps < NS; ++ps) mbar_arrive(&bar_slot[ps]);
+        next_done = NS;
+      }
+      for (int k = 0; k < nstg; ++k) {
+        const uint32_t st = g_cons % pl.nstage;
+        mbar_wait(&bar_full[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
+        ++g_cons;
+        const uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
+        const int v0 = k * R + rs0, v1 = k * R + rs1;
+        float ga0 = 0.f, ua0 = 0.f, ga1 = 0.f, ua1 = 0.f;
+        if (v0 < V) {
+          const uint8_t* rec = buf + (size_t)rs0 * lay.gu_row;
           SliceCodes<BITS> qg, qu;
           if constexpr (BITS == 4) {
-            qg.v = *reinterpret_cast<const uint4*>(gq + g.sl * 16);
-            qu.v = *reinterpret_cast<const uint4*>(uq + g.sl * 16);
+            qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
+            qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
           } else {
-            qg.v = *reinterpret_cast<const uint2*>(gq + g.sl * 8);
-            qu.v = *reinterpret_cast<const uint2*>(uq + g.sl * 8);
+            qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
+            qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
           }
-          const uint32_t sg = *reinterpret_cast<const uint32_t*>(gsb + (g.sl >> 1) * 4);
-          const uint32_t su = *reinterpret_cast<const uint32_t*>(usb + (g.sl >> 1) * 4);
-          ga = slice_term<BITS>(qg, sg, xs, xsum);
-          ua = slice_term<BITS>(qu, su, xs, xsum);
+          const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
+          const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
+          ga0 = slice_term<BITS>(qg, sg, xs, xsum);
+          ua0 = slice_term<BITS>(qu, su, xs, xsum);
         }
-        // team reduction of (ga, ua): split the pair at half width, then fold
-        {
-          const int half = g.red_w >> 1;
-          const bool low = (lane & half) == 0;
-          const float send = low ? ua : ga;
-          const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, half);
-          float v = (low ? ga : ua) + recv;
-          for (int o = half >> 1; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-          const int pos = lane & (g.red_w - 1);
-          if (g.team < rn && (pos == 0 || pos == half)) {
-            float* dst = s_part + ((((g_cons & 1u) * 32 + g.team) * 2 + (pos == 0 ? 0 : 1)) * 8 + g.wit);
-            *dst = v;
+        if (v1 < V) {
+          const uint8_t* rec = buf + (size_t)rs1 * lay.gu_row;
+          SliceCodes<BITS> qg, qu;
+          if constexpr (BITS == 4) {
+            qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
+            qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
+          } else {
+            qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
+            qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
           }
+          const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
+          const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
+          ga1 = slice_term<BITS>(qg, sg, xs, xsum);
+          ua1 = slice_term<BITS>(qu, su, xs, xsum);
         }
-        __syncthreads();
-        if (tid < rn) {
-          const float* src = s_part + (((g_cons & 1u) * 32 + tid) * 2) * 8;
-          float a = 0.f, u = 0.f;
-          for (int w = 0; w < g.wpt; ++w) {
-            a += src[w];
-            u += src[8 + w];
+        const float v = quad_reduce(ga0, ua0, ga1, ua1, gw, lane);
+        const int pos = lane & (gw - 1), qw = gw >> 2;
+        const int vv = pos < 2 * qw ? v0 : v1;
+        if (vv < V && (pos & (qw - 1)) == 0) {
+          const int ps = vv / nr, r = vv % nr;
+          s_part[(((size_t)ps * pl.nrmax + r) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        // slots whose last row was in this stage are complete
+        const int last_v = min(V, (k + 1) * R);
+        bool fenced = false;
+        while (next_done < NS && (next_done + 1) * nr <= last_v) {
+          if (!fenced) {
+            __threadfence_block();
+            __syncwarp();
+            fenced = true;
           }
-          p.hmid[(size_t)hidx(ps) * I + r0 + tid] = silu_f(a) * u;
+          if (lane == 0) mbar_arrive(&bar_slot[next_done]);
+          ++next_done;
         }
-        ++g_cons;
-        if (tid == 0) pump(g_cons + p.nstage);
+        while (next_down < next_done - dlag) down(next_down++);
       }
-      __syncthreads();
-      if (tid == 0) signal_counter(&ctr[ps]);
-      if (ps >= 1) do_down(ps - 1);
-    }
-    do_down(NS - 1);
+      while (next_down < NS) down(next_down++);
 
-    // ---- combine + residual, written by each row's owner ----
+      // combine + residual, written by each row's owner
 #pragma unroll
-    for (int i = 0; i < kMaxRowsPerTeam; ++i) {
-      const int jj = g.dteam + i * g.teams_d;
-      const float v = warp_sum(accd[i], g.tl_d);
-      if (g.dsl == 0 && jj < g.nd) {
-        const int j = g.ja + jj;
-        const float r = p.norm ? __ldcg(res + j) : res[j];
-        outp[j] = r + v;
+      for (int gi = 0; gi < kMaxDownGroups; ++gi) {
+        const int grp = warp + kConsumerWarps * gi;
+        const float v = warp_sum(acc[gi], lpr);
+        const int r = grp * rpp + lane / lpr;
+        if (grp < ngroups && r < nd && (lane % lpr) == 0) {
+          if (out_ll) ll_store(out_llp + ja + r, resv[gi] + v, tag);
+          else p.out[ja + r] = resv[gi] + v;
+        }
       }
     }
 
-    if (l < p.L - 1 || p.copy_back) {
-      __syncthreads();
-      if (tid == 0) {
-        signal_counter(&ctr[NS]);
-        wait_counter(&ctr[NS], (uint32_t)n, p.timeout_ns, p.err);
-      }
-      __syncthreads();
+    // ---- end of layer: every role is done with this layer's shared memory ----
+    __syncthreads();
+  }
+
+  // No copy may still be writing this block's shared memory when it exits:
+  // wait (bounded, whether or not the block gave up) for the last phase of
+  // every stage and down area that was used.
+  if (warp == kProducerWarp && lane == 0) {
+    volatile int no_abort = 0;
+    const uint32_t used = g_issue < (uint32_t)pl.nstage ? g_issue : (uint32_t)pl.nstage;
+    for (uint32_t st = 0; st < used; ++st) {
+      const uint32_t last = g_issue - 1 - ((g_issue - 1 - st) % pl.nstage);   // last issue index of stage st
+      mbar_wait(&bar_full[st], (last / pl.nstage) & 1u, tmo, p.err, &no_abort);
     }
+    for (int ps = 0; ps < NS; ++ps) mbar_wait(&bar_dfull[ps], (uint32_t)((p.L - 1) & 1), tmo, p.err, &no_abort);
   }
 
-  if (p.copy_back) {
-    for (int j = g.ja + tid; j < g.ja + g.nd; j += kFusedThreads) p.out[j] = __ldcg(p.hbuf + j);
-  }
-
-  // the last block out resets the counters for the next launch
+  // the last block out starts the next epoch of tags and resets the exit count
   __syncthreads();
   if (tid == 0) {
-    uint32_t* exit_ctr = p.counters + (size_t)p.L * (NS + 1);
     __threadfence();
-    const uint32_t old = atomicAdd(exit_ctr, 1u);
+    const uint32_t old = atomicAdd(p.exit_ctr, 1u);
     if (old == (uint32_t)n - 1) {
-      for (int i = 0; i < p.L * (NS + 1); ++i) p.counters[i] = 0;
-      *exit_ctr = 0;
+      *p.exit_ctr = 0;
+      atomicAdd(p.epoch, 1u);
       __threadfence();
     }
   }
@@ -427,35 +742,51 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
 // host side
 // ---------------------------------------------------------------------------
 static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+static int round_up_i(long long v, int a) { return (int)((v + a - 1) / a * a); }
 
 FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
   FusedPlan pl{};
   pl.ok = false;
-  const int tl_gu = H / kSlice, tl_d = I / kSlice;
-  if (H % kSlice || I % kSlice || !pow2(tl_gu) || !pow2(tl_d)) return pl;
-  if (tl_gu < 2 || tl_gu > kFusedThreads || tl_d < 1 || tl_d > 32) return pl;
-  if (K + S > kMaxSlots) return pl;
+  const int tl = H / kSlice, tld = I / kSlice;
+  if (H % kSlice || I % kSlice || !pow2(tl) || !pow2(tld)) return pl;
+  if (tl < 4 || tl > 32 * kConsumerWarps || tld < 1) return pl;
+  if (K + S > kMaxSlots || K < 1) return pl;
   int sms = 0, smem_max = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return pl;
   if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return pl;
   const int grid = sms;
-  const int teams_gu = kFusedThreads / tl_gu, teams_d = kFusedThreads / tl_d;
+  const int NS = K + S;
+  const BlobLayout lay = blob_layout(bits, H, I);
+  // gate/up stage: two rows per consumer warp and slice range
+  const int nparts = tl >= 32 ? tl / 32 : 1;
+  const int R = 2 * (tl >= 32 ? kConsumerWarps / nparts : kConsumerWarps * (32 / tl));
+  pl.rows_per_stage = R;
+  pl.nparts = nparts;
+  pl.stage_bytes = round_up_i((long long)R * lay.gu_row, 128);
+  // down records of one slot
   const int ndmax = (H + grid - 1) / grid;
-  if ((ndmax + teams_d - 1) / teams_d > kMaxRowsPerTeam) return pl;
-  if (teams_gu > 32) return pl;
-  const size_t qbh = (size_t)H * bits / 8, sbbh = (size_t)H / kGroup * 4;
-  const size_t qbi = (size_t)I * bits / 8, sbbi = (size_t)I / kGroup * 4;
-  pl.gu_cap_q = (int)round_up(teams_gu * qbh + 16, 16);
-  pl.gu_cap_sb = (int)round_up(teams_gu * sbbh + 32, 16);
-  pl.stage_bytes = (int)round_up(2 * (pl.gu_cap_q + pl.gu_cap_sb), 128);
-  pl.d_cap_q = (int)round_up(ndmax * qbi + 16, 16);
-  pl.d_cap_sb = (int)round_up(ndmax * sbbi + 32, 16);
-  pl.dslot_bytes = (int)round_up(pl.d_cap_q + pl.d_cap_sb, 128);
-  const long long avail = (long long)smem_max - kCtrlBytes - (long long)(K + S) * pl.dslot_bytes;
+  const int lpr = tld < 32 ? tld : 32, rpp = 32 / lpr;
+  if ((ndmax + rpp - 1) / rpp > kMaxDownGroups * kConsumerWarps) return pl;
+  pl.dslot_bytes = round_up_i((long long)ndmax * lay.d_row, 128);
+  pl.nrmax = (I + grid - 1) / grid;
+  pl.hs_slot_bytes = round_up_i((long long)8 * (tld + 1) * 16 + (long long)tld * 4, 128);
+  pl.part_off = kCtrlBytes;
+  pl.stage_off = round_up_i(pl.part_off + (long long)NS * pl.nrmax * nparts * 2 * 4, 128);
+  pl.hs_off = round_up_i(pl.stage_off + (long long)I * 8, 128);
+  // the layer input is staged where the slots' h will go: it is read by the
+  // consumers before their first gate/up stage, and the first h is written
+  // only after every block has finished a slot
+  pl.xs_off = pl.hs_off;
+  const long long hs_region = (long long)NS * pl.hs_slot_bytes > (long long)H * 4 ? (long long)NS * pl.hs_slot_bytes
+                                                                                  : (long long)H * 4;
+  pl.darea_off = round_up_i(pl.hs_off + hs_region, 128);
+  pl.ring_off = pl.darea_off + NS * pl.dslot_bytes;
+  const long long avail = (long long)smem_max - pl.ring_off;
   const long long ns = avail / pl.stage_bytes;
   if (ns < 2) return pl;
   pl.nstage = (int)(ns > kMaxStages ? kMaxStages : ns);
-  pl.smem = (size_t)kCtrlBytes + (size_t)pl.nstage * pl.stage_bytes + (size_t)(K + S) * pl.dslot_bytes;
+  pl.smem = (size_t)pl.ring_off + (size_t)pl.nstage * pl.stage_bytes;
+  pl.dlag = 2;
   pl.grid = grid;
   pl.ok = true;
   return pl;
@@ -478,8 +809,8 @@ static cudaError_t launch_fused_t(FusedParams& p, const FusedPlan& pl, cudaStrea
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     checked_smem = pl.smem;
   }
-  // cooperative: all blocks resident at once (the per-slot and per-layer
-  // counters are waited on by every block)
+  // cooperative: all blocks resident at once (every block waits for words
+  // that the other blocks publish)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kFusedThreads);
@@ -494,13 +825,7 @@ static cudaError_t launch_fused_t(FusedParams& p, const FusedPlan& pl, cudaStrea
 }
 
 cudaError_t launch_fused(FusedParams& p, const FusedPlan& pl, cudaStream_t st) {
-  p.nstage = pl.nstage;
-  p.stage_bytes = pl.stage_bytes;
-  p.dslot_bytes = pl.dslot_bytes;
-  p.gu_cap_q = pl.gu_cap_q;
-  p.gu_cap_sb = pl.gu_cap_sb;
-  p.d_cap_q = pl.d_cap_q;
-  p.d_cap_sb = pl.d_cap_sb;
+  p.plan = pl;
   return p.bits == 4 ? launch_fused_t<4>(p, pl, st) : launch_fused_t<2>(p, pl, st);
 }
 

@@ -73,15 +73,15 @@ __global__ void gateup_generic_kernel(GenericArgs a) {
   const uint8_t* blob = slot_blob(a, t, slot);
   float* hout = a.h + ((size_t)t * NS + slot) * a.I + r;
   if (blob == nullptr) { if (lane == 0) *hout = 0.f; return; }
-  const size_t qrow = (size_t)a.H * BITS / 8, sbrow = (size_t)a.H / kGroup * 4;
-  const uint8_t* gq = blob + a.lay.gate_q + (size_t)r * qrow;
-  const uint32_t* gsb = reinterpret_cast<const uint32_t*>(blob + a.lay.gate_sb + (size_t)r * sbrow);
-  const uint8_t* uq = blob + a.lay.up_q + (size_t)r * qrow;
-  const uint32_t* usb = reinterpret_cast<const uint32_t*>(blob + a.lay.up_sb + (size_t)r * sbrow);
+  const uint8_t* row = blob + (size_t)r * a.lay.gu_row;
+  const uint8_t* gq = row;
+  const uint8_t* uq = row + a.lay.qh;
+  const uint32_t* gsb = reinterpret_cast<const uint32_t*>(row + 2 * a.lay.qh);
+  const uint32_t* usb = reinterpret_cast<const uint32_t*>(row + 2 * a.lay.qh + a.lay.sh);
   const float* x = a.x + (size_t)t * a.H;
   float ga = 0.f, ua = 0.f;
   for (int s = lane; s < a.H / kSlice; s += 32) {
-    float xs[kSlice];
+    SliceX xs;
     const float xsum = load_slice_x<BITS, false>(x, s, 1.0f, xs);
     ga += slice_term<BITS>(load_codes<BITS>(gq, s), __ldg(gsb + s / 2), xs, xsum);
     ua += slice_term<BITS>(load_codes<BITS>(uq, s), __ldg(usb + s / 2), xs, xsum);
@@ -105,13 +105,12 @@ __global__ void down_y_kernel(GenericArgs a, float* __restrict__ y) {
   const uint8_t* blob = slot_blob(a, t, slot);
   float* yout = y + ((size_t)t * NS + slot) * a.H + j;
   if (blob == nullptr) { if (lane == 0) *yout = 0.f; return; }
-  const size_t qrow = (size_t)a.I * BITS / 8, sbrow = (size_t)a.I / kGroup * 4;
-  const uint8_t* dq = blob + a.lay.down_q + (size_t)j * qrow;
-  const uint32_t* dsb = reinterpret_cast<const uint32_t*>(blob + a.lay.down_sb + (size_t)j * sbrow);
+  const uint8_t* dq = blob + a.lay.d_off + (size_t)j * a.lay.d_row;
+  const uint32_t* dsb = reinterpret_cast<const uint32_t*>(dq + a.lay.qi);
   const float* h = a.h + ((size_t)t * NS + slot) * a.I;
   float acc = 0.f;
   for (int s = lane; s < a.I / kSlice; s += 32) {
-    float hs[kSlice];
+    SliceX hs;
     const float hsum = load_slice_x<BITS, false>(h, s, 1.0f, hs);
     acc += slice_term<BITS>(load_codes<BITS>(dq, s), __ldg(dsb + s / 2), hs, hsum);
   }
@@ -129,18 +128,17 @@ __global__ void down_combine_kernel(GenericArgs a) {
   if (gw >= (long long)a.T * a.H) return;
   const int j = (int)(gw % a.H);
   const int t = (int)(gw / a.H);
-  const size_t qrow = (size_t)a.I * BITS / 8, sbrow = (size_t)a.I / kGroup * 4;
   float acc = 0.f;
   for (int slot = 0; slot < NS; ++slot) {
     const uint8_t* blob = slot_blob(a, t, slot);
     if (blob == nullptr) continue;
     const float wk = (slot < a.K) ? a.weights[(size_t)t * a.K + slot] : a.gate[t];
-    const uint8_t* dq = blob + a.lay.down_q + (size_t)j * qrow;
-    const uint32_t* dsb = reinterpret_cast<const uint32_t*>(blob + a.lay.down_sb + (size_t)j * sbrow);
+    const uint8_t* dq = blob + a.lay.d_off + (size_t)j * a.lay.d_row;
+    const uint32_t* dsb = reinterpret_cast<const uint32_t*>(dq + a.lay.qi);
     const float* h = a.h + ((size_t)t * NS + slot) * a.I;
     float part = 0.f;
     for (int s = lane; s < a.I / kSlice; s += 32) {
-      float hs[kSlice];
+      SliceX hs;
       const float hsum = load_slice_x<BITS, false>(h, s, 1.0f, hs);
       part += slice_term<BITS>(load_codes<BITS>(dq, s), __ldg(dsb + s / 2), hs, hsum);
     }

@@ -40,25 +40,26 @@ constexpr uint32_t kErrBadExpert = 4u;     // expert id outside [0, E)
 // blob layout (the library's own statement of the packed format)
 // ---------------------------------------------------------------------------
 struct BlobLayout {
-  size_t gate_q, gate_sb, up_q, up_sb, down_q, down_sb, bytes;
+  size_t qh, sh;     // bytes of one gate/up row's codes and of its (scale,bias) words
+  size_t qi, si;     // the same for one down row
+  size_t gu_row;     // stride of gate/up row records [gate_q | up_q | gate_sb | up_sb], 16-byte padded
+  size_t d_off;      // offset of down row 0 (256-byte aligned)
+  size_t d_row;      // stride of down row records [down_q | down_sb], 16-byte padded
+  size_t bytes;      // blob size, a multiple of 256
 };
 
 __host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline BlobLayout blob_layout(int bits, int H, int I) {
   BlobLayout L;
-  const size_t qrow_in_h = (size_t)H * bits / 8;   // bytes of one gate/up code row
-  const size_t sbrow_in_h = (size_t)H / kGroup * 4;
-  const size_t qrow_in_i = (size_t)I * bits / 8;   // bytes of one down code row
-  const size_t sbrow_in_i = (size_t)I / kGroup * 4;
-  size_t pos = 0;
-  L.gate_q = pos;  pos = round_up(pos + (size_t)I * qrow_in_h, kPlaneAlign);
-  L.gate_sb = pos; pos = round_up(pos + (size_t)I * sbrow_in_h, kPlaneAlign);
-  L.up_q = pos;    pos = round_up(pos + (size_t)I * qrow_in_h, kPlaneAlign);
-  L.up_sb = pos;   pos = round_up(pos + (size_t)I * sbrow_in_h, kPlaneAlign);
-  L.down_q = pos;  pos = round_up(pos + (size_t)H * qrow_in_i, kPlaneAlign);
-  L.down_sb = pos; pos = round_up(pos + (size_t)H * sbrow_in_i, kPlaneAlign);
-  L.bytes = pos;
+  L.qh = (size_t)H * bits / 8;
+  L.sh = (size_t)H / kGroup * 4;
+  L.qi = (size_t)I * bits / 8;
+  L.si = (size_t)I / kGroup * 4;
+  L.gu_row = round_up(2 * L.qh + 2 * L.sh, 16);
+  L.d_row = round_up(L.qi + L.si, 16);
+  L.d_off = round_up((size_t)I * L.gu_row, kPlaneAlign);
+  L.bytes = round_up(L.d_off + (size_t)H * L.d_row, kPlaneAlign);
   return L;
 }
 
@@ -66,32 +67,36 @@ __host__ __device__ inline BlobLayout blob_layout(int bits, int H, int I) {
 // workspace layout
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t err;        // uint32 error word (+ padding)
-  size_t counters;   // uint32 device-wide counters
-  size_t n_counters;
+  size_t err;        // uint32 error word; the 256-byte header also holds:
+  size_t exit_ctr;   //   uint32: blocks of the current launch that have finished
+  size_t epoch;      //   uint32: launches completed on this workspace (tags the exchanges)
+  size_t header_clear;  // bytes of the header a fresh call may zero (everything before `epoch`)
   size_t ids;        // int32 [T][K]
   size_t weights;    // fp32 [T][K]
   size_t gate;       // fp32 [T]
   size_t h;          // fp32 [T][K+S][I]
-  size_t hbuf;       // fp32 [2][H] stack ping-pong
+  size_t hll;        // u64 [K+S][I]: (value, tag) exchange of h between blocks
+  size_t hbufll;     // u64 [2][H]: (value, tag) layer outputs of a stack
   size_t plan;       // int32 batch plan
   size_t plan_words;
   size_t bytes;
 };
 
 inline WsLayout ws_layout(int H, int I, int S, int T, int K, int L) {
+  (void)L;
   WsLayout w;
   size_t pos = 0;
-  w.err = pos; pos += 256;
-  w.counters = pos;
-  // per layer: one counter per slot, one layer-done counter; plus exit/test counters
-  w.n_counters = (size_t)L * (K + S + 1) + 8;
-  pos = round_up(pos + w.n_counters * 4, 256);
+  w.err = 0;
+  w.exit_ctr = 96;
+  w.epoch = 128;
+  w.header_clear = 128;
+  pos = 256;
   w.ids = pos; pos = round_up(pos + (size_t)T * K * 4, 256);
   w.weights = pos; pos = round_up(pos + (size_t)T * K * 4, 256);
   w.gate = pos; pos = round_up(pos + (size_t)T * 4, 256);
   w.h = pos; pos = round_up(pos + (size_t)T * (K + S) * I * 4, 256);
-  w.hbuf = pos; pos = round_up(pos + (size_t)2 * H * 4, 256);
+  w.hll = pos; pos = round_up(pos + (size_t)(K + S) * I * 8, 256);
+  w.hbufll = pos; pos = round_up(pos + (size_t)2 * H * 8, 256);
   // plan: unique count, unique ids[T*K+1], per-unique token count, token lists
   w.plan_words = 4 + 4 * (size_t)(T * K + 1) + (size_t)(T * K + 1) * (T + 1);
   w.plan = pos; pos = round_up(pos + w.plan_words * 4, 256);
@@ -112,18 +117,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// d.xy += a.xy * b.xy with one packed fp32x2 FMA (round to nearest, subnormals kept)
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rd, {%0, %1};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
 // Positional pre-scale of input element i of a 32-code slice.
 //   4-bit: codes 0..3 of a word are masked from the word, codes 4..7 from
 //          the word shifted right by 16; position p = i mod 4, factor 2^(85-4p)
@@ -136,53 +129,53 @@ __device__ __forceinline__ float pos_scale(int i) {
   return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
-// Sum over one 32-code slice of code * xs (xs pre-scaled by pos_scale):
-// returns 2^-64 * sum q_i x_i.
+// The 32 inputs of a slice, pre-scaled by pos_scale, as 16 pairs (element
+// 2k in .x, 2k+1 in .y) so that each packed fp32x2 FMA takes one pair.
+typedef float2 SliceX[kSlice / 2];
+
 template <int BITS> struct SliceCodes;
 template <> struct SliceCodes<4> { uint4 v; };
 template <> struct SliceCodes<2> { uint2 v; };
 
+// A code masked in place, read as an fp32 (see the file comment).
 __device__ __forceinline__ float mk(uint32_t w, uint32_t m) { return __uint_as_float(w & m); }
+__device__ __forceinline__ float2 mk2(uint32_t w, uint32_t m0, uint32_t m1) { return make_float2(mk(w, m0), mk(w, m1)); }
 
-__device__ __forceinline__ float slice_dot(const SliceCodes<4>& q, const float (&xs)[kSlice]) {
-  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+// Sum over one 32-code slice of code * xs: returns 2^-64 * sum q_i x_i.
+// Two independent packed accumulators; one AND per code, one fma.rn.f32x2
+// per two codes.
+__device__ __forceinline__ float slice_dot(const SliceCodes<4>& q, const SliceX& xs) {
+  float2 a = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t w = (&q.v.x)[j];
     const uint32_t hi = w >> 16;
-    const float* x = xs + 8 * j;
-    if (j & 1) {
-      ffma2(c0, c1, mk(w, 0xFu), mk(w, 0xF0u), x[0], x[1]);
-      ffma2(c0, c1, mk(w, 0xF00u), mk(w, 0xF000u), x[2], x[3]);
-      ffma2(c0, c1, mk(hi, 0xFu), mk(hi, 0xF0u), x[4], x[5]);
-      ffma2(c0, c1, mk(hi, 0xF00u), mk(hi, 0xF000u), x[6], x[7]);
-    } else {
-      ffma2(a0, a1, mk(w, 0xFu), mk(w, 0xF0u), x[0], x[1]);
-      ffma2(a0, a1, mk(w, 0xF00u), mk(w, 0xF000u), x[2], x[3]);
-      ffma2(a0, a1, mk(hi, 0xFu), mk(hi, 0xF0u), x[4], x[5]);
-      ffma2(a0, a1, mk(hi, 0xF00u), mk(hi, 0xF000u), x[6], x[7]);
-    }
+    a = __ffma2_rn(mk2(w, 0xFu, 0xF0u), xs[4 * j + 0], a);
+    c = __ffma2_rn(mk2(w, 0xF00u, 0xF000u), xs[4 * j + 1], c);
+    a = __ffma2_rn(mk2(hi, 0xFu, 0xF0u), xs[4 * j + 2], a);
+    c = __ffma2_rn(mk2(hi, 0xF00u, 0xF000u), xs[4 * j + 3], c);
   }
-  return (a0 + a1) + (c0 + c1);
+  const float2 s = __fadd2_rn(a, c);
+  return s.x + s.y;
 }
 
-__device__ __forceinline__ float slice_dot(const SliceCodes<2>& q, const float (&xs)[kSlice]) {
-  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+__device__ __forceinline__ float slice_dot(const SliceCodes<2>& q, const SliceX& xs) {
+  float2 a = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t w = (&q.v.x)[j];
     const uint32_t hi = w >> 16;
-    const float* x = xs + 16 * j;
-    ffma2(a0, a1, mk(w, 0x3u), mk(w, 0xCu), x[0], x[1]);
-    ffma2(c0, c1, mk(w, 0x30u), mk(w, 0xC0u), x[2], x[3]);
-    ffma2(a0, a1, mk(w, 0x300u), mk(w, 0xC00u), x[4], x[5]);
-    ffma2(c0, c1, mk(w, 0x3000u), mk(w, 0xC000u), x[6], x[7]);
-    ffma2(a0, a1, mk(hi, 0x3u), mk(hi, 0xCu), x[8], x[9]);
-    ffma2(c0, c1, mk(hi, 0x30u), mk(hi, 0xC0u), x[10], x[11]);
-    ffma2(a0, a1, mk(hi, 0x300u), mk(hi, 0xC00u), x[12], x[13]);
-    ffma2(c0, c1, mk(hi, 0x3000u), mk(hi, 0xC000u), x[14], x[15]);
+    a = __ffma2_rn(mk2(w, 0x3u, 0xCu), xs[8 * j + 0], a);
+    c = __ffma2_rn(mk2(w, 0x30u, 0xC0u), xs[8 * j + 1], c);
+    a = __ffma2_rn(mk2(w, 0x300u, 0xC00u), xs[8 * j + 2], a);
+    c = __ffma2_rn(mk2(w, 0x3000u, 0xC000u), xs[8 * j + 3], c);
+    a = __ffma2_rn(mk2(hi, 0x3u, 0xCu), xs[8 * j + 4], a);
+    c = __ffma2_rn(mk2(hi, 0x30u, 0xC0u), xs[8 * j + 5], c);
+    a = __ffma2_rn(mk2(hi, 0x300u, 0xC00u), xs[8 * j + 6], a);
+    c = __ffma2_rn(mk2(hi, 0x3000u, 0xC000u), xs[8 * j + 7], c);
   }
-  return (a0 + a1) + (c0 + c1);
+  const float2 s = __fadd2_rn(a, c);
+  return s.x + s.y;
 }
 
 // Contribution of one slice to a row dot product:
@@ -190,30 +183,35 @@ __device__ __forceinline__ float slice_dot(const SliceCodes<2>& q, const float (
 // where sb is the (scale, bias) word of the slice's group and xsum is the
 // plain sum of the slice's 32 (unscaled) inputs.
 template <int BITS>
-__device__ __forceinline__ float slice_term(const SliceCodes<BITS>& q, uint32_t sb,
-                                            const float (&xs)[kSlice], float xsum) {
+__device__ __forceinline__ float slice_term(const SliceCodes<BITS>& q, uint32_t sb, const SliceX& xs,
+                                            float xsum) {
   const float p = slice_dot(q, xs);
   const float s64 = bf16lo(sb) * 18446744073709551616.0f;   // scale * 2^64
   return fmaf(s64, p, bf16hi(sb) * xsum);
 }
 
-// Load the 32 inputs of slice `s` from fp32 global memory, pre-scaled; returns
-// their plain sum.  `cg` selects an L2-only load (data written earlier in the
-// same kernel by other blocks).
+// Pre-scale four consecutive inputs (elements 4j..4j+3 of a slice) into the
+// pair array; returns their plain sum.
+template <int BITS>
+__device__ __forceinline__ float put_x4(SliceX& xs, int j, float4 v) {
+  xs[2 * j] = make_float2(v.x * pos_scale<BITS>(4 * j + 0), v.y * pos_scale<BITS>(4 * j + 1));
+  xs[2 * j + 1] = make_float2(v.z * pos_scale<BITS>(4 * j + 2), v.w * pos_scale<BITS>(4 * j + 3));
+  return (v.x + v.y) + (v.z + v.w);
+}
+
+// Load the 32 inputs of slice `s` from fp32 global memory, multiplied by
+// `scale` and pre-scaled; returns the plain sum of the scaled values.  `CG`
+// selects an L2-only load (data written earlier in the same kernel by other
+// blocks).
 template <int BITS, bool CG>
-__device__ __forceinline__ float load_slice_x(const float* __restrict__ x, int s, float scale,
-                                              float (&xs)[kSlice]) {
+__device__ __forceinline__ float load_slice_x(const float* __restrict__ x, int s, float scale, SliceX& xs) {
   const float4* p = reinterpret_cast<const float4*>(x + (size_t)s * kSlice);
   float sum = 0.f;
 #pragma unroll
   for (int j = 0; j < kSlice / 4; ++j) {
     float4 v = CG ? __ldcg(p + j) : __ldg(p + j);
     v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
-    sum += (v.x + v.y) + (v.z + v.w);
-    xs[4 * j + 0] = v.x * pos_scale<BITS>(4 * j + 0);
-    xs[4 * j + 1] = v.y * pos_scale<BITS>(4 * j + 1);
-    xs[4 * j + 2] = v.z * pos_scale<BITS>(4 * j + 2);
-    xs[4 * j + 3] = v.w * pos_scale<BITS>(4 * j + 3);
+    sum += put_x4<BITS>(xs, j, v);
   }
   return sum;
 }

@@ -31,16 +31,38 @@ cudaError_t launch_down_combine(const GenericArgs& a, cudaStream_t st);
 // ---------------------------------------------------------------------------
 // single-launch persistent kernel (fmoe_fused.cu)
 // ---------------------------------------------------------------------------
-constexpr int kFusedThreads = 512;
+constexpr int kConsumerWarps = 16;                     // dequant GEMV warps
+constexpr int kProducerWarp = kConsumerWarps;          // issues the bulk copies
+constexpr int kFinalWarp = kConsumerWarps + 1;         // turns partial sums into h rows
+constexpr int kExchangeWarp = kConsumerWarps + 2;      // gathers every block's h rows
+constexpr int kFusedThreads = 32 * (kConsumerWarps + 3);
+// registers per thread: the most that every warp can hold when the warps are
+// spread over the SM's four schedulers, each with 16K registers (8 at a time)
+constexpr int kFusedWarpsPerScheduler = (kFusedThreads / 32 + 3) / 4;
+constexpr int kFusedMaxRegs = (16384 / (kFusedWarpsPerScheduler * 32)) / 8 * 8;
 constexpr int kMaxFusedLayers = 64;    // layers per launch; longer stacks use several launches
 constexpr int kMaxSlots = FMOE_MAX_TOPK + 1;
 constexpr int kMaxStages = 16;
-constexpr int kMaxRowsPerTeam = 4;     // down rows per team per block
+constexpr int kMaxDownGroups = 4;      // down row groups per consumer warp
+constexpr int kCtrlBytes = 2048;       // barriers, routing result, reductions
 
 struct FusedLayerPtrs {
   const uint8_t* experts;
   const uint8_t* shared;
   const uint16_t* wsg;
+};
+
+// Shared-memory plan and per-shape geometry (host computed by fused_plan).
+struct FusedPlan {
+  bool ok;
+  int grid;
+  size_t smem;
+  int rows_per_stage;       // gate/up rows per ring stage (two per consumer warp and slice range)
+  int nstage, stage_bytes;  // ring
+  int dslot_bytes;          // one slot's down records
+  int nrmax, nparts;        // gate/up rows per block and partial sums per row
+  int part_off, xs_off, stage_off, hs_off, hs_slot_bytes, darea_off, ring_off;
+  int dlag;                 // a slot's down records are copied, and used, dlag slots after its gate/up
 };
 
 struct FusedParams {
@@ -53,27 +75,18 @@ struct FusedParams {
   const float* residual;    // norm == 0: residual [H]
   float* out;               // norm == 0: output [H];  norm == 1: h (in for layer 0, out for the last)
   const float* logits;      // [L][E]
-  float* hmid;              // [K+S][I]
-  float* hbuf;              // [2][H]
+  float* hmid;              // [K+S][I] h of the last layer (plain fp32)
+  unsigned long long* hll;  // [K+S][I] (value, tag) exchange of h
+  unsigned long long* hbufll;  // [2][H] (value, tag) outputs of layers 0..L-2 (stacks)
   int32_t* ids_out;         // [L][K] or nullptr
   float* w_out;             // [L][K] or nullptr
   float* gate_out;          // [L] or nullptr
-  uint32_t* counters;       // [L][K+S+1] + 1 exit counter (zero on entry, zero on exit)
+  uint32_t* exit_ctr;       // zero on entry and on exit
+  uint32_t* epoch;          // incremented by the last block out
   uint32_t* err;
   unsigned long long timeout_ns;
-  int copy_back;            // norm == 1 and L == 1: the result goes through hbuf then to out
-  // shared-memory plan (host computed)
-  int nstage, stage_bytes, dslot_bytes;
-  int gu_cap_q, gu_cap_sb, d_cap_q, d_cap_sb;
+  FusedPlan plan;
   FusedLayerPtrs layer[kMaxFusedLayers];
-};
-
-struct FusedPlan {
-  bool ok;
-  int grid;
-  size_t smem;
-  int nstage, stage_bytes, dslot_bytes;
-  int gu_cap_q, gu_cap_sb, d_cap_q, d_cap_sb;
 };
 
 // Plan the persistent launch for a shape; ok == false if the shape does not

@@ -99,9 +99,11 @@ extern "C" fmoe_status fmoe_moe_block_noalloc(const fmoe_layer* layer, const flo
   if (base == nullptr) return FMOE_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The error word and the device-wide counters must start at zero; the
-  // previous call (or a timed-out one) may have left them otherwise.
-  cudaError_t e = cudaMemsetAsync(base, 0, wl.ids, st);
+  // The error word and the count of finished blocks must start at zero; the
+  // previous call (or a timed-out one) may have left them otherwise.  The
+  // launch counter that tags the blocks' exchanges must never go back, so it
+  // is left alone.
+  cudaError_t e = cudaMemsetAsync(base, 0, wl.header_clear, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FMOE_ERR_CUDA;
@@ -124,14 +126,15 @@ extern "C" fmoe_status fmoe_moe_block_noalloc(const fmoe_layer* layer, const flo
   p.out = out;
   p.logits = router_logits;
   p.hmid = reinterpret_cast<float*>(base + wl.h);
-  p.hbuf = reinterpret_cast<float*>(base + wl.hbuf);
+  p.hll = reinterpret_cast<unsigned long long*>(base + wl.hll);
+  p.hbufll = reinterpret_cast<unsigned long long*>(base + wl.hbufll);
   p.ids_out = nullptr;
   p.w_out = nullptr;
   p.gate_out = nullptr;
-  p.counters = reinterpret_cast<uint32_t*>(base + wl.counters);
+  p.exit_ctr = reinterpret_cast<uint32_t*>(base + wl.exit_ctr);
+  p.epoch = reinterpret_cast<uint32_t*>(base + wl.epoch);
   p.err = reinterpret_cast<uint32_t*>(base + wl.err);
   p.timeout_ns = kNoallocTimeoutNs;
-  p.copy_back = 0;
   p.layer[0].experts = static_cast<const uint8_t*>(layer->experts);
   p.layer[0].shared = static_cast<const uint8_t*>(layer->shared);
   p.layer[0].wsg = layer->shared_gate_w;

@@ -17,16 +17,22 @@ Two kinds of draws:
 * Activations (x, router logits, residual, shared-gate vector) are small and
   are always drawn on the CPU with ``torch.Generator`` and then moved.
 
-Blob format written here (one contiguous blob per expert, six planes, each
-plane starting on a 256-byte boundary):
+Blob format written here (one contiguous blob per expert):
 
-    gate_q  [I][H*bits/32] uint32   packed codes, element c of a row at
-                                    bits (c % (32/bits))*bits of word c/(32/bits)
-    gate_sb [I][H/64]      uint32   low half = scale (bf16), high half = bias (bf16)
-    up_q    [I][H*bits/32] uint32
-    up_sb   [I][H/64]      uint32
-    down_q  [H][I*bits/32] uint32
-    down_sb [H][I/64]      uint32
+    gate/up rows, r = 0..I-1, each padded to a multiple of 16 bytes:
+        gate_q [H*bits/32] uint32   packed codes of gate row r
+        up_q   [H*bits/32] uint32   packed codes of up row r
+        gate_sb [H/64]     uint32   low half = scale (bf16), high half = bias (bf16)
+        up_sb   [H/64]     uint32
+    down rows, j = 0..H-1, starting on a 256-byte boundary, each padded to a
+    multiple of 16 bytes:
+        down_q [I*bits/32] uint32
+        down_sb [I/64]     uint32
+    the blob is padded to a multiple of 256 bytes.
+
+Element c of a packed row sits at bits (c % (32/bits))*bits of word
+c/(32/bits).  One row of each matrix is contiguous with its scales, so any
+range of rows is one contiguous byte range.
 
 The packed-code and affine-group form follows the flash-moe write-ups'
 description of the 4-bit / 2-bit expert weights ("nibble * scale + bias",
@@ -102,7 +108,7 @@ def _round_up(n: int, a: int) -> int:
 
 
 def plane_words(bits: int, hidden: int, inter: int) -> dict:
-    """(rows, words per row) of each plane."""
+    """(rows, words per row) of each of the six parts of a blob."""
     per = 32 // bits
     return {
         "gate_q": (inter, hidden // per),
@@ -114,18 +120,26 @@ def plane_words(bits: int, hidden: int, inter: int) -> dict:
     }
 
 
-def plane_offsets(bits: int, hidden: int, inter: int) -> tuple:
-    """Byte offset of every plane and the blob size (a multiple of 256)."""
-    offs, pos = {}, 0
-    for name, (rows, wpr) in plane_words(bits, hidden, inter).items():
-        pos = _round_up(pos, PLANE_ALIGN)
-        offs[name] = pos
-        pos += rows * wpr * 4
-    return offs, _round_up(pos, PLANE_ALIGN)
+def row_layout(bits: int, hidden: int, inter: int) -> tuple:
+    """(dict part -> (byte offset of row 0, byte stride between rows), blob bytes)."""
+    qh, sh = hidden * bits // 8, hidden // GROUP * 4
+    qi, si = inter * bits // 8, inter // GROUP * 4
+    gu_row = _round_up(2 * qh + 2 * sh, 16)
+    d_row = _round_up(qi + si, 16)
+    d_off = _round_up(inter * gu_row, PLANE_ALIGN)
+    parts = {
+        "gate_q": (0, gu_row),
+        "up_q": (qh, gu_row),
+        "gate_sb": (2 * qh, gu_row),
+        "up_sb": (2 * qh + sh, gu_row),
+        "down_q": (d_off, d_row),
+        "down_sb": (d_off + qi, d_row),
+    }
+    return parts, _round_up(d_off + hidden * d_row, PLANE_ALIGN)
 
 
 def blob_bytes(bits: int, hidden: int, inter: int) -> int:
-    return plane_offsets(bits, hidden, inter)[1]
+    return row_layout(bits, hidden, inter)[1]
 
 
 # ---------------------------------------------------------------------------
@@ -187,22 +201,25 @@ def expert_blobs(shape: BlockShape, layer: int, experts, device="cpu",
     """
     seed = shape.seed if seed is None else seed
     bits, H, I = shape.bits, shape.hidden, shape.inter
-    offs, nbytes = plane_offsets(bits, H, I)
+    parts, nbytes = row_layout(bits, H, I)
     ex = torch.as_tensor(experts, dtype=torch.int64).reshape(-1, 1).to(device)
     words = torch.zeros((ex.shape[0], nbytes // 4), dtype=torch.int64, device=device)
     for name, (rows, wpr) in plane_words(bits, H, I).items():
         n = rows * wpr
-        o = offs[name] // 4
+        base, stride = parts[name]
         pid = _PLANE_ID[name]
-        idx = torch.arange(n, dtype=torch.int64, device=device).reshape(1, -1)
+        idx = torch.arange(n, dtype=torch.int64, device=device)
+        dst = base // 4 + (idx // wpr) * (stride // 4) + idx % wpr
+        idx = idx.reshape(1, -1)
         if name.endswith("_q"):
-            words[:, o:o + n] = _word_hash(_stream_key(seed, layer, pid, 0), ex, idx)
+            vals = _word_hash(_stream_key(seed, layer, pid, 0), ex, idx)
         else:
             s = _uniform_bf16_bits(_word_hash(_stream_key(seed, layer, pid, 1), ex, idx),
                                    shape.scale_lo, shape.scale_hi)
             b = _uniform_bf16_bits(_word_hash(_stream_key(seed, layer, pid, 2), ex, idx),
                                    shape.bias_lo, shape.bias_hi)
-            words[:, o:o + n] = s | (b << 16)
+            vals = s | (b << 16)
+        words[:, dst] = vals
     # reinterpret the low 32 bits as int32
     return (words - ((words >> 31) << 32)).to(torch.int32)
 

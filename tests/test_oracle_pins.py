@@ -55,14 +55,14 @@ def sb(scale, bias, rows, groups):
 
 def build_blob(bits, H, I, gate, up, down):
     """Blob bytes from (codes, sb_words) per matrix, placed with the generator's layout."""
-    offs, nbytes = synth.plane_offsets(bits, H, I)
+    parts, nbytes = synth.row_layout(bits, H, I)
     words = np.zeros(nbytes // 4, dtype=np.uint32)
     for name, (codes, sbw) in (("gate", gate), ("up", up), ("down", down)):
-        q = pack(codes, bits).reshape(-1)
-        o = offs[name + "_q"] // 4
-        words[o:o + q.size] = q
-        o = offs[name + "_sb"] // 4
-        words[o:o + sbw.size] = sbw.reshape(-1)
+        for part, rows in ((name + "_q", pack(codes, bits)), (name + "_sb", np.asarray(sbw, dtype=np.uint32))):
+            base, stride = parts[part]
+            for r in range(rows.shape[0]):
+                o = (base + r * stride) // 4
+                words[o:o + rows.shape[1]] = rows[r]
     return words.view(np.uint8)
 
 
@@ -300,11 +300,11 @@ def pin_page_sizes():
 
 
 def pin_layout_matches_generator():
-    for bits, H, I in ((4, 512, 128), (4, 4096, 1024), (2, 4096, 1024), (4, 2048, 512)):
-        planes, nbytes = om.layout(bits, H, I)
-        offs, nb2 = synth.plane_offsets(bits, H, I)
+    for bits, H, I in ((4, 512, 128), (4, 4096, 1024), (2, 4096, 1024), (4, 2048, 512), (2, 192, 320)):
+        parts, nbytes = om.layout(bits, H, I)
+        offs, nb2 = synth.row_layout(bits, H, I)
         assert nbytes == nb2
-        assert {k: v[0] for k, v in planes.items()} == offs
+        assert {k: (v[0], v[1]) for k, v in parts.items()} == offs
 
 
 def pin_block_closed_form():

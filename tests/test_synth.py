@@ -22,13 +22,16 @@ def test_blob_is_deterministic_and_chunk_independent():
 def test_codes_uniform_and_scales_in_range():
     s = synth.QWEN_Q4
     blob = synth.expert_blob(s, 0, 17).numpy().view(np.uint32)
-    offs, nbytes = synth.plane_offsets(s.bits, s.hidden, s.inter)
+    parts, nbytes = synth.row_layout(s.bits, s.hidden, s.inter)
     assert blob.size * 4 == nbytes == 7077888
-    q = blob[offs["gate_q"] // 4: offs["gate_sb"] // 4].astype(np.uint64)
+    base, stride = parts["gate_q"]
+    rows = blob[: s.inter * stride // 4].reshape(s.inter, stride // 4)
+    q = rows[:, base // 4: base // 4 + s.hidden // 8].astype(np.uint64).reshape(-1)
     nib = np.concatenate([(q >> np.uint64(4 * i)) & np.uint64(15) for i in range(8)])
     hist = np.bincount(nib.astype(np.int64), minlength=16) / nib.size
     assert np.all(np.abs(hist - 1 / 16) < 0.002)
-    sbw = blob[offs["gate_sb"] // 4: offs["up_q"] // 4]
+    base, stride = parts["gate_sb"]
+    sbw = rows[:, base // 4: base // 4 + s.hidden // 64].reshape(-1)
     sc = ((sbw & 0xFFFF).astype(np.uint32) << 16).view(np.float32)
     bi = ((sbw >> 16).astype(np.uint32) << 16).view(np.float32)
     assert sc.min() >= 0.0019 and sc.max() <= 0.0201
