@@ -81,6 +81,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Whether an mbarrier phase has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for an mbarrier phase, suspended (not spinning) for up to hint_ns.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
@@ -172,9 +185,14 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// named barrier over the consumer warps only
+// Block-wide barrier, counted per thread: the warps of this kernel take
+// different paths and may reach it diverged (a lane running a loop alone, a
+// row owner storing), which the aligned form (__syncthreads) does not allow.
+__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+
+// named barrier over the consumer warps only (per-thread count, as above)
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("barrier.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
 // Top-K key: larger key = larger logit, and among equal logits the lower
@@ -244,7 +262,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
 
   // Gate/up: this block owns rows [ra, ra+nr) of every slot.  The rows of
   // all slots form one sequence of NS*nr "virtual rows" (slot-major) that
-  // the ring carries R at a time; a consumer warp handles rows rs0 and rs1
+  // the ring carries R at a time; a gate/up warp handles rows rs0 and rs1
   // of each stage (its slice range `sl` of H).
   const int tl = H / kSlice;
   const int R = pl.rows_per_stage;
@@ -256,7 +274,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   const int nstg = (V + R - 1) / R;
   int rs0, sl, pi;
   if (tl >= 32) {
-    rs0 = warp / nparts;
+    rs0 = warp < (R / 2) * nparts ? warp / nparts : R;   // warps beyond a whole pass stay idle
     pi = warp % nparts;
     sl = pi * 32 + lane;
   } else {
@@ -282,19 +300,19 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], kConsumerWarps);
+      mbar_init(&bar_empty[i], kGuWarps);
     }
     for (int i = 0; i < kMaxSlots; ++i) {
       mbar_init(&bar_dfull[i], 1);
       mbar_init(&bar_routed[i], 1);
-      mbar_init(&bar_slot[i], kConsumerWarps);
+      mbar_init(&bar_slot[i], kGuWarps);
       mbar_init(&bar_hready[i], 1);
     }
     mbar_init(bar_xready, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  cta_sync();
 
   uint32_t g_issue = 0;   // gate/up stages issued (producer lane 0)
   uint32_t g_cons = 0;    // gate/up stages consumed (consumer warps)
@@ -395,11 +413,13 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           if (l == p.L - 1) hdst[r] = hv;
         }
       }
-    } else if (warp == kExchangeWarp) {
+    } else if (warp == kExchangeWarp || warp == kExchangeWarp2) {
       // ------------------------------------------------------------------
-      // exchanger: routing, then each slot's full h from L2 into shared memory
+      // exchangers: routing (the first), then each slot's full h from L2 into
+      // shared memory, the first exchanger taking even slots, the second odd
       // ------------------------------------------------------------------
-      {
+      const int xw = warp - kExchangeWarp;
+      if (xw == 0) {
         // top-K by repeated warp-wide max: each lane keeps the largest of its
         // logits (ties: lowest id); a round takes the warp maximum, the lowest
         // id holding it, and that lane rescans
@@ -458,19 +478,19 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_routed[0]);
       }
-      for (int q = 0; q < NS; ++q) {
+      unsigned long long* my_stage = s_stage + (size_t)xw * I;
+      for (int q = xw; q < NS; q += 2) {
         const unsigned long long* hsrc = p.hll + (size_t)hidx(q) * I;
         float* hsf = reinterpret_cast<float*>(s_hs + (size_t)q * pl.hs_slot_bytes);
-        float* hsum = hsf + (size_t)8 * hstride * 4;
         // fetch all I words of the slot, then re-fetch until every tag is current
         uint64_t t0 = 0;
         bool started = false;
         while (true) {
-          for (int c2 = lane; c2 < I / 2; c2 += 32) cp_async16(s_stage + 2 * c2, hsrc + 2 * c2);
+          for (int c2 = lane; c2 < I / 2; c2 += 32) cp_async16(my_stage + 2 * c2, hsrc + 2 * c2);
           cp_async_wait_all();
           __syncwarp();
           bool ok = true;
-          for (int i = lane; i < I; i += 32) ok = ok && ll_is(s_stage[i], tag);
+          for (int i = lane; i < I; i += 32) ok = ok && ll_is(my_stage[i], tag);
           if (__all_sync(0xFFFFFFFFu, ok)) break;
           if (*s_abort) break;
           const uint64_t t = global_timer_ns();
@@ -484,45 +504,21 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           }
           __nanosleep(32);
         }
-        // pre-scale into the padded slice-major layout; lane = position in
-        // the slice, 32 slices at a time, then a transposed reduction leaves
-        // slice g+lane's sum in lane `lane`
+        // pre-scale into the padded slice-major layout; lane = position in the
+        // slice, so that the reads are consecutive and the stores hit 32 banks
         const float ps_l = pos_scale<BITS>(lane);
         const int fo = ((lane >> 2) * hstride) * 4 + (lane & 3);
-        for (int g = 0; g < tld; g += 32) {
-          float v[32];
-#pragma unroll
-          for (int mm = 0; mm < 32; ++mm) {
-            const int m = g + mm;
-            v[mm] = 0.f;
-            if (m < tld) {
-              v[mm] = ll_value(s_stage[(size_t)m * kSlice + lane]);
-              hsf[fo + m * 4] = v[mm] * ps_l;
-            }
-          }
-#pragma unroll
-          for (int w = 16; w >= 1; w >>= 1) {
-            const bool up = (lane & w) != 0;
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-              const float send = up ? v[i] : v[i + w];
-              const float keep = up ? v[i + w] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
-            }
-          }
-          if (g + lane < tld) hsum[g + lane] = v[0];
-        }
+#pragma unroll 8
+        for (int m = 0; m < tld; ++m) hsf[fo + m * 4] = ll_value(my_stage[(size_t)m * kSlice + lane]) * ps_l;
         __threadfence_block();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_hready[q]);
       }
     } else {
       // ------------------------------------------------------------------
-      // consumers
+      // consumers: 12 gate/up warps and 4 down warps
       // ------------------------------------------------------------------
-      SliceX xs;
-      float xsum;
-      float resv[kMaxDownGroups];
+      float rinv;
       {
         // The layer input goes through shared memory, slice-major (float4 j of
         // slice s at j*tl + s), so that each lane then reads its slice without
@@ -562,24 +558,102 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           tot += s_red[2 * q];
           wgt += s_red[2 * q + 1];
         }
-        const float rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
+        rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
         if (warp == 0 && lane == 0) {
           const float gate = p.S ? sigmoid_f(wgt * rinv) : 0.f;
           if (p.S) s_w[0] = gate;
           if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
           mbar_arrive(bar_xready);
         }
-        xsum = 0.f;
+      }
+
+      if (warp < kGuWarps) {
+        // ---------------- gate/up: stream the ring, partial sums to smem ----
+        SliceX xs;
+        float xsum = 0.f;
 #pragma unroll
         for (int j = 0; j < kSlice / 4; ++j) {
           const float4 v = s_x4[j * tl + sl];
           xsum += put_x4<BITS>(xs, j, make_float4(v.x * rinv, v.y * rinv, v.z * rinv, v.w * rinv));
         }
+        int next_done = 0;
+        if (nr == 0) {               // no gate/up rows here: every slot is complete at once
+          __syncwarp();
+          if (lane == 0)
+            for (int ps = 0; ps < NS; ++ps) mbar_arrive(&bar_slot[ps]);
+          next_done = NS;
+        }
+        for (int k = 0; k < nstg; ++k) {
+          const uint32_t st = g_cons % pl.nstage;
+          mbar_wait(&bar_full[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
+          ++g_cons;
+          const uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
+          const int v0 = k * R + rs0, v1 = k * R + rs1;
+          float ga0 = 0.f, ua0 = 0.f, ga1 = 0.f, ua1 = 0.f;
+          if (rs0 < R / 2 && v0 < V) {
+            const uint8_t* rec = buf + (size_t)rs0 * lay.gu_row;
+            SliceCodes<BITS> qg, qu;
+            if constexpr (BITS == 4) {
+              qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
+              qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
+            } else {
+              qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
+              qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
+            }
+            const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
+            const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
+            ga0 = slice_term<BITS>(qg, sg, xs, xsum);
+            ua0 = slice_term<BITS>(qu, su, xs, xsum);
+          }
+          if (rs0 < R / 2 && v1 < V) {
+            const uint8_t* rec = buf + (size_t)rs1 * lay.gu_row;
+            SliceCodes<BITS> qg, qu;
+            if constexpr (BITS == 4) {
+              qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
+              qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
+            } else {
+              qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
+              qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
+            }
+            const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
+            const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
+            ga1 = slice_term<BITS>(qg, sg, xs, xsum);
+            ua1 = slice_term<BITS>(qu, su, xs, xsum);
+          }
+          const float v = quad_reduce(ga0, ua0, ga1, ua1, gw, lane);
+          const int pos = lane & (gw - 1), qw = gw >> 2;
+          const int vv = pos < 2 * qw ? v0 : v1;
+          if (rs0 < R / 2 && vv < V && (pos & (qw - 1)) == 0) {
+            const int ps = vv / nr, r = vv % nr;
+            s_part[(((size_t)ps * pl.nrmax + r) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_empty[st]);
+          // slots whose last row was in this stage are complete
+          const int last_v = min(V, (k + 1) * R);
+          bool fenced = false;
+          while (next_done < NS && (next_done + 1) * nr <= last_v) {
+            if (!fenced) {
+              __threadfence_block();
+              __syncwarp();
+              fenced = true;
+            }
+            if (lane == 0) mbar_arrive(&bar_slot[next_done]);
+            ++next_done;
+          }
+        }
+      } else {
+        // ---------------- down projection + combine + residual -------------
+        const int dw = warp - kGuWarps;
+        float acc[kMaxDownGroups];
+        float resv[kMaxDownGroups];
 #pragma unroll
         for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-          const int r = (warp + kConsumerWarps * gi) * rpp + lane / lpr;
+          const int grp = dw + kDownWarps * gi;
+          const int r = grp * rpp + lane / lpr;
+          acc[gi] = 0.f;
           resv[gi] = 0.f;
-          if ((warp + kConsumerWarps * gi) < ngroups && r < nd && (lane % lpr) == 0) {
+          if (grp < ngroups && r < nd && (lane % lpr) == 0) {
             if (p.norm) {
               const int e = ja + r;
               resv[gi] = reinterpret_cast<const float*>(s_x4)[(((e & 31) >> 2) * tl + (e >> 5)) * 4 + (e & 3)];
@@ -588,128 +662,68 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             }
           }
         }
-      }
-      float acc[kMaxDownGroups];
+        for (int ps = 0; ps < NS; ++ps) {
+          mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
+          mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
+          const float wk = s_w[ps];
+          const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
+          const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
+          for (int k = 0; k < spl; ++k) {
+            const int s = (lane % lpr) + 32 * k;
+            SliceX hs;
+            // the slice's plain sum, from the pre-scaled values: one partial sum
+            // per position class (an exact power-of-two rescaling each)
+            float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
+            float2 c45 = make_float2(0.f, 0.f), c67 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < kMaxDownGroups; ++i) acc[i] = 0.f;
-
-      auto down = [&](int ps) {
-        mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
-        mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
-        const float wk = s_w[ps];
-        const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
-        const float* hsum = reinterpret_cast<const float*>(s_hs + (size_t)ps * pl.hs_slot_bytes) + (size_t)8 * hstride * 4;
-        const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
-        for (int k = 0; k < spl; ++k) {
-          const int s = (lane % lpr) + 32 * k;
-          SliceX hs;
+            for (int j = 0; j < kSlice / 4; ++j) {
+              const float4 v = hs4[(size_t)j * hstride + s];
+              hs[2 * j] = make_float2(v.x, v.y);
+              hs[2 * j + 1] = make_float2(v.z, v.w);
+              if (BITS == 4 || (j & 1) == 0) {
+                c01 = __fadd2_rn(c01, hs[2 * j]);
+                c23 = __fadd2_rn(c23, hs[2 * j + 1]);
+              } else {
+                c45 = __fadd2_rn(c45, hs[2 * j]);
+                c67 = __fadd2_rn(c67, hs[2 * j + 1]);
+              }
+            }
+            float hsm = (c01.x / pos_scale<BITS>(0) + c01.y / pos_scale<BITS>(1)) +
+                        (c23.x / pos_scale<BITS>(2) + c23.y / pos_scale<BITS>(3));
+            if (BITS == 2)
+              hsm += (c45.x / pos_scale<BITS>(4) + c45.y / pos_scale<BITS>(5)) +
+                     (c67.x / pos_scale<BITS>(6) + c67.y / pos_scale<BITS>(7));
 #pragma unroll
-          for (int j = 0; j < kSlice / 4; ++j) {
-            const float4 v = hs4[(size_t)j * hstride + s];
-            hs[2 * j] = make_float2(v.x, v.y);
-            hs[2 * j + 1] = make_float2(v.z, v.w);
-          }
-          const float hsm = hsum[s];
-#pragma unroll
-          for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-            const int grp = warp + kConsumerWarps * gi;
-            const int r = grp * rpp + lane / lpr;
-            if (grp < ngroups && r < nd) {
-              const uint8_t* rec = buf + (size_t)r * lay.d_row;
-              SliceCodes<BITS> q;
-              if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
-              else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
-              const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
-              acc[gi] = fmaf(wk, slice_term<BITS>(q, sbw, hs, hsm), acc[gi]);
+            for (int gi = 0; gi < kMaxDownGroups; ++gi) {
+              const int grp = dw + kDownWarps * gi;
+              const int r = grp * rpp + lane / lpr;
+              if (grp < ngroups && r < nd) {
+                const uint8_t* rec = buf + (size_t)r * lay.d_row;
+                SliceCodes<BITS> q;
+                if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
+                else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
+                const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
+                acc[gi] = fmaf(wk, slice_term<BITS>(q, sbw, hs, hsm), acc[gi]);
+              }
             }
           }
         }
-      };
-
-      int next_done = 0, next_down = 0;
-      if (nr == 0) {                 // no gate/up rows here: every slot is complete at once
-        __syncwarp();
-        if (lane == 0)
-          for (int ps = 0; ps < NS; ++ps) mbar_arrive(&bar_slot[ps]);
-        next_done = NS;
-      }
-      for (int k = 0; k < nstg; ++k) {
-        const uint32_t st = g_cons % pl.nstage;
-        mbar_wait(&bar_full[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
-        ++g_cons;
-        const uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
-        const int v0 = k * R + rs0, v1 = k * R + rs1;
-        float ga0 = 0.f, ua0 = 0.f, ga1 = 0.f, ua1 = 0.f;
-        if (v0 < V) {
-          const uint8_t* rec = buf + (size_t)rs0 * lay.gu_row;
-          SliceCodes<BITS> qg, qu;
-          if constexpr (BITS == 4) {
-            qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
-            qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
-          } else {
-            qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
-            qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
-          }
-          const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
-          const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
-          ga0 = slice_term<BITS>(qg, sg, xs, xsum);
-          ua0 = slice_term<BITS>(qu, su, xs, xsum);
-        }
-        if (v1 < V) {
-          const uint8_t* rec = buf + (size_t)rs1 * lay.gu_row;
-          SliceCodes<BITS> qg, qu;
-          if constexpr (BITS == 4) {
-            qg.v = *reinterpret_cast<const uint4*>(rec + (size_t)sl * 16);
-            qu.v = *reinterpret_cast<const uint4*>(rec + lay.qh + (size_t)sl * 16);
-          } else {
-            qg.v = *reinterpret_cast<const uint2*>(rec + (size_t)sl * 8);
-            qu.v = *reinterpret_cast<const uint2*>(rec + lay.qh + (size_t)sl * 8);
-          }
-          const uint32_t sg = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + (size_t)(sl >> 1) * 4);
-          const uint32_t su = *reinterpret_cast<const uint32_t*>(rec + 2 * lay.qh + lay.sh + (size_t)(sl >> 1) * 4);
-          ga1 = slice_term<BITS>(qg, sg, xs, xsum);
-          ua1 = slice_term<BITS>(qu, su, xs, xsum);
-        }
-        const float v = quad_reduce(ga0, ua0, ga1, ua1, gw, lane);
-        const int pos = lane & (gw - 1), qw = gw >> 2;
-        const int vv = pos < 2 * qw ? v0 : v1;
-        if (vv < V && (pos & (qw - 1)) == 0) {
-          const int ps = vv / nr, r = vv % nr;
-          s_part[(((size_t)ps * pl.nrmax + r) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_empty[st]);
-        // slots whose last row was in this stage are complete
-        const int last_v = min(V, (k + 1) * R);
-        bool fenced = false;
-        while (next_done < NS && (next_done + 1) * nr <= last_v) {
-          if (!fenced) {
-            __threadfence_block();
-            __syncwarp();
-            fenced = true;
-          }
-          if (lane == 0) mbar_arrive(&bar_slot[next_done]);
-          ++next_done;
-        }
-        while (next_down < next_done - dlag) down(next_down++);
-      }
-      while (next_down < NS) down(next_down++);
-
-      // combine + residual, written by each row's owner
+        // combine + residual, written by each row's owner
 #pragma unroll
-      for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-        const int grp = warp + kConsumerWarps * gi;
-        const float v = warp_sum(acc[gi], lpr);
-        const int r = grp * rpp + lane / lpr;
-        if (grp < ngroups && r < nd && (lane % lpr) == 0) {
-          if (out_ll) ll_store(out_llp + ja + r, resv[gi] + v, tag);
-          else p.out[ja + r] = resv[gi] + v;
+        for (int gi = 0; gi < kMaxDownGroups; ++gi) {
+          const int grp = dw + kDownWarps * gi;
+          const float v = warp_sum(acc[gi], lpr);
+          const int r = grp * rpp + lane / lpr;
+          if (grp < ngroups && r < nd && (lane % lpr) == 0) {
+            if (out_ll) ll_store(out_llp + ja + r, resv[gi] + v, tag);
+            else p.out[ja + r] = resv[gi] + v;
+          }
         }
       }
     }
 
     // ---- end of layer: every role is done with this layer's shared memory ----
-    __syncthreads();
+    cta_sync();
   }
 
   // No copy may still be writing this block's shared memory when it exits:
@@ -726,7 +740,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   }
 
   // the last block out starts the next epoch of tags and resets the exit count
-  __syncthreads();
+  cta_sync();
   if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(p.exit_ctr, 1u);
@@ -759,20 +773,21 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
   const BlobLayout lay = blob_layout(bits, H, I);
   // gate/up stage: two rows per consumer warp and slice range
   const int nparts = tl >= 32 ? tl / 32 : 1;
-  const int R = 2 * (tl >= 32 ? kConsumerWarps / nparts : kConsumerWarps * (32 / tl));
+  if (nparts > kGuWarps) return pl;
+  const int R = 2 * (tl >= 32 ? kGuWarps / nparts : kGuWarps * (32 / tl));
   pl.rows_per_stage = R;
   pl.nparts = nparts;
   pl.stage_bytes = round_up_i((long long)R * lay.gu_row, 128);
   // down records of one slot
   const int ndmax = (H + grid - 1) / grid;
   const int lpr = tld < 32 ? tld : 32, rpp = 32 / lpr;
-  if ((ndmax + rpp - 1) / rpp > kMaxDownGroups * kConsumerWarps) return pl;
+  if ((ndmax + rpp - 1) / rpp > kMaxDownGroups * kDownWarps) return pl;
   pl.dslot_bytes = round_up_i((long long)ndmax * lay.d_row, 128);
   pl.nrmax = (I + grid - 1) / grid;
-  pl.hs_slot_bytes = round_up_i((long long)8 * (tld + 1) * 16 + (long long)tld * 4, 128);
+  pl.hs_slot_bytes = round_up_i((long long)8 * (tld + 1) * 16, 128);
   pl.part_off = kCtrlBytes;
   pl.stage_off = round_up_i(pl.part_off + (long long)NS * pl.nrmax * nparts * 2 * 4, 128);
-  pl.hs_off = round_up_i(pl.stage_off + (long long)I * 8, 128);
+  pl.hs_off = round_up_i(pl.stage_off + (long long)2 * I * 8, 128);
   // the layer input is staged where the slots' h will go: it is read by the
   // consumers before their first gate/up stage, and the first h is written
   // only after every block has finished a slot

@@ -31,11 +31,14 @@ cudaError_t launch_down_combine(const GenericArgs& a, cudaStream_t st);
 // ---------------------------------------------------------------------------
 // single-launch persistent kernel (fmoe_fused.cu)
 // ---------------------------------------------------------------------------
-constexpr int kConsumerWarps = 16;                     // dequant GEMV warps
+constexpr int kGuWarps = 12;                           // dequantised gate/up GEMV warps
+constexpr int kDownWarps = 4;                          // down projection + combine warps
+constexpr int kConsumerWarps = kGuWarps + kDownWarps;  // warps that hold the layer input
 constexpr int kProducerWarp = kConsumerWarps;          // issues the bulk copies
 constexpr int kFinalWarp = kConsumerWarps + 1;         // turns partial sums into h rows
-constexpr int kExchangeWarp = kConsumerWarps + 2;      // gathers every block's h rows
-constexpr int kFusedThreads = 32 * (kConsumerWarps + 3);
+constexpr int kExchangeWarp = kConsumerWarps + 2;      // routes; gathers the h of even slots
+constexpr int kExchangeWarp2 = kConsumerWarps + 3;     // gathers the h of odd slots
+constexpr int kFusedThreads = 32 * (kConsumerWarps + 4);
 // registers per thread: the most that every warp can hold when the warps are
 // spread over the SM's four schedulers, each with 16K registers (8 at a time)
 constexpr int kFusedWarpsPerScheduler = (kFusedThreads / 32 + 3) / 4;
@@ -43,8 +46,8 @@ constexpr int kFusedMaxRegs = (16384 / (kFusedWarpsPerScheduler * 32)) / 8 * 8;
 constexpr int kMaxFusedLayers = 64;    // layers per launch; longer stacks use several launches
 constexpr int kMaxSlots = FMOE_MAX_TOPK + 1;
 constexpr int kMaxStages = 16;
-constexpr int kMaxDownGroups = 4;      // down row groups per consumer warp
-constexpr int kCtrlBytes = 2048;       // barriers, routing result, reductions
+constexpr int kMaxDownGroups = 8;      // down row groups per down warp
+constexpr int kCtrlBytes = 1536;       // barriers, routing result, reductions
 
 struct FusedLayerPtrs {
   const uint8_t* experts;
