@@ -45,7 +45,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fmoe", choices=["fmoe", "reference"])
     ap.add_argument("--workload", default="qwen_q4",
-                    choices=["qwen_q4", "qwen_q2", "stack48", "tiny"])
+                    choices=["qwen_q4", "qwen_q2", "stack48", "tiny", "qwen_q4_zipf"])
+    ap.add_argument("--tokens", type=int, default=16,
+                    help="T of the batched Zipf workload (qwen_q4_zipf): 1..16")
     ap.add_argument("--chain", type=int, default=CHAIN,
                     help="blocks per step for the single-block workloads (1..64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -69,6 +71,8 @@ def workload_desc(name, chain=CHAIN):
         return synth.STACK48, synth.STACK48.n_layers
     if name == "tiny":
         return synth.TINY, chain
+    if name == "qwen_q4_zipf":
+        return synth.QWEN_Q4_BATCH, chain
     raise ValueError(name)
 
 
@@ -175,6 +179,7 @@ class ClockSampler:
 # committed ncu traffic summary (null when the kernel sources changed since)
 # ---------------------------------------------------------------------------
 KERNEL_SOURCES = ["quantized_moe_expert_05_b300/csrc/fmoe_fused.cu",
+                  "quantized_moe_expert_05_b300/csrc/fmoe_async.cuh",
                   "quantized_moe_expert_05_b300/csrc/fmoe_internal.cuh",
                   "quantized_moe_expert_05_b300/csrc/fmoe_kernels.cuh"]
 
@@ -200,6 +205,22 @@ def committed_traffic(workload):
             if parts[2] == want:
                 return float(parts[1])
     return None
+
+
+def max_over_ranks(vals, device, world):
+    """Element-wise maximum of `vals` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(bytes_per_step, steps, world, ms):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time (ms)."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
 
 
 def load_peaks():
@@ -314,12 +335,106 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# batched block with Zipf routing: unique-expert bytes per second
+# ---------------------------------------------------------------------------
+def run_batch(args):
+    """T tokens through one Qwen-shaped 4-bit block (fmoe_moe_block, batched
+    path) with Zipf(1.1) routing; value = distinct experts' bytes (routed +
+    shared) per second.  Each step is one graph replay of the block's launches
+    over one of NSETS input sets.  L2 is flushed before every timed step,
+    outside its events, by a read of 256 MiB: that leaves L2 holding clean
+    lines only (a write would leave dirty lines whose write-back would land in
+    the timed region)."""
+    import torch
+    from quantized_moe_expert_05_b300 import build
+    build.build()
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    T = args.tokens
+    if not 1 <= T <= 16:
+        raise ValueError("--tokens must be in 1..16")
+    shape = synth.QWEN_Q4_BATCH
+    K = shape.top_k
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+    pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
+    synth.fill_pool(pool, shape, 0, 0, shape.n_experts)
+    shared = torch.empty(nw, dtype=torch.int32, device=dev)
+    synth.fill_pool(shared, shape, 0, shape.n_experts, 1)
+    layer = fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool, shared,
+                     synth.shared_gate_vector(shape).to(dev))
+    ws = fm.new_workspace(layer, T, K)
+    NSETS = 8
+    sets = [synth.block_inputs(shape, T, tag=100 + i) for i in range(NSETS)]
+    xs = [s_.x.to(dev) for s_ in sets]
+    lgs = [s_.logits.to(dev) for s_ in sets]
+    res = [s_.residual.to(dev) for s_ in sets]
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device=dev)
+    # distinct experts per set (from the routing the library leaves in the workspace)
+    uniq = []
+    for i in range(NSETS):
+        fm.moe_block(layer, xs[i], lgs[i], res[i], K, ws, out=out)
+        ids = fm.ws_routing(ws, layer, T, K)["ids"]
+        uniq.append(len(set(ids.flatten().tolist())) + 1)
+    torch.cuda.synchronize()
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device error in the batched block")
+    blob = synth.blob_bytes(shape.bits, shape.hidden, shape.inter)
+    graphs = []
+    for i in range(NSETS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fm.moe_block(layer, xs[i], lgs[i], res[i], K, ws, out=out)
+        graphs.append(g)
+    flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        graphs[i % NSETS].replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    nbytes = 0
+    with ClockSampler(0) as clocks:
+        for i in range(args.steps):
+            flush.sum()
+            evs[i][0].record(stream)
+            graphs[i % NSETS].replay()
+            evs[i][1].record(stream)
+            nbytes += uniq[i % NSETS] * blob
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device error in the timed region")
+    value = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    line = {
+        "metric": "unique-expert GB/s (batched block, Zipf routing)", "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{shape.name}: T={T} tokens through one block, Zipf(1.1) routing",
+                   "distinct_experts_per_step": uniq, "l2": "flushed (256 MiB read) before every step"},
+        "tokens_per_s": T * args.steps / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)", "traffic": None,
+                     "kernel": "plan + gate/up + down + combine (4 launches, one graph)"},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # CUDA path
 # ---------------------------------------------------------------------------
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "qwen_q4_zipf":
+        return run_batch(args)
 
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -468,16 +583,11 @@ def main():
     d2h = shape.hidden * 4
 
     # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev, world)
 
     per_step = bytes_per_token(shape, n_layers)
-    total_bytes = per_step * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    value = job_gbs(per_step, args.steps, world, ms)
+    e2e_value = job_gbs(per_step, args.steps, world, e2e_ms)
     ms_step = ms / args.steps
     # algorithmic bytes of one fused launch over its average launch time
     achieved = per_step / (kernel_ms * 1e-3) / 1e9
