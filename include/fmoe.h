@@ -136,6 +136,10 @@ fmoe_status fmoe_route(const float* logits, int T, int E, int K,
  *   x    fp32  [T][H]
  *   y    fp32  [T][K+S][H]    out, unweighted (S = has_shared)
  *   ws   workspace of fmoe_workspace_bytes(layer, T, K, 1) bytes
+ * Each distinct expert among the T*K ids (and the shared expert) is read
+ * once, whatever the number of tokens that use it.  An id outside [0, E) is
+ * not read: its y row is zero and the workspace error word records it
+ * (fmoe_last_device_error then returns FMOE_ERR_INVALID_ARG).
  */
 fmoe_status fmoe_expert_ffn(const fmoe_layer* layer /* host */, const int32_t* ids,
                             int T, int K, const float* x, float* y,
@@ -149,8 +153,11 @@ fmoe_status fmoe_expert_ffn(const fmoe_layer* layer /* host */, const int32_t* i
  * (the sigmoid term only if layer->has_shared).
  *   x, residual, out  fp32 [T][H];  router_logits fp32 [T][E]
  *   out may alias residual; it must not overlap x or router_logits.
- * With T > 1 each distinct expert among the T*K picks is read once.  The
- * routing result is left in the workspace (see fmoe_ws_routing).
+ * T = 1 runs as one persistent launch when the shape fits it; otherwise
+ * (and for every T > 1) four launches: plan, gate/up, down, combine, in
+ * which each distinct expert among the T*K picks is read once (see
+ * fmoe_ws_batch_plan).  The routing result is left in the workspace (see
+ * fmoe_ws_routing).
  */
 fmoe_status fmoe_moe_block(const fmoe_layer* layer /* host */, const float* x,
                            const float* router_logits, const float* residual,
@@ -182,6 +189,21 @@ fmoe_status fmoe_stack_decode(const fmoe_layer* layers /* host */, int L,
  */
 fmoe_status fmoe_ws_routing(void* ws, const fmoe_layer* layer /* host */, int T, int K,
                             int32_t** ids, float** weights, float** gate, float** h);
+
+/*
+ * Device pointer, inside a workspace, to the batch plan written by the last
+ * fmoe_expert_ffn call or batched fmoe_moe_block call (T > 1) on it:
+ *   plan[0]  number of items;  plan[1]  distinct experts read (shared incl.)
+ *   item i at plan + 8 + 8*i:  [0] expert id (-1: shared expert)
+ *                              [1] n, the item's tokens (1..4)
+ *                              [2+g], g < n: (t << 8) | slot of token g
+ * A distinct expert picked by m tokens has ceil(m/G) items (G = 4, or 2 or 1
+ * for shapes whose staged inputs leave no room for four tokens), listed in
+ * order of first appearance in ids (token-major); its codes are read from
+ * HBM once.
+ * Diagnostic; host function, no sync.
+ */
+fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer /* host */, int T, int K, int32_t** plan);
 
 /* Static description of a status code (host). */
 const char* fmoe_status_string(fmoe_status s);

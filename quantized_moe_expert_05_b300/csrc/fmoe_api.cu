@@ -52,6 +52,8 @@ struct Ws {
   float* weights() const { return reinterpret_cast<float*>(base + lay.weights); }
   float* gate() const { return reinterpret_cast<float*>(base + lay.gate); }
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
+  float* y() const { return reinterpret_cast<float*>(base + lay.y); }
+  int32_t* plan() const { return reinterpret_cast<int32_t*>(base + lay.plan); }
 };
 
 Ws carve(void* ws, const fmoe_layer* L, int T, int K, int n_layers) {
@@ -61,8 +63,8 @@ Ws carve(void* ws, const fmoe_layer* L, int T, int K, int n_layers) {
   return w;
 }
 
-GenericArgs generic_args(const fmoe_layer* L, int T, int K, const Ws& w) {
-  GenericArgs a{};
+BatchArgs batch_args(const fmoe_layer* L, int T, int K, const Ws& w) {
+  BatchArgs a{};
   a.bits = L->bits;
   a.H = L->hidden;
   a.I = L->inter;
@@ -74,8 +76,14 @@ GenericArgs generic_args(const fmoe_layer* L, int T, int K, const Ws& w) {
   a.blob = a.lay.bytes;
   a.experts = static_cast<const uint8_t*>(L->experts);
   a.shared = static_cast<const uint8_t*>(L->shared);
+  a.ids = w.ids();
+  a.weights = w.weights();
+  a.gate = w.gate();
   a.h = w.h();
+  a.y = w.y();
+  a.plan = w.plan();
   a.err = w.err();
+  a.timeout_ns = kTimeoutNs;
   return a;
 }
 
@@ -125,12 +133,11 @@ fmoe_status fmoe_expert_ffn(const fmoe_layer* layer, const int32_t* ids, int T, 
     return FMOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ws w = carve(ws, layer, T, K, 1);
-  GenericArgs a = generic_args(layer, T, K, w);
-  a.ids = ids;
+  BatchArgs a = batch_args(layer, T, K, w);
+  a.ids_in = ids;
   a.x = x;
-  cudaError_t e = launch_gateup_generic(a, st);
-  if (e == cudaSuccess) e = launch_down_y(a, y, st);
-  return from_cuda(e);
+  a.y = y;
+  return from_cuda(launch_batch(a, y, st));
 }
 
 fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float* router_logits,
@@ -193,19 +200,15 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float*
       return from_cuda(launch_fused(p, pl, st));
     }
   }
-  // general path: route (+ gate), gate/up + SwiGLU, down + combine
-  GenericArgs a = generic_args(layer, T, K, w);
-  a.ids = w.ids();
-  a.weights = w.weights();
-  a.gate = w.gate();
+  // batched path: plan (route, shared gate, distinct experts), gate/up +
+  // SwiGLU, down, combine
+  BatchArgs a = batch_args(layer, T, K, w);
+  a.logits = router_logits;
+  a.wsg = S ? layer->shared_gate_w : nullptr;
   a.x = x;
   a.residual = residual;
   a.out = out;
-  cudaError_t e = launch_route(router_logits, T, layer->n_experts, K, w.ids(), w.weights(),
-                               S ? layer->shared_gate_w : nullptr, x, layer->hidden, w.gate(), st);
-  if (e == cudaSuccess) e = launch_gateup_generic(a, st);
-  if (e == cudaSuccess) e = launch_down_combine(a, st);
-  return from_cuda(e);
+  return from_cuda(launch_batch(a, a.y, st));
 }
 
 fmoe_status fmoe_stack_decode(const fmoe_layer* layers, int L, const float* logits, float* h, int K, float eps,
@@ -278,6 +281,13 @@ fmoe_status fmoe_ws_routing(void* ws, const fmoe_layer* layer, int T, int K, int
   if (weights) *weights = w.weights();
   if (gate) *gate = w.gate();
   if (h) *h = w.h();
+  return FMOE_OK;
+}
+
+fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer, int T, int K, int32_t** plan) {
+  if (ws == nullptr || layer == nullptr || plan == nullptr || T < 1 || K < 1) return FMOE_ERR_INVALID_ARG;
+  if (check_layer(layer, false) != FMOE_OK) return FMOE_ERR_INVALID_ARG;
+  *plan = carve(ws, layer, T, K, 1).plan();
   return FMOE_OK;
 }
 

@@ -1,0 +1,737 @@
+// Routing kernel and the batched (T >= 1 tokens) expert kernels.
+//
+// The single-launch persistent kernel (fmoe_fused.cu) is the fast path for one
+// token; these kernels serve every shape the ABI accepts at any T, and read
+// each DISTINCT expert of a batch once: when several tokens pick the same
+// expert, its codes are dequantised once per 32-column slice and applied to
+// all of those tokens from registers.  The write-ups stream experts for one
+// token at a time; their failed-experiments table notes that per-token expert
+// I/O is what makes batching (speculative decoding) pay nothing, which is the
+// cost this deduplication removes for resident experts.
+//
+// Sequence (four launches on one stream, graph-capturable):
+//   batch_plan_kernel    route (top-K + softmax, shared gate) or take given
+//                        ids; list the distinct experts and, for each, the
+//                        tokens that picked it, in groups of G <= 4
+//   batch_gateup_kernel  h[t][k] = silu(Wg x_t) * (Wu x_t) for every (expert,
+//                        token group) item, 2 intermediate rows per warp
+//   batch_down_kernel    y[t][k] = Wd h[t][k], 4 output rows per warp
+//   batch_combine_kernel out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
+// The two expert kernels run one block per SM over a contiguous share of
+// (item, row block) work units: a producer warp streams each unit's packed
+// rows (one contiguous range of the blob) into a shared-memory ring with
+// bulk asynchronous copies (TMA engine, mbarrier completion), eight consumer
+// warps compute from the ring.
+//
+// Sources: flash-moe write-up (discuss.pytorch.kr): "per-layer pipeline"
+// (softmax + top-K routing, expert forward, combine), "hand-written Metal
+// compute shaders" (dequant matvec, fused SwiGLU, MoE combine + residual +
+// sigmoid gate), "FMA-optimised dequant kernel" (code * scale + bias).
+#include <algorithm>
+
+#include "fmoe_async.cuh"
+#include "fmoe_kernels.cuh"
+
+namespace fmoe {
+
+// One warp per token: top-K + softmax, and the shared-expert gate
+// g = sigmoid(w_sg . x) when wsg != nullptr.
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int K,
+                             int32_t* __restrict__ ids, float* __restrict__ weights,
+                             const uint16_t* __restrict__ wsg, const float* __restrict__ x, int H,
+                             float* __restrict__ gate) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int id; float w;
+  warp_route(logits + (size_t)t * E, E, K, id, w);
+  if (lane < K) {
+    ids[(size_t)t * K + lane] = id;
+    weights[(size_t)t * K + lane] = w;
+  }
+  if (gate != nullptr) {
+    float acc = 0.f;
+    if (wsg != nullptr) {
+      for (int c = lane; c < H; c += 32) acc += bf16v(wsg[c]) * x[(size_t)t * H + c];
+      acc = warp_sum(acc);
+    }
+    if (lane == 0) gate[t] = (wsg != nullptr) ? sigmoid_f(acc) : 0.f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// plan: distinct experts and their token groups
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 512;
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kMaxPairs = FMOE_MAX_TOKENS * FMOE_MAX_TOPK;
+static_assert(kMaxPairs <= kPlanThreads, "one thread per (token, slot) pair");
+static_assert(FMOE_MAX_TOKENS <= kPlanWarps, "one warp per token");
+static_assert(kPlanHeader == 8 && kItemWords == 8, "ws_layout sizes the plan for these");
+
+// Item i of the plan (kItemWords int32 at plan + kPlanHeader + i * kItemWords):
+//   [0] expert id (-1: the shared expert)   [1] n tokens (1..G)
+//   [2 + g] (t << 8) | slot of the g-th token: h[t][slot] / y[t][slot]
+__global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
+  __shared__ int s_id[kMaxPairs];
+  __shared__ int s_rank[kMaxPairs];   // earlier pairs with the same expert
+  __shared__ int s_cnt[kMaxPairs];    // all pairs with the same expert
+  __shared__ int s_first[kMaxPairs];  // first pair with the same expert
+  __shared__ int s_base[kMaxPairs];   // first item of the expert (valid at first pairs)
+  __shared__ float s_gpart[kPlanWarps][FMOE_MAX_TOKENS];
+  __shared__ int s_nitems, s_nuniq;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, K = a.K, NS = a.K + a.S, TK = a.T * a.K, G = a.geo.G;
+
+  if (a.logits != nullptr) {
+    if (warp < T) {
+      int id; float w;
+      warp_route(a.logits + (size_t)warp * a.E, a.E, K, id, w);
+      if (lane < K) {
+        a.ids[warp * K + lane] = id;
+        a.weights[warp * K + lane] = w;
+        s_id[warp * K + lane] = id;
+      }
+    }
+    if (a.S) {
+      // w_sg . x_t for every token: warp w takes a sixteenth of the columns
+      // of all tokens, so that every load of the block is in flight at once
+      const int H4 = a.H / 4, per = (H4 + kPlanWarps - 1) / kPlanWarps;
+      const int c0 = warp * per, c1 = min(H4, c0 + per);
+      const uint2* w4 = reinterpret_cast<const uint2*>(a.wsg);
+      const float4* x4 = reinterpret_cast<const float4*>(a.x);
+      float acc[FMOE_MAX_TOKENS];
+#pragma unroll
+      for (int t = 0; t < FMOE_MAX_TOKENS; ++t) acc[t] = 0.f;
+      for (int c = c0 + lane; c < c1; c += 32) {
+        const uint2 wv = __ldg(w4 + c);
+#pragma unroll
+        for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
+          if (t < T) {
+            const float4 xv = __ldcg(x4 + (size_t)t * H4 + c);
+            acc[t] = fmaf(bf16lo(wv.x), xv.x, acc[t]);
+            acc[t] = fmaf(bf16hi(wv.x), xv.y, acc[t]);
+            acc[t] = fmaf(bf16lo(wv.y), xv.z, acc[t]);
+            acc[t] = fmaf(bf16hi(wv.y), xv.w, acc[t]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
+        if (t < T) {
+          const float v = warp_sum(acc[t]);
+          if (lane == 0) s_gpart[warp][t] = v;
+        }
+      }
+    }
+  } else {
+    for (int p = tid; p < TK; p += kPlanThreads) {
+      int id = a.ids_in[p];
+      if (id < 0 || id >= a.E) {
+        atomicOr(a.err, kErrBadExpert);
+        id = -1;
+      }
+      s_id[p] = id;
+    }
+  }
+  __syncthreads();
+
+  if (a.logits != nullptr && a.S && tid < T) {
+    float g = 0.f;
+    for (int w = 0; w < kPlanWarps; ++w) g += s_gpart[w][tid];
+    a.gate[tid] = sigmoid_f(g);
+  }
+
+  // an expert id outside [0, E) leaves its output row zero
+  if (a.ids_in != nullptr) {
+    for (int p = 0; p < TK; ++p)
+      if (s_id[p] < 0) {
+        float* yrow = a.y + ((size_t)(p / K) * NS + (p % K)) * a.H;
+        for (int j = tid; j < a.H; j += kPlanThreads) yrow[j] = 0.f;
+      }
+  }
+
+  if (tid < TK) {
+    const int id = s_id[tid];
+    int rank = 0, cnt = 0, first = tid;
+    if (id >= 0) {
+      for (int q = 0; q < TK; ++q) {
+        if (s_id[q] == id) {
+          ++cnt;
+          if (q < tid) ++rank;
+          if (q < first) first = q;
+        }
+      }
+    }
+    s_rank[tid] = rank;
+    s_cnt[tid] = cnt;
+    s_first[tid] = first;
+  }
+  __syncthreads();
+
+  // items of each distinct expert, in order of first appearance
+  if (warp == 0) {
+    int base = 0, uniq = 0;
+    for (int c0 = 0; c0 < TK; c0 += 32) {
+      const int p = c0 + lane;
+      const bool lead = p < TK && s_id[p] >= 0 && s_rank[p] == 0;
+      const int n = lead ? (s_cnt[p] + G - 1) / G : 0;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (p < TK) s_base[p] = base + incl - n;
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      uniq += __popc(__ballot_sync(0xFFFFFFFFu, lead));
+    }
+    if (lane == 0) {
+      s_nitems = base;
+      s_nuniq = uniq;
+    }
+  }
+  __syncthreads();
+
+  int32_t* items = a.plan + kPlanHeader;
+  if (tid < TK && s_id[tid] >= 0) {
+    const int r = s_rank[tid];
+    const int it = s_base[s_first[tid]] + r / G;
+    const int g = r % G;
+    items[it * kItemWords + 2 + g] = ((tid / K) << 8) | (tid % K);
+    if (g == 0) {
+      items[it * kItemWords + 0] = s_id[tid];
+      items[it * kItemWords + 1] = min(G, s_cnt[tid] - r);
+    }
+  }
+  const int n_shared_items = a.S ? (T + G - 1) / G : 0;
+  if (a.S && tid < T) {
+    const int it = s_nitems + tid / G;
+    const int g = tid % G;
+    items[it * kItemWords + 2 + g] = (tid << 8) | K;
+    if (g == 0) {
+      items[it * kItemWords + 0] = -1;
+      items[it * kItemWords + 1] = min(G, T - tid);
+    }
+  }
+  if (tid == 0) {
+    a.plan[0] = s_nitems + n_shared_items;
+    a.plan[1] = s_nuniq + a.S;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// expert kernels: shared helpers
+// ---------------------------------------------------------------------------
+// Codes 8j..8j+7 of a 32-code slice (one "octet"), masked in place as the
+// pairs (2i, 2i+1), i = 0..3, that meet the pre-scaled inputs.
+__device__ __forceinline__ void octet_pairs(const SliceCodes<4>& q, int j, float2 (&p)[4]) {
+  const uint32_t w = (&q.v.x)[j];
+  const uint32_t hi = w >> 16;
+  p[0] = mk2(w, 0xFu, 0xF0u);
+  p[1] = mk2(w, 0xF00u, 0xF000u);
+  p[2] = mk2(hi, 0xFu, 0xF0u);
+  p[3] = mk2(hi, 0xF00u, 0xF000u);
+}
+
+__device__ __forceinline__ void octet_pairs(const SliceCodes<2>& q, int j, float2 (&p)[4]) {
+  const uint32_t w = (&q.v.x)[j >> 1] >> (16 * (j & 1));
+  p[0] = mk2(w, 0x3u, 0xCu);
+  p[1] = mk2(w, 0x30u, 0xC0u);
+  p[2] = mk2(w, 0x300u, 0xC00u);
+  p[3] = mk2(w, 0x3000u, 0xC000u);
+}
+
+// The codes of slice s of a row held in shared memory.
+template <int BITS>
+__device__ __forceinline__ SliceCodes<BITS> smem_codes(const uint8_t* row, int s) {
+  SliceCodes<BITS> q;
+  if constexpr (BITS == 4) q.v = reinterpret_cast<const uint4*>(row)[s];
+  else q.v = reinterpret_cast<const uint2*>(row)[s];
+  return q;
+}
+
+// Sum over the 32 lanes of 16 values per lane; lane L receives the total of
+// value index L >> 1 (lanes 2i and 2i+1 both hold total i).
+__device__ __forceinline__ float reduce16(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = 8; half >= 1; half >>= 1) {
+    const bool upper = (lane & (2 * half)) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2 * half);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
+}
+
+// Load the inputs of an item's tokens into shared memory, pre-scaled and
+// laid out [token][float4 index q within a slice][slice s] (rows of NSL+1
+// float4) so that the 32 lanes of a warp (consecutive slices) read
+// consecutive 16-byte words; and the plain sum of each slice.  src(i) is the
+// fp32 input of token i (n of them), NSL slices of 32 values.  Eight
+// consecutive threads take the eight float4 of one slice (coalesced global
+// reads, conflict-free stores thanks to the +1 row padding, slice sums by
+// three shuffles); each thread keeps kStageUnroll loads in flight.
+// Called by the nthreads consumer threads (a multiple of 32).
+constexpr int kStageUnroll = 8;
+
+template <int BITS, typename Src>
+__device__ __forceinline__ void stage_inputs(float4* xs4, float* xsum, int n, int NSL, int nthreads, Src src) {
+  const int per_tok = NSL * 8, total = n * per_tok, ld = NSL + 1;
+  const int tid = threadIdx.x;
+  for (int g0 = tid; g0 - tid < total; g0 += nthreads * kStageUnroll) {
+    float4 v[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int g = g0 + u * nthreads;
+      if (g < total) {
+        const int i = g / per_tok, rem = g - i * per_tok;
+        v[u] = __ldcg(reinterpret_cast<const float4*>(src(i)) + rem);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int g = g0 + u * nthreads;
+      float sum = 0.f;
+      if (g < total) {
+        const int i = g / per_tok, rem = g - i * per_tok;
+        const int s = rem >> 3, q = rem & 7;
+        float4 w = v[u];
+        sum = (w.x + w.y) + (w.z + w.w);
+        w.x *= pos_scale<BITS>(4 * q + 0);
+        w.y *= pos_scale<BITS>(4 * q + 1);
+        w.z *= pos_scale<BITS>(4 * q + 2);
+        w.w *= pos_scale<BITS>(4 * q + 3);
+        xs4[(i * 8 + q) * ld + s] = w;
+      }
+      // groups of eight lanes hold one slice (total and nthreads are
+      // multiples of 8, so a group is wholly in or out of range)
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+      if (g < total && (g & 7) == 0) {
+        const int i = g / per_tok, s = (g - i * per_tok) >> 3;
+        xsum[i * NSL + s] = sum;
+      }
+    }
+  }
+}
+
+// Bytes of shared memory that stage_inputs needs for G tokens of `cols` inputs.
+static size_t staged_bytes(int cols, int G) {
+  return (size_t)G * 8 * (cols / kSlice + 1) * 16 + (size_t)G * (cols / kSlice) * sizeof(float);
+}
+
+// Where the rows of a warp live: row r (0..3) has its codes at
+// base + (r >> 1) * pair + (r & 1) * step and its (scale, bias) words at
+// base + sb + (r >> 1) * pair + (r & 1) * sb_step.
+struct RowAddr {
+  uint32_t pair, step, sb, sb_step;
+  __device__ __forceinline__ uint32_t q(int r) const { return (uint32_t)(r >> 1) * pair + (uint32_t)(r & 1) * step; }
+  __device__ __forceinline__ uint32_t w(int r) const {
+    return sb + (uint32_t)(r >> 1) * pair + (uint32_t)(r & 1) * sb_step;
+  }
+};
+
+// acc[row][tok] = dot(row's codes, token tok's input) over the lane's slices,
+// for the 4 rows at (base, ra) in shared memory and n <= kMaxTokGroup tokens
+// staged by stage_inputs.  Per slice the codes are masked once and meet
+// every token from registers.
+template <int BITS>
+__device__ __forceinline__ void rows_dot(const uint8_t* base, const RowAddr ra, const float4* xs4,
+                                         const float* xsum, int n, int NSL, float (&acc)[4][kMaxTokGroup]) {
+  const int lane = threadIdx.x & 31;
+  const int ld = NSL + 1;
+  for (int s = lane; s < NSL; s += 32) {
+    SliceCodes<BITS> c[4];
+    uint32_t sb[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      c[r] = smem_codes<BITS>(base + ra.q(r), s);
+      sb[r] = reinterpret_cast<const uint32_t*>(base + ra.w(r))[s >> 1];
+    }
+    float2 pacc[4][kMaxTokGroup];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int t = 0; t < kMaxTokGroup; ++t) pacc[r][t] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 xp[kMaxTokGroup][4];
+#pragma unroll
+      for (int t = 0; t < kMaxTokGroup; ++t) {
+        if (t < n) {
+          const float4 xa = xs4[(t * 8 + 2 * j) * ld + s];
+          const float4 xb = xs4[(t * 8 + 2 * j + 1) * ld + s];
+          xp[t][0] = make_float2(xa.x, xa.y);
+          xp[t][1] = make_float2(xa.z, xa.w);
+          xp[t][2] = make_float2(xb.x, xb.y);
+          xp[t][3] = make_float2(xb.z, xb.w);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float2 qp[4];
+        octet_pairs(c[r], j, qp);
+#pragma unroll
+        for (int t = 0; t < kMaxTokGroup; ++t) {
+          if (t < n) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pacc[r][t] = __ffma2_rn(qp[i], xp[t][i], pacc[r][t]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float s64 = bf16lo(sb[r]) * 18446744073709551616.0f;   // scale * 2^64
+      const float b = bf16hi(sb[r]);
+#pragma unroll
+      for (int t = 0; t < kMaxTokGroup; ++t)
+        if (t < n) acc[r][t] += fmaf(s64, pacc[r][t].x + pacc[r][t].y, b * xsum[t * NSL + s]);
+    }
+  }
+}
+
+__device__ __forceinline__ const uint8_t* item_blob(const BatchArgs& a, int expert) {
+  return expert >= 0 ? a.experts + (size_t)expert * a.blob : a.shared;
+}
+
+// named barrier over the consumer warps only (per-thread count)
+__device__ __forceinline__ void batch_consumer_sync() {
+  asm volatile("barrier.sync 1, %0;" ::"n"(kBatchConsumerWarps * 32) : "memory");
+}
+
+// Shared control area of the expert kernels.
+struct BatchCtrl {
+  uint64_t full[kBatchMaxStages];
+  uint64_t empty[kBatchMaxStages];
+  int item[kItemWords];
+  int abort;
+};
+constexpr int kBatchCtrlBytes = 256;
+static_assert(sizeof(BatchCtrl) <= kBatchCtrlBytes, "control area");
+
+// One work unit of an expert kernel: `rows` consecutive records of an
+// expert, `rec_bytes` apart, starting at record `first` of the part that
+// begins at byte `part` of the blob.
+struct UnitShape {
+  size_t part, rec_bytes;
+  int rows;
+};
+
+// The producer side, run by one lane: stream the records of the block's
+// units [u0, u1) into the ring, in order.  Returns after its last copy has
+// landed (bounded), so that no copy outlives the block.
+__device__ void batch_produce(const BatchArgs& a, BatchCtrl* ctl, uint8_t* ring, int nstage, int stage_bytes,
+                              long long u0, long long u1, int n_rb, const UnitShape us) {
+  const uint32_t bytes = (uint32_t)(us.rows * us.rec_bytes);
+  int cur_item = -1, expert = 0;
+  long long k = 0;
+  for (long long u = u0; u < u1; ++u, ++k) {
+    const int st = (int)(k % nstage);
+    const uint32_t use = (uint32_t)(k / nstage);
+    if (use >= 1 && !mbar_wait(&ctl->empty[st], (use - 1) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
+    const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
+    if (item != cur_item) {
+      expert = __ldcg(a.plan + kPlanHeader + item * kItemWords);
+      cur_item = item;
+    }
+    const uint8_t* src = item_blob(a, expert) + us.part + (size_t)rb * us.rows * us.rec_bytes;
+    mbar_arrive_expect_tx(&ctl->full[st], bytes);
+    bulk_g2s(ring + (size_t)st * stage_bytes, src, bytes, &ctl->full[st]);
+  }
+  // drain: every stage's last copy has landed before the block may exit
+  const long long issued = k;
+  for (int st = 0; st < nstage && st < issued; ++st) {
+    const long long last = st + ((issued - 1 - st) / nstage) * nstage;
+    if (!mbar_wait_drain(&ctl->full[st], (uint32_t)(last / nstage) & 1u, a.timeout_ns)) {
+      atomicOr(a.err, kErrCopyTimeout);
+      ctl->abort = 1;
+    }
+  }
+}
+
+// Work units of a block: a contiguous share of W.
+__device__ __forceinline__ void block_share(long long W, long long& u0, long long& u1) {
+  u0 = W * blockIdx.x / gridDim.x;
+  u1 = W * (blockIdx.x + 1) / gridDim.x;
+}
+
+__device__ __forceinline__ void batch_init(BatchCtrl* ctl, int nstage) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nstage; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], kBatchConsumerWarps);
+    }
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// gate/up + SwiGLU: unit = (item, gu_rows intermediate rows); consumer warp w
+// < gu_warps takes records 2w and 2w+1 of the unit: gate and up of each
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  BatchCtrl* ctl = reinterpret_cast<BatchCtrl*>(smem);
+  const BatchGeom& geo = a.geo;
+  const int NSL = a.H / kSlice;
+  float4* xs4 = reinterpret_cast<float4*>(smem + kBatchCtrlBytes);
+  float* xsum = reinterpret_cast<float*>(xs4 + geo.G * 8 * (NSL + 1));
+  uint8_t* ring = smem + kBatchCtrlBytes + geo.gu_xs_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = a.K + a.S;
+  const int n_rb = a.I / geo.gu_rows;
+  const long long W = (long long)__ldcg(a.plan) * n_rb;
+  long long u0, u1;
+  block_share(W, u0, u1);
+  batch_init(ctl, geo.gu_nstage);
+
+  if (warp == kBatchProducerWarp) {
+    if (lane == 0)
+      batch_produce(a, ctl, ring, geo.gu_nstage, geo.gu_stage_bytes, u0, u1, n_rb,
+                    UnitShape{0, a.lay.gu_row, geo.gu_rows});
+    return;
+  }
+  const RowAddr ra{(uint32_t)a.lay.gu_row, (uint32_t)a.lay.qh, (uint32_t)(2 * a.lay.qh), (uint32_t)a.lay.sh};
+  int cur = -1;
+  long long k = 0;
+  for (long long u = u0; u < u1; ++u, ++k) {
+    const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
+    if (item != cur) {
+      batch_consumer_sync();
+      if (threadIdx.x < kItemWords) ctl->item[threadIdx.x] = __ldcg(a.plan + kPlanHeader + item * kItemWords + threadIdx.x);
+      batch_consumer_sync();
+      stage_inputs<BITS>(xs4, xsum, ctl->item[1], NSL, kBatchConsumerWarps * 32,
+                         [&](int i) { return a.x + (size_t)(ctl->item[2 + i] >> 8) * a.H; });
+      batch_consumer_sync();
+      cur = item;
+    }
+    const int st = (int)(k % geo.gu_nstage);
+    if (!mbar_wait(&ctl->full[st], (uint32_t)(k / geo.gu_nstage) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
+    const int n = ctl->item[1];
+    float acc[4][kMaxTokGroup] = {};
+    if (warp < geo.gu_warps)
+      rows_dot<BITS>(ring + (size_t)st * geo.gu_stage_bytes + (size_t)(2 * warp) * a.lay.gu_row, ra, xs4, xsum, n,
+                     NSL, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[st]);
+    if (warp < geo.gu_warps) {
+      float v[16];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < kMaxTokGroup; ++t) v[r * kMaxTokGroup + t] = acc[r][t];
+      const float tot = reduce16(v);
+      // lane L holds value (row L >> 3, token (L >> 1) & 3); the up row of
+      // the same token is 8 lanes up
+      const float up = __shfl_xor_sync(0xFFFFFFFFu, tot, 8);
+      const int tok = (lane >> 1) & 3;
+      if ((lane & 9) == 0 && tok < n) {
+        const int pr = ctl->item[2 + tok];
+        const int r = rb * geo.gu_rows + 2 * warp + (lane >> 4);
+        a.h[((size_t)(pr >> 8) * NS + (pr & 255)) * a.I + r] = silu_f(tot) * up;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// down: unit = (item, 4 * consumer warps output rows); warp w takes records
+// 4w .. 4w+3 of the unit
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kBatchThreads, 1) batch_down_kernel(BatchArgs a, float* __restrict__ y) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  BatchCtrl* ctl = reinterpret_cast<BatchCtrl*>(smem);
+  const BatchGeom& geo = a.geo;
+  const int NSL = a.I / kSlice;
+  float4* xs4 = reinterpret_cast<float4*>(smem + kBatchCtrlBytes);
+  float* xsum = reinterpret_cast<float*>(xs4 + geo.G * 8 * (NSL + 1));
+  uint8_t* ring = smem + kBatchCtrlBytes + geo.d_xs_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = a.K + a.S;
+  const int rows = kDownRowsPerWarp * kBatchConsumerWarps;
+  const int n_rb = a.H / rows;
+  const long long W = (long long)__ldcg(a.plan) * n_rb;
+  long long u0, u1;
+  block_share(W, u0, u1);
+  batch_init(ctl, geo.d_nstage);
+
+  if (warp == kBatchProducerWarp) {
+    if (lane == 0)
+      batch_produce(a, ctl, ring, geo.d_nstage, geo.d_stage_bytes, u0, u1, n_rb,
+                    UnitShape{a.lay.d_off, a.lay.d_row, rows});
+    return;
+  }
+  const RowAddr ra{(uint32_t)(2 * a.lay.d_row), (uint32_t)a.lay.d_row, (uint32_t)a.lay.qi, (uint32_t)a.lay.d_row};
+  int cur = -1;
+  long long k = 0;
+  for (long long u = u0; u < u1; ++u, ++k) {
+    const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
+    if (item != cur) {
+      batch_consumer_sync();
+      if (threadIdx.x < kItemWords) ctl->item[threadIdx.x] = __ldcg(a.plan + kPlanHeader + item * kItemWords + threadIdx.x);
+      batch_consumer_sync();
+      stage_inputs<BITS>(xs4, xsum, ctl->item[1], NSL, kBatchConsumerWarps * 32, [&](int i) {
+        const int pr = ctl->item[2 + i];
+        return a.h + ((size_t)(pr >> 8) * NS + (pr & 255)) * a.I;
+      });
+      batch_consumer_sync();
+      cur = item;
+    }
+    const int st = (int)(k % geo.d_nstage);
+    if (!mbar_wait(&ctl->full[st], (uint32_t)(k / geo.d_nstage) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
+    const int n = ctl->item[1];
+    float acc[4][kMaxTokGroup] = {};
+    rows_dot<BITS>(ring + (size_t)st * geo.d_stage_bytes + (size_t)(kDownRowsPerWarp * warp) * a.lay.d_row, ra, xs4,
+                   xsum, n, NSL, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[st]);
+    float v[16];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int t = 0; t < kMaxTokGroup; ++t) v[r * kMaxTokGroup + t] = acc[r][t];
+    const float tot = reduce16(v);
+    const int tok = (lane >> 1) & 3;
+    if ((lane & 1) == 0 && tok < n) {
+      const int pr = ctl->item[2 + tok];
+      y[((size_t)(pr >> 8) * NS + (pr & 255)) * a.H + rb * rows + kDownRowsPerWarp * warp + (lane >> 3)] = tot;
+    }
+  }
+}
+
+// out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
+__global__ void batch_combine_kernel(BatchArgs a) {
+  const int H4 = a.H / 4;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= a.T * H4) return;
+  const int t = idx / H4, j4 = idx % H4;
+  const int NS = a.K + a.S;
+  const float4* y4 = reinterpret_cast<const float4*>(a.y);
+  float4 acc = reinterpret_cast<const float4*>(a.residual)[idx];
+  auto add = [&](float w, int slot) {
+    const float4 v = y4[((size_t)t * NS + slot) * H4 + j4];
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  };
+  for (int k = 0; k < a.K; ++k) add(a.weights[t * a.K + k], k);
+  if (a.S) add(a.gate[t], a.K);
+  reinterpret_cast<float4*>(a.out)[idx] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights,
+                         const uint16_t* wsg, const float* x, int H, float* gate, cudaStream_t st) {
+  const int warps = 4;
+  route_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, st>>>(logits, T, E, K, ids, weights, wsg, x,
+                                                                 H, gate);
+  return cudaGetLastError();
+}
+
+int batch_max_items(int T, int K, int S, int G) { return T * K + S * ((T + G - 1) / G); }
+
+static size_t round_up128(size_t v) { return (v + 127) / 128 * 128; }
+
+BatchGeom batch_geometry(int bits, int H, int I, int device) {
+  BatchGeom g{};
+  int sms = 0, smem_max = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return g;
+  if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return g;
+  const BlobLayout lay = blob_layout(bits, H, I);
+  const size_t avail = (size_t)smem_max - kBatchCtrlBytes;
+  const int d_rows = kDownRowsPerWarp * kBatchConsumerWarps;
+  if (H % d_rows) return g;
+  // the most tokens per item, then the most gate/up warps, for which two
+  // ring stages fit next to the staged inputs of both kernels
+  for (int G = kMaxTokGroup; G >= 1; G /= 2) {
+    const size_t gx = round_up128(staged_bytes(H, G)), dx = round_up128(staged_bytes(I, G));
+    const size_t d_stage = round_up128((size_t)d_rows * lay.d_row);
+    if (dx + 2 * d_stage > avail) continue;
+    for (int w = kBatchConsumerWarps; w >= 1; w /= 2) {
+      const size_t gu_stage = round_up128((size_t)2 * w * lay.gu_row);
+      if (I % (2 * w) || gx + 2 * gu_stage > avail) continue;
+      g.G = G;
+      g.gu_warps = w;
+      g.gu_rows = 2 * w;
+      g.gu_stage_bytes = (int)gu_stage;
+      g.gu_nstage = (int)std::min<size_t>(kBatchMaxStages, (avail - gx) / gu_stage);
+      g.gu_xs_bytes = (int)gx;
+      g.gu_smem = kBatchCtrlBytes + gx + (size_t)g.gu_nstage * gu_stage;
+      g.d_stage_bytes = (int)d_stage;
+      g.d_nstage = (int)std::min<size_t>(kBatchMaxStages, (avail - dx) / d_stage);
+      g.d_xs_bytes = (int)dx;
+      g.d_smem = kBatchCtrlBytes + dx + (size_t)g.d_nstage * d_stage;
+      g.grid = sms;
+      return g;
+    }
+  }
+  return g;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` (once per kernel,
+// device and size; `done` remembers the largest size set so far).
+template <typename Kern>
+static cudaError_t allow_smem(Kern k, size_t bytes, size_t& done) {
+  if (bytes <= 48 * 1024 || bytes <= done) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done = bytes;
+  return e;
+}
+// per device: gate/up 4-bit, 2-bit; down 4-bit, 2-bit (function attributes
+// belong to the device's context)
+static size_t g_smem_set[64][4];
+
+cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  a.geo = batch_geometry(a.bits, a.H, a.I, dev);
+  if (a.geo.grid == 0) return cudaErrorInvalidValue;
+  size_t* set = g_smem_set[dev];
+
+  batch_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const BatchGeom& g = a.geo;
+  if (a.bits == 4) {
+    if ((e = allow_smem(batch_gateup_kernel<4>, g.gu_smem, set[0])) != cudaSuccess) return e;
+    batch_gateup_kernel<4><<<g.grid, kBatchThreads, g.gu_smem, st>>>(a);
+  } else {
+    if ((e = allow_smem(batch_gateup_kernel<2>, g.gu_smem, set[1])) != cudaSuccess) return e;
+    batch_gateup_kernel<2><<<g.grid, kBatchThreads, g.gu_smem, st>>>(a);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  if (a.bits == 4) {
+    if ((e = allow_smem(batch_down_kernel<4>, g.d_smem, set[2])) != cudaSuccess) return e;
+    batch_down_kernel<4><<<g.grid, kBatchThreads, g.d_smem, st>>>(a, y);
+  } else {
+    if ((e = allow_smem(batch_down_kernel<2>, g.d_smem, set[3])) != cudaSuccess) return e;
+    batch_down_kernel<2><<<g.grid, kBatchThreads, g.d_smem, st>>>(a, y);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  if (a.out != nullptr) {
+    const int n = a.T * (a.H / 4);
+    batch_combine_kernel<<<(n + 255) / 256, 256, 0, st>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace fmoe

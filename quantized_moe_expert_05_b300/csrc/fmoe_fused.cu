@@ -38,93 +38,12 @@
 // finished the previous layer.  Every wait is bounded (%globaltimer); a wait
 // that runs out records the time-out in the workspace error word, and every
 // later wait of the block returns at once, so the launch always ends.
+#include "fmoe_async.cuh"
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
 
 namespace {
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Whether an mbarrier phase has completed, without waiting.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for an mbarrier phase, suspended (not spinning) for up to hint_ns.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait on an mbarrier phase.  The waiting warp sleeps in the
-// barrier unit rather than spinning, so it takes no issue slots from the
-// warps doing the arithmetic.  Returns false (and sets the abort flag and
-// the error word on a time-out) if the block has given up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
-                                          uint32_t* err, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 50000u)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      atomicOr(err, kErrCopyTimeout);
-      *abort = 1;
-      return false;
-    }
-  }
-}
 
 // (value, tag) words: a float and the tag of the launch and layer that wrote
 // it, stored and loaded as one 64-bit access so that a reader sees either the
@@ -136,12 +55,6 @@ __device__ __forceinline__ void ll_store(unsigned long long* p, float v, uint32_
 
 __device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long ll_load(const unsigned long long* p) {
-  unsigned long long w;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-  return w;
 }
 
 __device__ __forceinline__ float ll_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
@@ -482,6 +395,11 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
       for (int q = xw; q < NS; q += 2) {
         const unsigned long long* hsrc = p.hll + (size_t)hidx(q) * I;
         float* hsf = reinterpret_cast<float*>(s_hs + (size_t)q * pl.hs_slot_bytes);
+#if FMOE_XCHG_WAIT_OWN
+        // the other blocks finish a slot at about the time this one does:
+        // polling earlier only returns stale words one round trip later
+        mbar_wait(&bar_slot[q], lpar, tmo, p.err, s_abort);
+#endif
         // fetch all I words of the slot, then re-fetch until every tag is current
         uint64_t t0 = 0;
         bool started = false;
@@ -799,9 +717,9 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
   const long long avail = (long long)smem_max - pl.ring_off;
   const long long ns = avail / pl.stage_bytes;
   if (ns < 2) return pl;
-  pl.nstage = (int)(ns > kMaxStages ? kMaxStages : ns);
+  pl.nstage = (int)(ns > kFusedStageCap ? kFusedStageCap : ns);
   pl.smem = (size_t)pl.ring_off + (size_t)pl.nstage * pl.stage_bytes;
-  pl.dlag = 2;
+  pl.dlag = kFusedDownLag;
   pl.grid = grid;
   pl.ok = true;
   return pl;

@@ -77,7 +77,8 @@ struct WsLayout {
   size_t h;          // fp32 [T][K+S][I]
   size_t hll;        // u64 [K+S][I]: (value, tag) exchange of h between blocks
   size_t hbufll;     // u64 [2][H]: (value, tag) layer outputs of a stack
-  size_t plan;       // int32 batch plan
+  size_t y;          // fp32 [T][K+S][H] unweighted expert outputs (batched path)
+  size_t plan;       // int32 batch plan: 8-word header + 8 words per item
   size_t plan_words;
   size_t bytes;
 };
@@ -97,8 +98,10 @@ inline WsLayout ws_layout(int H, int I, int S, int T, int K, int L) {
   w.h = pos; pos = round_up(pos + (size_t)T * (K + S) * I * 4, 256);
   w.hll = pos; pos = round_up(pos + (size_t)(K + S) * I * 8, 256);
   w.hbufll = pos; pos = round_up(pos + (size_t)2 * H * 8, 256);
-  // plan: unique count, unique ids[T*K+1], per-unique token count, token lists
-  w.plan_words = 4 + 4 * (size_t)(T * K + 1) + (size_t)(T * K + 1) * (T + 1);
+  w.y = pos; pos = round_up(pos + (size_t)T * (K + S) * H * 4, 256);
+  // plan: header, then at most T*K + S*T items of 8 words (one token per
+  // item at worst)
+  w.plan_words = 8 + 8 * ((size_t)T * K + (size_t)S * T);
   w.plan = pos; pos = round_up(pos + w.plan_words * 4, 256);
   w.bytes = pos;
   return w;

@@ -5,28 +5,62 @@
 
 namespace fmoe {
 
-// Arguments of the general kernels (fmoe_generic.cu).
-struct GenericArgs {
+// Geometry of the batched expert kernels (host computed by batch_geometry).
+struct BatchGeom {
+  int G;                    // tokens per plan item (4, 2 or 1: what the staged inputs leave room for)
+  int gu_warps;             // consumer warps with gate/up rows (2 rows each per unit)
+  int gu_rows;              // intermediate rows per gate/up work unit (2 * gu_warps)
+  int gu_nstage, gu_stage_bytes;
+  int d_nstage, d_stage_bytes;    // down: 4 rows per consumer warp per unit
+  int gu_xs_bytes, d_xs_bytes;    // staged inputs
+  size_t gu_smem, d_smem;
+  int grid;
+};
+
+// Arguments of the routing and batched kernels (fmoe_batch.cu).
+struct BatchArgs {
   int bits, H, I, E, K, S, T;
   size_t blob;
   BlobLayout lay;
   const uint8_t* experts;
   const uint8_t* shared;
-  const int32_t* ids;       // [T][K]
-  const float* weights;     // [T][K]
-  const float* gate;        // [T]
+  const float* logits;      // [T][E]: route in the plan kernel; nullptr: ids_in given
+  const int32_t* ids_in;    // [T][K] caller's ids (fmoe_expert_ffn) or nullptr
+  const uint16_t* wsg;      // shared gate vector [H] (S == 1, routing) or nullptr
+  int32_t* ids;             // [T][K] routing result
+  float* weights;           // [T][K]
+  float* gate;              // [T]
   const float* x;           // [T][H]
   const float* residual;    // [T][H]
-  float* out;               // [T][H]
+  float* out;               // [T][H], or nullptr: stop after y
   float* h;                 // [T][K+S][I]
+  float* y;                 // [T][K+S][H] unweighted expert outputs
+  int32_t* plan;            // batch plan (fmoe_batch.cu)
   uint32_t* err;
+  unsigned long long timeout_ns;
+  BatchGeom geo;
 };
+
+constexpr int kMaxTokGroup = 4;        // most tokens that share one pass over an expert's codes
+constexpr int kPlanHeader = 8;         // int32: [0] items, [1] distinct experts (incl. shared)
+constexpr int kItemWords = 8;          // int32 per plan item
+constexpr int kBatchConsumerWarps = 8;
+constexpr int kBatchProducerWarp = kBatchConsumerWarps;
+constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 1);
+constexpr int kBatchMaxStages = 8;
+constexpr int kDownRowsPerWarp = 4;
+
+// Largest number of plan items for T tokens, top-K, S shared experts, G
+// tokens per item.
+int batch_max_items(int T, int K, int S, int G);
+// Geometry for a shape; grid == 0 if it does not fit (never for the shapes
+// the ABI accepts).
+BatchGeom batch_geometry(int bits, int H, int I, int device);
 
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights,
                          const uint16_t* wsg, const float* x, int H, float* gate, cudaStream_t st);
-cudaError_t launch_gateup_generic(const GenericArgs& a, cudaStream_t st);
-cudaError_t launch_down_y(const GenericArgs& a, float* y, cudaStream_t st);
-cudaError_t launch_down_combine(const GenericArgs& a, cudaStream_t st);
+// plan -> gate/up -> down into y (-> combine into a.out when non-null)
+cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // single-launch persistent kernel (fmoe_fused.cu)
@@ -46,6 +80,21 @@ constexpr int kFusedMaxRegs = (16384 / (kFusedWarpsPerScheduler * 32)) / 8 * 8;
 constexpr int kMaxFusedLayers = 64;    // layers per launch; longer stacks use several launches
 constexpr int kMaxSlots = FMOE_MAX_TOPK + 1;
 constexpr int kMaxStages = 16;
+// Tuning of the persistent kernel (compile-time; the defaults are the
+// measured best): ring stages at most, slots by which a slot's down records
+// trail its gate/up records, and whether an exchange warp waits for its own
+// block's share of a slot before polling the other blocks' shares.
+#ifndef FMOE_FUSED_STAGE_CAP
+#define FMOE_FUSED_STAGE_CAP 16
+#endif
+#ifndef FMOE_FUSED_DOWN_LAG
+#define FMOE_FUSED_DOWN_LAG 2
+#endif
+#ifndef FMOE_XCHG_WAIT_OWN
+#define FMOE_XCHG_WAIT_OWN 0
+#endif
+constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
+constexpr int kFusedDownLag = FMOE_FUSED_DOWN_LAG;
 constexpr int kMaxDownGroups = 8;      // down row groups per down warp
 constexpr int kCtrlBytes = 1536;       // barriers, routing result, reductions
 

@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "fmoe_stack_decode": (I, [LP, I, P, P, I, F, P, P]),
         "fmoe_ws_routing": (I, [P, LP, I, I, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P),
                                 ctypes.POINTER(P)]),
+        "fmoe_ws_batch_plan": (I, [P, LP, I, I, ctypes.POINTER(P)]),
         "fmoe_status_string": (ctypes.c_char_p, [I]),
         "fmoe_last_device_error": (I, [P, P]),
         "fmoe_debug_wait_test": (I, [P, I, I, I, P]),
@@ -206,6 +207,21 @@ def ws_routing(ws: torch.Tensor, layer: Layer, T: int, K: int) -> dict:
         "gate": view(g, torch.float32, T),
         "h": view(h, torch.float32, T * (K + S) * layer.inter).view(T, K + S, layer.inter),
     }
+
+
+def ws_batch_plan(ws: torch.Tensor, layer: Layer, T: int, K: int) -> dict:
+    """The batch plan left in a workspace by expert_ffn or a batched moe_block
+    (copied to the host; synchronises): item count, distinct experts read, and
+    per item (expert id or -1 for the shared expert, [(t, slot), ...])."""
+    p = ctypes.c_void_p()
+    _check(lib.fmoe_ws_batch_plan(_ptr(ws), ctypes.byref(layer.c()), T, K, ctypes.byref(p)),
+           "fmoe_ws_batch_plan")
+    off = p.value - ws.data_ptr()
+    head = ws[off: off + 32].view(torch.int32).cpu().tolist()
+    n = head[0]
+    body = ws[off + 32: off + 32 + 32 * n].view(torch.int32).view(n, 8).cpu().tolist()
+    items = [(r[0], [(v >> 8, v & 255) for v in r[2: 2 + r[1]]]) for r in body]
+    return {"n_items": n, "n_unique": head[1], "items": items}
 
 
 def last_device_error(ws: torch.Tensor, stream=None) -> int:

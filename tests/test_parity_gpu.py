@@ -6,6 +6,7 @@ block at batch 1..16 with Zipf(1.1) routing, and the 48-layer stack (H 2048,
 512 experts, top-10, I 512).  Expert ids must match exactly; outputs within
 max relative error 2e-3 (both the max-normalised and the elementwise form).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -235,6 +236,84 @@ def test_qwen_batch_zipf(fm, qwen_pools, T):
     layer = make_layer(fm, shape, pool=_zipf_pool(shape))
     ws = fm.new_workspace(layer, 16, 4)
     check_block(fm, layer, shape, synth.block_inputs(shape, T, tag=T), 4, ws)
+
+
+def check_plan(fm, layer, ws, T, K, ids, S):
+    """The batch plan lists each distinct expert once (ceil(m/4) items for m
+    tokens), covers every (token, slot) exactly once, tokens ascending."""
+    plan = fm.ws_batch_plan(ws, layer, T, K)
+    ids = np.asarray(ids)
+    distinct = sorted(set(int(v) for v in ids.ravel()))
+    assert plan["n_unique"] == len(distinct) + S
+    seen, order = {}, []
+    for expert, pairs in plan["items"]:
+        assert 1 <= len(pairs) <= 4
+        for t, k in pairs:
+            assert (t, k) not in seen
+            seen[(t, k)] = expert
+            assert expert == (int(ids[t, k]) if k < K else -1)
+        if not order or order[-1][0] != expert:
+            order.append((expert, []))
+        order[-1][1].extend(t for t, _ in pairs)
+    want = {(t, k) for t in range(T) for k in range(K)} | ({(t, K) for t in range(T)} if S else set())
+    assert set(seen) == want
+    experts_in_order = [e for e, _ in order]
+    assert len(experts_in_order) == len(set(experts_in_order)), "an expert's items are not contiguous"
+    for _, toks in order:
+        assert toks == sorted(toks)
+    m = {e: sum(1 for v in seen.values() if v == e) for e in set(seen.values())}
+    assert plan["n_items"] == sum((c + 3) // 4 for c in m.values())
+    return plan
+
+
+@pytest.mark.parametrize("T", [2, 16])
+def test_batch_plan_reads_each_expert_once(fm, qwen_pools, T):
+    shape = synth.QWEN_Q4_BATCH
+    layer = make_layer(fm, shape, pool=_zipf_pool(shape))
+    ws = fm.new_workspace(layer, 16, 4)
+    inp = synth.block_inputs(shape, T, tag=T)
+    run_block(fm, layer, shape, inp, 4, ws)
+    ids = fm.ws_routing(ws, layer, T, 4)["ids"].cpu().numpy()
+    plan = check_plan(fm, layer, ws, T, 4, ids, 1)
+    print(f"T={T}: {plan['n_unique']} distinct experts (incl. shared) for {T * 4 + T} picks")
+
+
+def test_batch_all_tokens_share_experts(fm, qwen_pools):
+    # every token routes to the same 4 experts: 5 distinct experts, 4 items each
+    shape = synth.QWEN_Q4_BATCH
+    layer = make_layer(fm, shape, pool=_zipf_pool(shape))
+    ws = fm.new_workspace(layer, 16, 4)
+    inp = synth.block_inputs(shape, 16, tag=60)
+    inp.logits[:] = inp.logits[0:1]
+    check_block(fm, layer, shape, inp, 4, ws)
+    plan = check_plan(fm, layer, ws, 16, 4, fm.ws_routing(ws, layer, 16, 4)["ids"].cpu().numpy(), 1)
+    assert plan["n_unique"] == 5 and plan["n_items"] == 20
+
+
+def test_batch_q2_zipf(fm, qwen_pools):
+    shape = dataclasses.replace(synth.QWEN_Q2, zipf_s=1.1)
+    layer = make_layer(fm, shape, pool=qwen_pools[synth.QWEN_Q2.name])
+    ws = fm.new_workspace(layer, 8, 4)
+    check_block(fm, layer, shape, synth.block_inputs(shape, 8, tag=3), 4, ws)
+
+
+def test_expert_ffn_duplicate_ids(fm):
+    # the same expert twice in one token and across tokens; the tiny block
+    shape = synth.TINY
+    layer = make_layer(fm, shape)
+    T, K = 6, 3
+    ws = fm.new_workspace(layer, T, K)
+    ids = torch.tensor([[3, 3, 1], [1, 3, 0], [7, 7, 7], [0, 1, 3], [3, 5, 1], [1, 3, 3]], dtype=torch.int32)
+    x = synth.normal(shape.seed, 78, (T, shape.hidden))
+    y = fm.expert_ffn(layer, ids.cuda(), x.cuda(), ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    y = y.cpu().numpy()
+    for t in range(T):
+        for k in range(K):
+            ref = oracle.expert_ffn(oracle_expert(shape, 0, int(ids[t, k])), x[t].numpy())
+            assert_close(y[t, k], ref, what=f"y[{t},{k}]")
+    check_plan(fm, layer, ws, T, K, ids.numpy(), 0)
 
 
 _ZP = {}
