@@ -6,8 +6,9 @@ Default workload (the one the headline metric is quoted on): the Qwen-shaped
 bf16 scale/bias), run as a decode chain: one step = one token through 64 such
 blocks, each with its own shared expert and fresh router logits, RMSNorm +
 residual between blocks, all in ONE launch of the persistent kernel
-(fmoe_stack_decode).  No block's weights are requested before the previous
-block's output exists.
+(fmoe_stack_decode).  No block's routed experts are requested before the
+previous block's output exists (the shared expert, whose identity is fixed,
+may be requested once the reading SM has finished the previous block).
 
 value     active-expert bytes (5 experts x 7,077,888 B per block) per second,
           inputs resident in HBM, CUDA events on the launching stream

@@ -175,7 +175,10 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer /* host */, const float* x,
  *           hidden, inter, n_experts and has_shared
  *   logits  fp32 [L][E];  h fp32 [H] in/out
  *   ws      workspace of fmoe_workspace_bytes(&layers[0], 1, K, L) bytes
- * No layer's weights are read before the previous layer's output is complete.
+ * No layer's routed experts are read before the previous layer's output is
+ * complete (their ids depend on it); a layer's shared expert, whose identity
+ * is fixed, may be requested as soon as the reading block has finished its
+ * share of the previous layer.
  */
 fmoe_status fmoe_stack_decode(const fmoe_layer* layers /* host */, int L,
                               const float* logits, float* h, int K, float eps,

@@ -6,7 +6,7 @@
 // memory-pool callback, in a plugin whose host framework owns every device
 // allocation, or in a hard-real-time loop where an allocation may block).
 // For them this file keeps the scratch the single-launch kernel needs
-// (error word, device-wide counters, routing result, intermediate
+// (error word, exit counter, launch epoch, routing result, intermediate
 // activations) in one file-scope __device__ array.  That array is part of the
 // library image: every GPU that loads libfmoe.so holds its
 // FMOE_NOALLOC_SCRATCH_BYTES bytes until the process exits.
