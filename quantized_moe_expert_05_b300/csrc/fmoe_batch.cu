@@ -69,9 +69,15 @@ static_assert(kMaxPairs <= kPlanThreads, "one thread per (token, slot) pair");
 static_assert(FMOE_MAX_TOKENS <= kPlanWarps, "one warp per token");
 static_assert(kPlanHeader == 8 && kItemWords == 8, "ws_layout sizes the plan for these");
 
+// Relative cost of one work unit of an item with n tokens: its bytes (a
+// constant per unit) plus its arithmetic (one pass per token).
+__device__ __forceinline__ int unit_cost(int n) { return 2 + n; }
+
 // Item i of the plan (kItemWords int32 at plan + kPlanHeader + i * kItemWords):
 //   [0] expert id (-1: the shared expert)   [1] n tokens (1..G)
 //   [2 + g] (t << 8) | slot of the g-th token: h[t][slot] / y[t][slot]
+//   [6] sum of unit_cost over the items before i
+// Header: [0] items, [1] distinct experts (shared included), [2] cost total.
 __global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
   __shared__ int s_id[kMaxPairs];
   __shared__ int s_rank[kMaxPairs];   // earlier pairs with the same expert
@@ -80,6 +86,7 @@ __global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
   __shared__ int s_base[kMaxPairs];   // first item of the expert (valid at first pairs)
   __shared__ float s_gpart[kPlanWarps][FMOE_MAX_TOKENS];
   __shared__ int s_nitems, s_nuniq;
+  __shared__ int s_itemn[kMaxPairs + FMOE_MAX_TOKENS];   // tokens of each item
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, K = a.K, NS = a.K + a.S, TK = a.T * a.K, G = a.geo.G;
 
@@ -95,32 +102,43 @@ __global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
     }
     if (a.S) {
       // w_sg . x_t for every token: warp w takes a sixteenth of the columns
-      // of all tokens, so that every load of the block is in flight at once
+      // of all tokens, eight tokens at a time with all their loads in flight
+      constexpr int kTokChunk = 8;
       const int H4 = a.H / 4, per = (H4 + kPlanWarps - 1) / kPlanWarps;
       const int c0 = warp * per, c1 = min(H4, c0 + per);
       const uint2* w4 = reinterpret_cast<const uint2*>(a.wsg);
       const float4* x4 = reinterpret_cast<const float4*>(a.x);
-      float acc[FMOE_MAX_TOKENS];
+      for (int t0 = 0; t0 < T; t0 += kTokChunk) {
+        float acc[kTokChunk];
 #pragma unroll
-      for (int t = 0; t < FMOE_MAX_TOKENS; ++t) acc[t] = 0.f;
-      for (int c = c0 + lane; c < c1; c += 32) {
-        const uint2 wv = __ldg(w4 + c);
+        for (int t = 0; t < kTokChunk; ++t) acc[t] = 0.f;
+        for (int c = c0 + lane; c < c1; c += 64) {
+          const bool two = c + 32 < c1;
+          const uint2 wa = __ldg(w4 + c);
+          const uint2 wb = two ? __ldg(w4 + c + 32) : make_uint2(0u, 0u);
+          float4 xa[kTokChunk], xb[kTokChunk];
 #pragma unroll
-        for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
-          if (t < T) {
-            const float4 xv = __ldcg(x4 + (size_t)t * H4 + c);
-            acc[t] = fmaf(bf16lo(wv.x), xv.x, acc[t]);
-            acc[t] = fmaf(bf16hi(wv.x), xv.y, acc[t]);
-            acc[t] = fmaf(bf16lo(wv.y), xv.z, acc[t]);
-            acc[t] = fmaf(bf16hi(wv.y), xv.w, acc[t]);
+          for (int t = 0; t < kTokChunk; ++t) {
+            const bool in = t0 + t < T;
+            xa[t] = in ? __ldcg(x4 + (size_t)(t0 + t) * H4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[t] = (in && two) ? __ldcg(x4 + (size_t)(t0 + t) * H4 + c + 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int t = 0; t < kTokChunk; ++t) {
+            acc[t] = fmaf(bf16lo(wa.x), xa[t].x, acc[t]);
+            acc[t] = fmaf(bf16hi(wa.x), xa[t].y, acc[t]);
+            acc[t] = fmaf(bf16lo(wa.y), xa[t].z, acc[t]);
+            acc[t] = fmaf(bf16hi(wa.y), xa[t].w, acc[t]);
+            acc[t] = fmaf(bf16lo(wb.x), xb[t].x, acc[t]);
+            acc[t] = fmaf(bf16hi(wb.x), xb[t].y, acc[t]);
+            acc[t] = fmaf(bf16lo(wb.y), xb[t].z, acc[t]);
+            acc[t] = fmaf(bf16hi(wb.y), xb[t].w, acc[t]);
           }
         }
-      }
 #pragma unroll
-      for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
-        if (t < T) {
+        for (int t = 0; t < kTokChunk; ++t) {
           const float v = warp_sum(acc[t]);
-          if (lane == 0) s_gpart[warp][t] = v;
+          if (lane == 0 && t0 + t < T) s_gpart[warp][t0 + t] = v;
         }
       }
     }
@@ -202,6 +220,7 @@ __global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
     if (g == 0) {
       items[it * kItemWords + 0] = s_id[tid];
       items[it * kItemWords + 1] = min(G, s_cnt[tid] - r);
+      s_itemn[it] = min(G, s_cnt[tid] - r);
     }
   }
   const int n_shared_items = a.S ? (T + G - 1) / G : 0;
@@ -212,11 +231,32 @@ __global__ void __launch_bounds__(kPlanThreads) batch_plan_kernel(BatchArgs a) {
     if (g == 0) {
       items[it * kItemWords + 0] = -1;
       items[it * kItemWords + 1] = min(G, T - tid);
+      s_itemn[it] = min(G, T - tid);
     }
   }
-  if (tid == 0) {
-    a.plan[0] = s_nitems + n_shared_items;
-    a.plan[1] = s_nuniq + a.S;
+  __syncthreads();
+  // cost prefix of the items (item word 6) and the total (header word 2):
+  // the expert kernels split their work units by cost, not by count
+  const int n_items = s_nitems + n_shared_items;
+  if (warp == 0) {
+    int base = 0;
+    for (int c0 = 0; c0 < n_items; c0 += 32) {
+      const int i = c0 + lane;
+      const int cst = i < n_items ? unit_cost(s_itemn[i]) : 0;
+      int incl = cst;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (i < n_items) items[i * kItemWords + 6] = base + incl - cst;
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) {
+      a.plan[0] = n_items;
+      a.plan[1] = s_nuniq + a.S;
+      a.plan[2] = base;
+    }
   }
 }
 
@@ -338,12 +378,12 @@ struct RowAddr {
 };
 
 // acc[row][tok] = dot(row's codes, token tok's input) over the lane's slices,
-// for the 4 rows at (base, ra) in shared memory and n <= kMaxTokGroup tokens
-// staged by stage_inputs.  Per slice the codes are masked once and meet
-// every token from registers.
-template <int BITS>
+// for the 4 rows at (base, ra) in shared memory and the NT tokens staged by
+// stage_inputs.  Per slice the codes are masked once and meet every token
+// from registers.
+template <int BITS, int NT>
 __device__ __forceinline__ void rows_dot(const uint8_t* base, const RowAddr ra, const float4* xs4,
-                                         const float* xsum, int n, int NSL, float (&acc)[4][kMaxTokGroup]) {
+                                         const float* xsum, int NSL, float (&acc)[4][kMaxTokGroup]) {
   const int lane = threadIdx.x & 31;
   const int ld = NSL + 1;
   for (int s = lane; s < NSL; s += 32) {
@@ -354,36 +394,31 @@ __device__ __forceinline__ void rows_dot(const uint8_t* base, const RowAddr ra, 
       c[r] = smem_codes<BITS>(base + ra.q(r), s);
       sb[r] = reinterpret_cast<const uint32_t*>(base + ra.w(r))[s >> 1];
     }
-    float2 pacc[4][kMaxTokGroup];
+    float2 pacc[4][NT];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int t = 0; t < kMaxTokGroup; ++t) pacc[r][t] = make_float2(0.f, 0.f);
+      for (int t = 0; t < NT; ++t) pacc[r][t] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 xp[kMaxTokGroup][4];
+      float2 xp[NT][4];
 #pragma unroll
-      for (int t = 0; t < kMaxTokGroup; ++t) {
-        if (t < n) {
-          const float4 xa = xs4[(t * 8 + 2 * j) * ld + s];
-          const float4 xb = xs4[(t * 8 + 2 * j + 1) * ld + s];
-          xp[t][0] = make_float2(xa.x, xa.y);
-          xp[t][1] = make_float2(xa.z, xa.w);
-          xp[t][2] = make_float2(xb.x, xb.y);
-          xp[t][3] = make_float2(xb.z, xb.w);
-        }
+      for (int t = 0; t < NT; ++t) {
+        const float4 xa = xs4[(t * 8 + 2 * j) * ld + s];
+        const float4 xb = xs4[(t * 8 + 2 * j + 1) * ld + s];
+        xp[t][0] = make_float2(xa.x, xa.y);
+        xp[t][1] = make_float2(xa.z, xa.w);
+        xp[t][2] = make_float2(xb.x, xb.y);
+        xp[t][3] = make_float2(xb.z, xb.w);
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         float2 qp[4];
         octet_pairs(c[r], j, qp);
 #pragma unroll
-        for (int t = 0; t < kMaxTokGroup; ++t) {
-          if (t < n) {
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pacc[r][t] = __ffma2_rn(qp[i], xp[t][i], pacc[r][t]);
-          }
-        }
+          for (int i = 0; i < 4; ++i) pacc[r][t] = __ffma2_rn(qp[i], xp[t][i], pacc[r][t]);
       }
     }
 #pragma unroll
@@ -391,10 +426,20 @@ __device__ __forceinline__ void rows_dot(const uint8_t* base, const RowAddr ra, 
       const float s64 = bf16lo(sb[r]) * 18446744073709551616.0f;   // scale * 2^64
       const float b = bf16hi(sb[r]);
 #pragma unroll
-      for (int t = 0; t < kMaxTokGroup; ++t)
-        if (t < n) acc[r][t] += fmaf(s64, pacc[r][t].x + pacc[r][t].y, b * xsum[t * NSL + s]);
+      for (int t = 0; t < NT; ++t) acc[r][t] += fmaf(s64, pacc[r][t].x + pacc[r][t].y, b * xsum[t * NSL + s]);
     }
   }
+}
+
+// rows_dot for the item's n tokens (1..4): the token count is a template
+// argument so that no register or instruction is spent on absent tokens.
+template <int BITS>
+__device__ __forceinline__ void rows_dot_n(int n, const uint8_t* base, const RowAddr ra, const float4* xs4,
+                                           const float* xsum, int NSL, float (&acc)[4][kMaxTokGroup]) {
+  if (n == 1) rows_dot<BITS, 1>(base, ra, xs4, xsum, NSL, acc);
+  else if (n == 2) rows_dot<BITS, 2>(base, ra, xs4, xsum, NSL, acc);
+  else if (n == 3) rows_dot<BITS, 3>(base, ra, xs4, xsum, NSL, acc);
+  else rows_dot<BITS, 4>(base, ra, xs4, xsum, NSL, acc);
 }
 
 __device__ __forceinline__ const uint8_t* item_blob(const BatchArgs& a, int expert) {
@@ -410,6 +455,7 @@ __device__ __forceinline__ void batch_consumer_sync() {
 struct BatchCtrl {
   uint64_t full[kBatchMaxStages];
   uint64_t empty[kBatchMaxStages];
+  long long range[2];
   int item[kItemWords];
   int abort;
 };
@@ -423,6 +469,8 @@ struct UnitShape {
   size_t part, rec_bytes;
   int rows;
 };
+
+constexpr int kCopiesPerUnit = 4;
 
 // The producer side, run by one lane: stream the records of the block's
 // units [u0, u1) into the ring, in order.  Returns after its last copy has
@@ -443,7 +491,13 @@ __device__ void batch_produce(const BatchArgs& a, BatchCtrl* ctl, uint8_t* ring,
     }
     const uint8_t* src = item_blob(a, expert) + us.part + (size_t)rb * us.rows * us.rec_bytes;
     mbar_arrive_expect_tx(&ctl->full[st], bytes);
-    bulk_g2s(ring + (size_t)st * stage_bytes, src, bytes, &ctl->full[st]);
+    // a few copies per unit: the copy engine streams several at once
+    const int per = (us.rows + kCopiesPerUnit - 1) / kCopiesPerUnit;
+    for (int r0 = 0; r0 < us.rows; r0 += per) {
+      const uint32_t b = (uint32_t)((us.rows - r0 < per ? us.rows - r0 : per) * us.rec_bytes);
+      bulk_g2s(ring + (size_t)st * stage_bytes + (size_t)r0 * us.rec_bytes, src + (size_t)r0 * us.rec_bytes, b,
+               &ctl->full[st]);
+    }
   }
   // drain: every stage's last copy has landed before the block may exit
   const long long issued = k;
@@ -456,10 +510,28 @@ __device__ void batch_produce(const BatchArgs& a, BatchCtrl* ctl, uint8_t* ring,
   }
 }
 
-// Work units of a block: a contiguous share of W.
-__device__ __forceinline__ void block_share(long long W, long long& u0, long long& u1) {
-  u0 = W * blockIdx.x / gridDim.x;
-  u1 = W * (blockIdx.x + 1) / gridDim.x;
+// Work units of this block: a contiguous share of the units (item-major,
+// n_rb per item) holding an equal share of their total cost.  Called by every
+// thread of the block (one thread per item looks for the two boundaries).
+__device__ __forceinline__ void block_share(const BatchArgs& a, int n_rb, long long* range, long long& u0,
+                                            long long& u1) {
+  const int n_items = __ldcg(a.plan);
+  const long long W = (long long)n_items * n_rb;
+  const long long C = (long long)__ldcg(a.plan + 2) * n_rb;
+  const long long x[2] = {C * blockIdx.x / gridDim.x, C * (blockIdx.x + 1) / gridDim.x};
+  if (threadIdx.x == 0) range[0] = range[1] = W;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_items; i += blockDim.x) {
+    const int32_t* it = a.plan + kPlanHeader + i * kItemWords;
+    const long long c = unit_cost(__ldcg(it + 1));
+    const long long q0 = (long long)__ldcg(it + 6) * n_rb, q1 = q0 + c * n_rb;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (q0 <= x[k] && x[k] < q1) range[k] = (long long)i * n_rb + (x[k] - q0 + c - 1) / c;
+  }
+  __syncthreads();
+  u0 = range[0];
+  u1 = range[1];
 }
 
 __device__ __forceinline__ void batch_init(BatchCtrl* ctl, int nstage) {
@@ -490,9 +562,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.K + a.S;
   const int n_rb = a.I / geo.gu_rows;
-  const long long W = (long long)__ldcg(a.plan) * n_rb;
   long long u0, u1;
-  block_share(W, u0, u1);
+  block_share(a, n_rb, ctl->range, u0, u1);
   batch_init(ctl, geo.gu_nstage);
 
   if (warp == kBatchProducerWarp) {
@@ -520,8 +591,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
     const int n = ctl->item[1];
     float acc[4][kMaxTokGroup] = {};
     if (warp < geo.gu_warps)
-      rows_dot<BITS>(ring + (size_t)st * geo.gu_stage_bytes + (size_t)(2 * warp) * a.lay.gu_row, ra, xs4, xsum, n,
-                     NSL, acc);
+      rows_dot_n<BITS>(n, ring + (size_t)st * geo.gu_stage_bytes + (size_t)(2 * warp) * a.lay.gu_row, ra, xs4,
+                       xsum, NSL, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->empty[st]);
     if (warp < geo.gu_warps) {
@@ -561,9 +632,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_down_kernel(BatchArgs 
   const int NS = a.K + a.S;
   const int rows = kDownRowsPerWarp * kBatchConsumerWarps;
   const int n_rb = a.H / rows;
-  const long long W = (long long)__ldcg(a.plan) * n_rb;
   long long u0, u1;
-  block_share(W, u0, u1);
+  block_share(a, n_rb, ctl->range, u0, u1);
   batch_init(ctl, geo.d_nstage);
 
   if (warp == kBatchProducerWarp) {
@@ -592,8 +662,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_down_kernel(BatchArgs 
     if (!mbar_wait(&ctl->full[st], (uint32_t)(k / geo.d_nstage) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
     const int n = ctl->item[1];
     float acc[4][kMaxTokGroup] = {};
-    rows_dot<BITS>(ring + (size_t)st * geo.d_stage_bytes + (size_t)(kDownRowsPerWarp * warp) * a.lay.d_row, ra, xs4,
-                   xsum, n, NSL, acc);
+    rows_dot_n<BITS>(n, ring + (size_t)st * geo.d_stage_bytes + (size_t)(kDownRowsPerWarp * warp) * a.lay.d_row,
+                     ra, xs4, xsum, NSL, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->empty[st]);
     float v[16];

@@ -5,37 +5,36 @@
 // per layer as GPU command buffers submitted without waiting; the slotstream
 // write-up (simpler24.com, "the disk was not the slow part") measured batch-1
 // quantised matmuls at 20 % of memory bandwidth because of dispatch cost.
-// Here one cooperative launch (one block per SM) runs every layer, with three
-// warp roles per block:
+// Here one cooperative launch (one block per SM) runs every layer.  Block c
+// owns intermediate rows [I*c/n, I*(c+1)/n) and output rows [H*c/n, H*(c+1)/n)
+// of every selected expert ("slot"); its warps have fixed roles:
 //
-//   producer warp  issues bulk asynchronous copies (TMA engine, mbarrier
-//                  completion) of the block's packed rows: for every selected
-//                  expert ("slot") the gate/up rows [I*c/n, I*(c+1)/n) into a
-//                  shared-memory ring, and the down rows [H*c/n, H*(c+1)/n)
-//                  into a per-slot area.  The shared expert needs no routing,
-//                  so its rows are requested first; a routed slot's rows are
-//                  requested as soon as its id is known.
-//   final warp     turns the consumers' partial sums into h = silu(gate) * up
-//                  for the block's rows and publishes them to L2
-//   exchange warp  gathers each slot's full h from L2 into shared memory,
-//                  pre-scaled for the down projection
-//   16 consumer    route (each warp takes the top-K of its share of the
-//   warps          logits, one warp merges and publishes the ids one by one),
-//                  hold a pre-scaled slice of the input in registers, compute
-//                  dequantised gate/up dot products stage by stage (no block
-//                  barrier per stage: each warp releases a stage through an
-//                  mbarrier), and fold w_slot * (down_row . h_slot) into
-//                  per-row accumulators a slot or two behind the gate/up
-//                  stream; finally out[j] = residual[j] + sum over slots.
+//   producer       one lane issues every bulk asynchronous copy (TMA engine,
+//                  mbarrier completion) of the block's packed rows in the
+//                  order they are consumed: gate/up records through a ring
+//                  of stages, each slot's down records into its own area.
+//                  The shared expert needs no routing, so its rows go first.
+//   12 gate/up     dequantised gate/up dot products of the ring's stages
+//   warps          against the layer input (pre-scaled, in shared memory);
+//                  partial sums per row; a stage is released through an
+//                  mbarrier, never a block barrier.
+//   finaliser      h = silu(gate) * up for the block's rows, published to L2
+//   2 exchange     gather each slot's full h from L2 into shared memory,
+//   warps          pre-scaled for the down projection (even / odd slots); the
+//                  second also routes: it computes the next layer's top-K at
+//                  the end of the current layer and publishes the ids once
+//                  that layer's input is complete.
+//   4 down warps   fold w_slot * (down_row . h_slot) into per-row sums as each
+//                  slot's h arrives; finally out[j] = residual[j] + sum.
 //
 // Blocks exchange data without counters or barriers: every value published
 // to another block (h rows, and the layer outputs of a stack) is stored as
 // one 64-bit (value, tag) word whose tag names the launch and layer, so a
 // reader knows a value is current from the load that fetches it (the
 // low-latency protocol idea of NCCL's LL transport).  A layer's routed
-// experts are requested only after routing on its complete input; the shared
-// expert, which needs no routing, may be requested as soon as this block has
-// finished the previous layer.  Every wait is bounded (%globaltimer); a wait
+// experts are requested only once its input is complete (their ids are
+// published then); the shared expert, which needs no routing, may be
+// requested as soon as this block has finished the previous layer.  Every wait is bounded (%globaltimer); a wait
 // that runs out records the time-out in the workspace error word, and every
 // later wait of the block returns at once, so the launch always ends.
 #include "fmoe_async.cuh"
@@ -107,23 +106,6 @@ __device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: 
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("barrier.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
-
-// Top-K key: larger key = larger logit, and among equal logits the lower
-// expert id (-0 and +0 compare equal).  Valid keys are never 0.
-__device__ __forceinline__ uint64_t route_key(float v, int id) {
-  uint32_t b = __float_as_uint(v);
-  if (b == 0x80000000u) b = 0u;
-  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)id);
-}
-
-__device__ __forceinline__ float key_value(uint64_t k) {
-  const uint32_t ord = (uint32_t)(k >> 32);
-  const uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
-  return __uint_as_float(b);
-}
-
-
 
 // Reduce four values over `width` consecutive lanes (a power of two, 4..32)
 // with a transposed butterfly: on return the group's lane 0 holds sum(a),
@@ -234,6 +216,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   // the value of a freshly zeroed workspace)
   const uint32_t tag0 = *reinterpret_cast<volatile uint32_t*>(p.epoch) * (uint32_t)kMaxFusedLayers + 1u;
 
+  int nx_id = -1;       // routing exchange warp: top-K pick of its lane for the coming layer
+  float nx_l = 0.f;
   for (int l = 0; l < p.L; ++l) {
     const FusedLayerPtrs lp = p.layer[l];
     const uint32_t lpar = (uint32_t)(l & 1);
@@ -272,8 +256,12 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           ensure_routed(ps);
           const uint32_t bytes = (uint32_t)(nd * lay.d_row);
           mbar_arrive_expect_tx(&bar_dfull[ps], bytes);
-          bulk_g2s(darea + (size_t)ps * pl.dslot_bytes, slot_blob(ps) + lay.d_off + (size_t)ja * lay.d_row, bytes,
-                   &bar_dfull[ps]);
+          // a few copies: the copy engine streams several at once
+          const int per = (nd + kFusedDownCopies - 1) / kFusedDownCopies;
+          for (int r0 = 0; r0 < nd; r0 += per)
+            bulk_g2s(darea + (size_t)ps * pl.dslot_bytes + (size_t)r0 * lay.d_row,
+                     slot_blob(ps) + lay.d_off + (size_t)(ja + r0) * lay.d_row,
+                     (uint32_t)(min(per, nd - r0) * lay.d_row), &bar_dfull[ps]);
         };
         int dnext = 0;
         for (int k = 0; k < nstg; ++k) {
@@ -289,9 +277,9 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             // segment goes out at once, routed segments once ids are known
             mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((v1 - v0) * lay.gu_row));
             uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
-            for (int v = v0; v < v1;) {           // one copy per slot segment
+            for (int v = v0; v < v1;) {           // copies of at most kFusedRowsPerCopy rows of one slot
               const int ps = v / nr, r = v % nr;
-              const int cnt = min(v1 - v, nr - r);
+              const int cnt = min(min(v1 - v, nr - r), kFusedRowsPerCopy);
               ensure_routed(ps);
               if (!*s_abort)
                 bulk_g2s(buf + (size_t)(v - v0) * lay.gu_row, slot_blob(ps) + (size_t)(ra + r) * lay.gu_row,
@@ -328,64 +316,24 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
       }
     } else if (warp == kExchangeWarp || warp == kExchangeWarp2) {
       // ------------------------------------------------------------------
-      // exchangers: routing (the first), then each slot's full h from L2 into
-      // shared memory, the first exchanger taking even slots, the second odd
+      // exchangers: each slot's full h from L2 into shared memory, the first
+      // exchanger taking even slots, the second odd; the second also routes
       // ------------------------------------------------------------------
       const int xw = warp - kExchangeWarp;
-      if (xw == 0) {
-        // top-K by repeated warp-wide max: each lane keeps the largest of its
-        // logits (ties: lowest id); a round takes the warp maximum, the lowest
-        // id holding it, and that lane rescans
-        const float* lg = p.logits + (size_t)l * p.E;
-        const int nv = (p.E + 31) >> 5;
-        uint32_t ord[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int id = lane + 32 * j;
-          ord[j] = (j < nv && id < p.E) ? (uint32_t)(route_key(__ldg(lg + id), id) >> 32) : 0u;
-        }
-        uint32_t bo = 0u;
-        int bj = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (ord[j] > bo) {
-            bo = ord[j];
-            bj = j;
-          }
-        float my_l = 0.f;
-        int my_id = -1;
-        for (int k = 0; k < p.K; ++k) {
-          const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bo);
-          const uint32_t cid = __reduce_min_sync(0xFFFFFFFFu, bo == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
-          if (lane == k) {
-            my_l = key_value((uint64_t)m << 32);
-            my_id = (int)cid;
-          }
-          if ((int)(cid & 31u) == lane) {
-            const int jr = (int)(cid >> 5);
-            bo = 0u;
-            bj = 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j == jr) ord[j] = 0u;
-              if (ord[j] > bo) {
-                bo = ord[j];
-                bj = j;
-              }
-            }
-          }
-        }
-        const float lmax = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-        const float e = lane < p.K ? expf(my_l - lmax) : 0.f;
-        const float etot = warp_sum(e);
+      if (xw == kRouteXw) {
+        // the layer's top-K: computed at the end of the previous layer (the
+        // logits are inputs), or now for the first layer of the launch
+        if (l == 0) warp_topk(p.logits, p.E, p.K, nx_id, nx_l);
+        const int my_id = nx_id;
+        const float my_w = warp_topk_softmax(nx_l, p.K);
         // publish once the consumers hold the whole layer input
         mbar_wait(bar_xready, lpar, tmo, p.err, s_abort);
         if (lane < p.K) {
           s_ids[p.S + lane] = my_id;
-          s_w[p.S + lane] = e / etot;
+          s_w[p.S + lane] = my_w;
           if (c == 0 && p.ids_out != nullptr) {
             p.ids_out[(size_t)l * p.K + lane] = my_id;
-            p.w_out[(size_t)l * p.K + lane] = e / etot;
+            p.w_out[(size_t)l * p.K + lane] = my_w;
           }
         }
         __syncwarp();
@@ -432,6 +380,9 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_hready[q]);
       }
+      // the next layer's top-K, off its critical path; its ids are published
+      // only once that layer's input is complete
+      if (xw == kRouteXw && l + 1 < p.L) warp_topk(p.logits + (size_t)(l + 1) * p.E, p.E, p.K, nx_id, nx_l);
     } else {
       // ------------------------------------------------------------------
       // consumers: 12 gate/up warps and 4 down warps

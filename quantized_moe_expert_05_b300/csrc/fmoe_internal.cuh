@@ -229,58 +229,85 @@ __device__ __forceinline__ float warp_sum(float v, int width = 32) {
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 
-// "a ranks before b": larger logit first, equal logits -> lower id first.
-// Float comparison treats -0 and +0 as equal.
-__device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
-  return av > bv || (av == bv && ai < bi);
+// Top-K key of a logit: an unsigned integer whose order is the order of the
+// fp32 values (larger = larger logit), -0 and +0 mapped to the same key.
+// Valid keys are never 0.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Top-K of E logits + softmax over the selected ones; executed by one full
-// warp (flash-moe write-up, "per-layer pipeline": softmax + top-K routing).
-// Lane k < K receives the k-th pick in (*id_out, *w_out) of its own lane;
-// the function returns (id, weight) for lanes < K and (-1, 0) otherwise.
-// E <= 1024.
-__device__ __forceinline__ void warp_route(const float* __restrict__ logits, int E, int K,
-                                           int& my_id, float& my_w) {
+// The fp32 value of a logit_key.
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Top-K of E logits, executed by one full warp.  Each lane keeps its best
+// remaining key; a round takes the warp maximum (redux.sync), the lowest id
+// holding it, and that lane rescans.  Lane k < K receives the k-th pick
+// (descending logit, equal logits -> lower id) and its logit in (my_id,
+// my_l); other lanes get (-1, 0).  E <= 1024.
+__device__ __forceinline__ void warp_topk(const float* __restrict__ logits, int E, int K, int& my_id,
+                                          float& my_l) {
   const int lane = threadIdx.x & 31;
-  float v[32];
-  uint32_t taken = 0;
   const int nv = (E + 31) >> 5;
+  uint32_t key[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = (j < nv && lane + 32 * j < E) ? __ldg(logits + lane + 32 * j) : 0.f;
-  // local best
-  auto local_best = [&](float& bv, int& bi) {
-    bv = 0.f; bi = 0x7FFFFFFF;
+  for (int j = 0; j < 32; ++j) {
+    const int id = lane + 32 * j;
+    key[j] = (j < nv && id < E) ? logit_key(__ldg(logits + id)) : 0u;
+  }
+  uint32_t bk = 0u;
+  int bj = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int id = lane + 32 * j;
-      if (j < nv && id < E && !((taken >> j) & 1u)) {
-        if (bi == 0x7FFFFFFF || ranks_before(v[j], id, bv, bi)) { bv = v[j]; bi = id; }
+  for (int j = 0; j < 32; ++j)
+    if (key[j] > bk) {
+      bk = key[j];
+      bj = j;
+    }
+  my_l = 0.f;
+  my_id = -1;
+  for (int k = 0; k < K; ++k) {
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cid = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+    if (lane == k) {
+      my_l = key_logit(m);
+      my_id = (int)cid;
+    }
+    if ((int)(cid & 31u) == lane) {        // the winner's lane drops it and rescans
+      const int jr = (int)(cid >> 5);
+      bk = 0u;
+      bj = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j == jr) key[j] = 0u;
+        if (key[j] > bk) {
+          bk = key[j];
+          bj = j;
+        }
       }
     }
-  };
-  float bv; int bi;
-  local_best(bv, bi);
-  my_id = -1;
-  float my_l = 0.f;
-  for (int k = 0; k < K; ++k) {
-    float cv = bv; int ci = bi;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, cv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, ci, o);
-      if (oi != 0x7FFFFFFF && (ci == 0x7FFFFFFF || ranks_before(ov, oi, cv, ci))) { cv = ov; ci = oi; }
-    }
-    if (lane == k) { my_id = ci; my_l = cv; }
-    if ((ci & 31) == lane) {            // the winner's lane drops it and rescans
-      taken |= 1u << (ci >> 5);
-      local_best(bv, bi);
-    }
   }
+}
+
+// Softmax over the K picks of warp_topk (lane k < K holds pick k's logit):
+// the weight of lane k's pick, 0 on other lanes.
+__device__ __forceinline__ float warp_topk_softmax(float my_l, int K) {
+  const int lane = threadIdx.x & 31;
   const float lmax = __shfl_sync(0xFFFFFFFFu, my_l, 0);
   const float e = (lane < K) ? expf(my_l - lmax) : 0.f;
   const float tot = warp_sum(e);
-  my_w = (lane < K) ? e / tot : 0.f;
+  return (lane < K) ? e / tot : 0.f;
+}
+
+// Top-K + softmax over the selected logits (flash-moe write-up, "per-layer
+// pipeline": softmax + top-K routing); one full warp.
+__device__ __forceinline__ void warp_route(const float* __restrict__ logits, int E, int K,
+                                           int& my_id, float& my_w) {
+  float my_l;
+  warp_topk(logits, E, K, my_id, my_l);
+  my_w = warp_topk_softmax(my_l, K);
 }
 
 // Wait until *ctr >= target, for at most timeout_ns; on time-out set the error

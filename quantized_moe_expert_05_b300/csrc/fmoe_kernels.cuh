@@ -70,8 +70,9 @@ constexpr int kDownWarps = 4;                          // down projection + comb
 constexpr int kConsumerWarps = kGuWarps + kDownWarps;  // warps that hold the layer input
 constexpr int kProducerWarp = kConsumerWarps;          // issues the bulk copies
 constexpr int kFinalWarp = kConsumerWarps + 1;         // turns partial sums into h rows
-constexpr int kExchangeWarp = kConsumerWarps + 2;      // routes; gathers the h of even slots
-constexpr int kExchangeWarp2 = kConsumerWarps + 3;     // gathers the h of odd slots
+constexpr int kExchangeWarp = kConsumerWarps + 2;      // gathers the h of even slots
+constexpr int kExchangeWarp2 = kConsumerWarps + 3;     // routes; gathers the h of odd slots
+constexpr int kRouteXw = 1;                            // the exchange warp (0, 1) that routes
 constexpr int kFusedThreads = 32 * (kConsumerWarps + 4);
 // registers per thread: the most that every warp can hold when the warps are
 // spread over the SM's four schedulers, each with 16K registers (8 at a time)
@@ -82,17 +83,26 @@ constexpr int kMaxSlots = FMOE_MAX_TOPK + 1;
 constexpr int kMaxStages = 16;
 // Tuning of the persistent kernel (compile-time; the defaults are the
 // measured best): ring stages at most, slots by which a slot's down records
-// trail its gate/up records, and whether an exchange warp waits for its own
-// block's share of a slot before polling the other blocks' shares.
+// trail its gate/up records, whether an exchange warp waits for its own
+// block's share of a slot before polling the other blocks' shares, and how
+// the block's rows are split into bulk copies.
 #ifndef FMOE_FUSED_STAGE_CAP
 #define FMOE_FUSED_STAGE_CAP 16
 #endif
 #ifndef FMOE_FUSED_DOWN_LAG
-#define FMOE_FUSED_DOWN_LAG 2
+#define FMOE_FUSED_DOWN_LAG 3
 #endif
 #ifndef FMOE_XCHG_WAIT_OWN
-#define FMOE_XCHG_WAIT_OWN 0
+#define FMOE_XCHG_WAIT_OWN 1
 #endif
+#ifndef FMOE_FUSED_ROWS_PER_COPY
+#define FMOE_FUSED_ROWS_PER_COPY 64
+#endif
+#ifndef FMOE_FUSED_DOWN_COPIES
+#define FMOE_FUSED_DOWN_COPIES 1
+#endif
+constexpr int kFusedRowsPerCopy = FMOE_FUSED_ROWS_PER_COPY;   // gate/up records per bulk copy
+constexpr int kFusedDownCopies = FMOE_FUSED_DOWN_COPIES;      // bulk copies per slot's down records
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
 constexpr int kFusedDownLag = FMOE_FUSED_DOWN_LAG;
 constexpr int kMaxDownGroups = 8;      // down row groups per down warp
