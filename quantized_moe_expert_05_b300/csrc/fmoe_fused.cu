@@ -84,7 +84,7 @@ __device__ __forceinline__ void ll_wait8(const unsigned long long* p, uint32_t t
       *abort = 1;
       return;
     }
-    __nanosleep(32);
+    __nanosleep(kInputPollNs);
   }
 }
 
@@ -97,13 +97,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Block-wide barrier, counted per thread: the warps of this kernel take
-// different paths and may reach it diverged (a lane running a loop alone, a
-// row owner storing), which the aligned form (__syncthreads) does not allow.
-__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+// Block-wide barrier.  The warps of this kernel take different paths and
+// reach it after divergent code (a lane running a loop alone, a row owner
+// storing); each warp first reconverges all of its lanes, so that the barrier
+// counts whole warps that arrive once each.
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  asm volatile("barrier.sync 0;" ::: "memory");
+}
 
-// named barrier over the consumer warps only (per-thread count, as above)
+// named barrier over the consumer warps only (reconverged, as above)
 __device__ __forceinline__ void consumer_sync() {
+  __syncwarp();
   asm volatile("barrier.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
@@ -138,10 +143,12 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   uint64_t* bar_slot = bar_routed + kMaxSlots;                      // slot's partial sums written
   uint64_t* bar_hready = bar_slot + kMaxSlots;                      // slot's full h staged
   uint64_t* bar_xready = bar_hready + kMaxSlots;                    // layer input complete (consumers)
-  int* s_ids = reinterpret_cast<int*>(smem + 832);                  // [kMaxSlots]
-  float* s_w = reinterpret_cast<float*>(smem + 960);                // [kMaxSlots] routing weights, shared gate
-  float* s_red = reinterpret_cast<float*>(smem + 1088);             // [kConsumerWarps][2]
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 1280);
+  uint64_t* bar_ddone = bar_xready + 1;                             // slot's down records used (down warps)
+  uint64_t* bar_layer = bar_ddone + kMaxSlots;                      // layer done (every warp but the producer)
+  int* s_ids = reinterpret_cast<int*>(smem + 1024);                 // [kMaxSlots]
+  float* s_w = reinterpret_cast<float*>(smem + 1152);               // [kMaxSlots] routing weights, shared gate
+  float* s_red = reinterpret_cast<float*>(smem + 1280);             // [kConsumerWarps][2]
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 1408);
   float* s_part = reinterpret_cast<float*>(smem + pl.part_off);    // [slot][row][part][2]
   unsigned long long* s_stage = reinterpret_cast<unsigned long long*>(smem + pl.stage_off);  // one slot's h words
   uint8_t* s_hs = smem + pl.hs_off;                                // [slot] h slices + slice sums
@@ -204,6 +211,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
       mbar_init(&bar_hready[i], 1);
     }
     mbar_init(bar_xready, 1);
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&bar_ddone[i], kDownWarps);
+    mbar_init(bar_layer, kFusedThreads / 32 - 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -236,6 +245,10 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
       // ------------------------------------------------------------------
       // producer: one lane issues every copy of the layer in consumption order
       // ------------------------------------------------------------------
+#if FMOE_FUSED_LATE_PREFETCH
+      // the previous layer's exchanges go first: its last slot's h staged
+      if (lane == 0 && l > 0) mbar_wait(&bar_hready[NS - 1], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
+#endif
       if (lane == 0) {
         auto slot_blob = [&](int ps) -> const uint8_t* {
           if (p.S && ps == 0) return lp.shared;
@@ -250,10 +263,13 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
         };
         auto issue_down = [&](int ps) {
           if (nd == 0 || *s_abort) {
+            if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
             mbar_arrive_expect_tx(&bar_dfull[ps], 0);
             return;
           }
           ensure_routed(ps);
+          // the previous layer's down warps are done with this slot's area
+          if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
           const uint32_t bytes = (uint32_t)(nd * lay.d_row);
           mbar_arrive_expect_tx(&bar_dfull[ps], bytes);
           // a few copies: the copy engine streams several at once
@@ -368,7 +384,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             *s_abort = 1;
             break;
           }
-          __nanosleep(32);
+          __nanosleep(kExchangePollNs);
         }
         // pre-scale into the padded slice-major layout; lane = position in the
         // slice, so that the reads are consecutive and the stores hit 32 banks
@@ -557,11 +573,11 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
                 c67 = __fadd2_rn(c67, hs[2 * j + 1]);
               }
             }
-            float hsm = (c01.x / pos_scale<BITS>(0) + c01.y / pos_scale<BITS>(1)) +
-                        (c23.x / pos_scale<BITS>(2) + c23.y / pos_scale<BITS>(3));
+            float hsm = (c01.x * inv_pos_scale<BITS>(0) + c01.y * inv_pos_scale<BITS>(1)) +
+                        (c23.x * inv_pos_scale<BITS>(2) + c23.y * inv_pos_scale<BITS>(3));
             if (BITS == 2)
-              hsm += (c45.x / pos_scale<BITS>(4) + c45.y / pos_scale<BITS>(5)) +
-                     (c67.x / pos_scale<BITS>(6) + c67.y / pos_scale<BITS>(7));
+              hsm += (c45.x * inv_pos_scale<BITS>(4) + c45.y * inv_pos_scale<BITS>(5)) +
+                     (c67.x * inv_pos_scale<BITS>(6) + c67.y * inv_pos_scale<BITS>(7));
 #pragma unroll
             for (int gi = 0; gi < kMaxDownGroups; ++gi) {
               const int grp = dw + kDownWarps * gi;
@@ -576,6 +592,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
               }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_ddone[ps]);
         }
         // combine + residual, written by each row's owner
 #pragma unroll
@@ -591,8 +609,16 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
       }
     }
 
-    // ---- end of layer: every role is done with this layer's shared memory ----
-    cta_sync();
+    // ---- end of layer: every role but the producer is done with this
+    // layer's shared memory.  The producer runs on into the next layer: the
+    // ring's stages come back to it through bar_empty and the down areas
+    // through bar_ddone, so it may request the next layer's shared expert
+    // while this layer's down projection finishes.
+    if (warp != kProducerWarp) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_layer);
+      mbar_wait(bar_layer, lpar, tmo, p.err, s_abort);
+    }
   }
 
   // No copy may still be writing this block's shared memory when it exits:

@@ -132,6 +132,14 @@ __device__ __forceinline__ float pos_scale(int i) {
   return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
+// 1 / pos_scale(i), exactly (a power of two).
+template <int BITS>
+__device__ __forceinline__ float inv_pos_scale(int i) {
+  const int p = (BITS == 4) ? (i & 3) : (i & 7);
+  const int e = 149 - kXScaleExp - BITS * p;                // 85 - BITS*p
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
 // The 32 inputs of a slice, pre-scaled by pos_scale, as 16 pairs (element
 // 2k in .x, 2k+1 in .y) so that each packed fp32x2 FMA takes one pair.
 typedef float2 SliceX[kSlice / 2];

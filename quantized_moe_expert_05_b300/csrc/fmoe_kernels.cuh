@@ -65,8 +65,11 @@ cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st);
 // ---------------------------------------------------------------------------
 // single-launch persistent kernel (fmoe_fused.cu)
 // ---------------------------------------------------------------------------
-constexpr int kGuWarps = 12;                           // dequantised gate/up GEMV warps
-constexpr int kDownWarps = 4;                          // down projection + combine warps
+#ifndef FMOE_FUSED_GU_WARPS
+#define FMOE_FUSED_GU_WARPS 12
+#endif
+constexpr int kGuWarps = FMOE_FUSED_GU_WARPS;          // dequantised gate/up GEMV warps
+constexpr int kDownWarps = 16 - kGuWarps;              // down projection + combine warps
 constexpr int kConsumerWarps = kGuWarps + kDownWarps;  // warps that hold the layer input
 constexpr int kProducerWarp = kConsumerWarps;          // issues the bulk copies
 constexpr int kFinalWarp = kConsumerWarps + 1;         // turns partial sums into h rows
@@ -84,8 +87,10 @@ constexpr int kMaxStages = 16;
 // Tuning of the persistent kernel (compile-time; the defaults are the
 // measured best): ring stages at most, slots by which a slot's down records
 // trail its gate/up records, whether an exchange warp waits for its own
-// block's share of a slot before polling the other blocks' shares, and how
-// the block's rows are split into bulk copies.
+// block's share of a slot before polling the other blocks' shares, whether
+// the producer waits for the previous layer's last exchange before it
+// requests the next layer's rows (its copies would otherwise queue ahead of
+// the exchange's loads), and how the block's rows are split into bulk copies.
 #ifndef FMOE_FUSED_STAGE_CAP
 #define FMOE_FUSED_STAGE_CAP 16
 #endif
@@ -95,6 +100,20 @@ constexpr int kMaxStages = 16;
 #ifndef FMOE_XCHG_WAIT_OWN
 #define FMOE_XCHG_WAIT_OWN 1
 #endif
+#ifndef FMOE_FUSED_LATE_PREFETCH
+#define FMOE_FUSED_LATE_PREFETCH 1
+#endif
+// Pause between two polls of published (value, tag) words: every block
+// polls the same few lines of L2, so polling too often slows down the
+// stores it is waiting for.
+#ifndef FMOE_INPUT_POLL_NS
+#define FMOE_INPUT_POLL_NS 32
+#endif
+#ifndef FMOE_EXCHANGE_POLL_NS
+#define FMOE_EXCHANGE_POLL_NS 32
+#endif
+constexpr unsigned kInputPollNs = FMOE_INPUT_POLL_NS;
+constexpr unsigned kExchangePollNs = FMOE_EXCHANGE_POLL_NS;
 #ifndef FMOE_FUSED_ROWS_PER_COPY
 #define FMOE_FUSED_ROWS_PER_COPY 64
 #endif
