@@ -130,6 +130,46 @@ __device__ __forceinline__ float quad_reduce(float a, float b, float c, float d,
 
 }  // namespace
 
+// Slice s of a slot's staged h (float4 j of slice s at j*hstride + s, already
+// pre-scaled): the 32 values as pairs, and their plain sum, taken from the
+// pre-scaled values one position class at a time (an exact power-of-two
+// rescaling each).
+template <int BITS>
+__device__ __forceinline__ float staged_h_slice(const float4* hs4, int hstride, int s, SliceX& hs) {
+  float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
+  float2 c45 = make_float2(0.f, 0.f), c67 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kSlice / 4; ++j) {
+    const float4 v = hs4[(size_t)j * hstride + s];
+    hs[2 * j] = make_float2(v.x, v.y);
+    hs[2 * j + 1] = make_float2(v.z, v.w);
+    if (BITS == 4 || (j & 1) == 0) {
+      c01 = __fadd2_rn(c01, hs[2 * j]);
+      c23 = __fadd2_rn(c23, hs[2 * j + 1]);
+    } else {
+      c45 = __fadd2_rn(c45, hs[2 * j]);
+      c67 = __fadd2_rn(c67, hs[2 * j + 1]);
+    }
+  }
+  float hsm = (c01.x * inv_pos_scale<BITS>(0) + c01.y * inv_pos_scale<BITS>(1)) +
+              (c23.x * inv_pos_scale<BITS>(2) + c23.y * inv_pos_scale<BITS>(3));
+  if (BITS == 2)
+    hsm += (c45.x * inv_pos_scale<BITS>(4) + c45.y * inv_pos_scale<BITS>(5)) +
+           (c67.x * inv_pos_scale<BITS>(6) + c67.y * inv_pos_scale<BITS>(7));
+  return hsm;
+}
+
+// w * (down row r . h) over slice s: the row's record in shared memory.
+template <int BITS>
+__device__ __forceinline__ float down_slice(const uint8_t* rec, const BlobLayout& lay, int s, const SliceX& hs,
+                                            float hsm, float w, float acc) {
+  SliceCodes<BITS> q;
+  if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
+  else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
+  const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
+  return fmaf(w, slice_term<BITS>(q, sbw, hs, hsm), acc);
+}
+
 template <int BITS>
 __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -145,6 +185,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   uint64_t* bar_xready = bar_hready + kMaxSlots;                    // layer input complete (consumers)
   uint64_t* bar_ddone = bar_xready + 1;                             // slot's down records used (down warps)
   uint64_t* bar_layer = bar_ddone + kMaxSlots;                      // layer done (every warp but the producer)
+  uint64_t* bar_tail = bar_layer + 1;                               // tail slots' down rows done (gate/up warps)
+  float* s_tail = reinterpret_cast<float*>(smem + 1536);            // [nd] tail slots' sum per down row
   int* s_ids = reinterpret_cast<int*>(smem + 1024);                 // [kMaxSlots]
   float* s_w = reinterpret_cast<float*>(smem + 1152);               // [kMaxSlots] routing weights, shared gate
   float* s_red = reinterpret_cast<float*>(smem + 1280);             // [kConsumerWarps][2]
@@ -198,6 +240,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   const int spl = tld > 32 ? tld / 32 : 1;
   const int ngroups = (nd + rpp - 1) / rpp;
   const int dlag = pl.dlag;
+  // slots whose down rows the gate/up warps take over at the end of a layer
+  const int ntail = NS - 1 < kFusedTailSlots ? NS - 1 : kFusedTailSlots;
 
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -213,6 +257,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
     mbar_init(bar_xready, 1);
     for (int i = 0; i < kMaxSlots; ++i) mbar_init(&bar_ddone[i], kDownWarps);
     mbar_init(bar_layer, kFusedThreads / 32 - 1);
+    mbar_init(bar_tail, kGuWarps);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -527,6 +572,43 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             ++next_done;
           }
         }
+        if (ntail > 0) {
+          // the last slots' down rows: by the time their h is gathered the
+          // gate/up warps are idle, and twelve warps finish a slot sooner
+          // than the four down warps, whose every instruction waits on the
+          // one before it
+          float tacc[kMaxTailGroups];
+#pragma unroll
+          for (int gi = 0; gi < kMaxTailGroups; ++gi) tacc[gi] = 0.f;
+          for (int ps = NS - ntail; ps < NS; ++ps) {
+            mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
+            mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
+            const float wk = s_w[ps];
+            const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
+            const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
+            for (int k = 0; k < spl; ++k) {
+              const int s = (lane % lpr) + 32 * k;
+              SliceX hs;
+              const float hsm = staged_h_slice<BITS>(hs4, hstride, s, hs);
+#pragma unroll
+              for (int gi = 0; gi < kMaxTailGroups; ++gi) {
+                const int grp = warp + kGuWarps * gi;
+                const int r = grp * rpp + lane / lpr;
+                if (grp < ngroups && r < nd)
+                  tacc[gi] = down_slice<BITS>(buf + (size_t)r * lay.d_row, lay, s, hs, hsm, wk, tacc[gi]);
+              }
+            }
+          }
+#pragma unroll
+          for (int gi = 0; gi < kMaxTailGroups; ++gi) {
+            const int grp = warp + kGuWarps * gi;
+            const float v = warp_sum(tacc[gi], lpr);
+            const int r = grp * rpp + lane / lpr;
+            if (grp < ngroups && r < nd && (lane % lpr) == 0) s_tail[r] = v;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tail);
+        }
       } else {
         // ---------------- down projection + combine + residual -------------
         const int dw = warp - kGuWarps;
@@ -547,7 +629,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             }
           }
         }
-        for (int ps = 0; ps < NS; ++ps) {
+        for (int ps = 0; ps < NS - ntail; ++ps) {
           mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
           mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
           const float wk = s_w[ps];
@@ -556,44 +638,24 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           for (int k = 0; k < spl; ++k) {
             const int s = (lane % lpr) + 32 * k;
             SliceX hs;
-            // the slice's plain sum, from the pre-scaled values: one partial sum
-            // per position class (an exact power-of-two rescaling each)
-            float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
-            float2 c45 = make_float2(0.f, 0.f), c67 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < kSlice / 4; ++j) {
-              const float4 v = hs4[(size_t)j * hstride + s];
-              hs[2 * j] = make_float2(v.x, v.y);
-              hs[2 * j + 1] = make_float2(v.z, v.w);
-              if (BITS == 4 || (j & 1) == 0) {
-                c01 = __fadd2_rn(c01, hs[2 * j]);
-                c23 = __fadd2_rn(c23, hs[2 * j + 1]);
-              } else {
-                c45 = __fadd2_rn(c45, hs[2 * j]);
-                c67 = __fadd2_rn(c67, hs[2 * j + 1]);
-              }
-            }
-            float hsm = (c01.x * inv_pos_scale<BITS>(0) + c01.y * inv_pos_scale<BITS>(1)) +
-                        (c23.x * inv_pos_scale<BITS>(2) + c23.y * inv_pos_scale<BITS>(3));
-            if (BITS == 2)
-              hsm += (c45.x * inv_pos_scale<BITS>(4) + c45.y * inv_pos_scale<BITS>(5)) +
-                     (c67.x * inv_pos_scale<BITS>(6) + c67.y * inv_pos_scale<BITS>(7));
+            const float hsm = staged_h_slice<BITS>(hs4, hstride, s, hs);
 #pragma unroll
             for (int gi = 0; gi < kMaxDownGroups; ++gi) {
               const int grp = dw + kDownWarps * gi;
               const int r = grp * rpp + lane / lpr;
-              if (grp < ngroups && r < nd) {
-                const uint8_t* rec = buf + (size_t)r * lay.d_row;
-                SliceCodes<BITS> q;
-                if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
-                else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
-                const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
-                acc[gi] = fmaf(wk, slice_term<BITS>(q, sbw, hs, hsm), acc[gi]);
-              }
+              if (grp < ngroups && r < nd)
+                acc[gi] = down_slice<BITS>(buf + (size_t)r * lay.d_row, lay, s, hs, hsm, wk, acc[gi]);
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar_ddone[ps]);
+        }
+        if (ntail > 0) {
+          // the tail slots' rows were done by the gate/up warps
+          mbar_wait(bar_tail, lpar, tmo, p.err, s_abort);
+          __syncwarp();
+          if (lane == 0)
+            for (int ps = NS - ntail; ps < NS; ++ps) mbar_arrive(&bar_ddone[ps]);
         }
         // combine + residual, written by each row's owner
 #pragma unroll
@@ -602,8 +664,9 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           const float v = warp_sum(acc[gi], lpr);
           const int r = grp * rpp + lane / lpr;
           if (grp < ngroups && r < nd && (lane % lpr) == 0) {
-            if (out_ll) ll_store(out_llp + ja + r, resv[gi] + v, tag);
-            else p.out[ja + r] = resv[gi] + v;
+            const float o = resv[gi] + v + (ntail > 0 ? s_tail[r] : 0.f);
+            if (out_ll) ll_store(out_llp + ja + r, o, tag);
+            else p.out[ja + r] = o;
           }
         }
       }
@@ -677,6 +740,7 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
   const int ndmax = (H + grid - 1) / grid;
   const int lpr = tld < 32 ? tld : 32, rpp = 32 / lpr;
   if ((ndmax + rpp - 1) / rpp > kMaxDownGroups * kDownWarps) return pl;
+  if ((ndmax + rpp - 1) / rpp > kMaxTailGroups * kGuWarps || ndmax > kMaxTailRows) return pl;
   pl.dslot_bytes = round_up_i((long long)ndmax * lay.d_row, 128);
   pl.nrmax = (I + grid - 1) / grid;
   pl.hs_slot_bytes = round_up_i((long long)8 * (tld + 1) * 16, 128);

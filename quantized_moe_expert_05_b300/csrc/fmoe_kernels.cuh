@@ -114,6 +114,10 @@ constexpr int kMaxStages = 16;
 #endif
 constexpr unsigned kInputPollNs = FMOE_INPUT_POLL_NS;
 constexpr unsigned kExchangePollNs = FMOE_EXCHANGE_POLL_NS;
+#ifndef FMOE_FUSED_TAIL_SLOTS
+#define FMOE_FUSED_TAIL_SLOTS 2
+#endif
+constexpr int kFusedTailSlots = FMOE_FUSED_TAIL_SLOTS;   // last slots whose down rows the gate/up warps do
 #ifndef FMOE_FUSED_ROWS_PER_COPY
 #define FMOE_FUSED_ROWS_PER_COPY 64
 #endif
@@ -125,7 +129,9 @@ constexpr int kFusedDownCopies = FMOE_FUSED_DOWN_COPIES;      // bulk copies per
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
 constexpr int kFusedDownLag = FMOE_FUSED_DOWN_LAG;
 constexpr int kMaxDownGroups = 8;      // down row groups per down warp
-constexpr int kCtrlBytes = 1536;       // barriers, routing result, reductions
+constexpr int kCtrlBytes = 2048;       // barriers, routing result, reductions, tail sums
+constexpr int kMaxTailRows = (kCtrlBytes - 1536) / 4;   // down rows per block the tail sums can hold
+constexpr int kMaxTailGroups = 4;      // down row groups per gate/up warp in the tail
 
 struct FusedLayerPtrs {
   const uint8_t* experts;
