@@ -263,7 +263,8 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
   }
   cta_sync();
 
-  uint32_t g_issue = 0;   // gate/up stages issued (producer lane 0)
+  uint32_t g_issue = 0;   // gate/up stages issued (producer warp)
+  uint32_t n_copies = 0;  // bulk copies issued (producer warp): picks the issuing lane
   uint32_t g_cons = 0;    // gate/up stages consumed (consumer warps)
   const unsigned long long tmo = p.timeout_ns;
   // tags of this launch: layer l publishes with epoch * 64 + l + 1 (never 0,
@@ -288,72 +289,78 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
 
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------------
-      // producer: one lane issues every copy of the layer in consumption order
+      // producer: the warp walks the layer's copies in consumption order;
+      // lane 0 declares each barrier's bytes, and successive copies are
+      // issued by successive lanes: the copies one thread issues are carried
+      // out one after another, those of different threads side by side
       // ------------------------------------------------------------------
 #if FMOE_FUSED_LATE_PREFETCH
       // the previous layer's exchanges go first: its last slot's h staged
-      if (lane == 0 && l > 0) mbar_wait(&bar_hready[NS - 1], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
+      if (l > 0) mbar_wait(&bar_hready[NS - 1], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
 #endif
-      if (lane == 0) {
-        auto slot_blob = [&](int ps) -> const uint8_t* {
-          if (p.S && ps == 0) return lp.shared;
-          return lp.experts + (size_t)s_ids[ps] * p.blob;
-        };
-        bool routed = false;       // routed ids are published all at once
-        auto ensure_routed = [&](int ps) {
-          if (ps >= p.S && !routed) {
-            mbar_wait(&bar_routed[0], lpar, tmo, p.err, s_abort);
-            routed = true;
-          }
-        };
-        auto issue_down = [&](int ps) {
-          if (nd == 0 || *s_abort) {
-            if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
-            mbar_arrive_expect_tx(&bar_dfull[ps], 0);
-            return;
-          }
-          ensure_routed(ps);
-          // the previous layer's down warps are done with this slot's area
-          if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
-          const uint32_t bytes = (uint32_t)(nd * lay.d_row);
-          mbar_arrive_expect_tx(&bar_dfull[ps], bytes);
-          // a few copies: the copy engine streams several at once
-          const int per = (nd + kFusedDownCopies - 1) / kFusedDownCopies;
-          for (int r0 = 0; r0 < nd; r0 += per)
-            bulk_g2s(darea + (size_t)ps * pl.dslot_bytes + (size_t)r0 * lay.d_row,
-                     slot_blob(ps) + lay.d_off + (size_t)(ja + r0) * lay.d_row,
-                     (uint32_t)(min(per, nd - r0) * lay.d_row), &bar_dfull[ps]);
-        };
-        int dnext = 0;
-        for (int k = 0; k < nstg; ++k) {
-          const uint32_t st = g_issue % pl.nstage;
-          const uint32_t use = g_issue / pl.nstage;
-          ++g_issue;
-          if (use >= 1) mbar_wait(&bar_empty[st], (use - 1) & 1u, tmo, p.err, s_abort);
-          const int v0 = k * R, v1 = min(V, v0 + R);
-          if (*s_abort) {
-            mbar_arrive_expect_tx(&bar_full[st], 0);
-          } else {
-            // the stage's bytes are expected up front; the shared expert's
-            // segment goes out at once, routed segments once ids are known
-            mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((v1 - v0) * lay.gu_row));
-            uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
-            for (int v = v0; v < v1;) {           // copies of at most kFusedRowsPerCopy rows of one slot
-              const int ps = v / nr, r = v % nr;
-              const int cnt = min(min(v1 - v, nr - r), kFusedRowsPerCopy);
-              ensure_routed(ps);
-              if (!*s_abort)
-                bulk_g2s(buf + (size_t)(v - v0) * lay.gu_row, slot_blob(ps) + (size_t)(ra + r) * lay.gu_row,
-                         (uint32_t)(cnt * lay.gu_row), &bar_full[st]);
-              v += cnt;
-            }
-          }
-          // down records of slots whose gate/up is dlag slots behind
-          const int slots_issued = v1 / nr;
-          while (dnext < slots_issued - dlag) issue_down(dnext++);
+      auto slot_blob = [&](int ps) -> const uint8_t* {
+        if (p.S && ps == 0) return lp.shared;
+        return lp.experts + (size_t)s_ids[ps] * p.blob;
+      };
+      // lane 0's view of the abort flag, the same in every lane
+      auto aborted = [&]() -> bool { return __shfl_sync(0xFFFFFFFFu, *s_abort, 0) != 0; };
+      bool routed = false;       // routed ids are published all at once
+      auto ensure_routed = [&](int ps) {
+        if (ps >= p.S && !routed) {
+          mbar_wait(&bar_routed[0], lpar, tmo, p.err, s_abort);
+          routed = true;
         }
-        while (dnext < NS) issue_down(dnext++);
+      };
+      auto copy = [&](void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+        if (lane == (int)(n_copies % kFusedIssueLanes)) bulk_g2s(dst, src, bytes, bar);
+        ++n_copies;
+      };
+      auto issue_down = [&](int ps) {
+        // the previous layer's down work is done with this slot's area
+        if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
+        if (nd == 0 || aborted()) {
+          if (lane == 0) mbar_arrive_expect_tx(&bar_dfull[ps], 0);
+          return;
+        }
+        ensure_routed(ps);
+        if (lane == 0) mbar_arrive_expect_tx(&bar_dfull[ps], (uint32_t)(nd * lay.d_row));
+        __syncwarp();
+        const int per = (nd + kFusedDownCopies - 1) / kFusedDownCopies;
+        for (int r0 = 0; r0 < nd; r0 += per)
+          copy(darea + (size_t)ps * pl.dslot_bytes + (size_t)r0 * lay.d_row,
+               slot_blob(ps) + lay.d_off + (size_t)(ja + r0) * lay.d_row, (uint32_t)(min(per, nd - r0) * lay.d_row),
+               &bar_dfull[ps]);
+      };
+      int dnext = 0;
+      for (int k = 0; k < nstg; ++k) {
+        const uint32_t st = g_issue % pl.nstage;
+        const uint32_t use = g_issue / pl.nstage;
+        ++g_issue;
+        if (use >= 1) mbar_wait(&bar_empty[st], (use - 1) & 1u, tmo, p.err, s_abort);
+        const int v0 = k * R, v1 = min(V, v0 + R);
+        if (aborted()) {
+          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], 0);
+        } else {
+          // the stage's bytes are expected up front; the shared expert's
+          // segment goes out at once, routed segments once ids are known
+          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((v1 - v0) * lay.gu_row));
+          __syncwarp();
+          uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
+          for (int v = v0; v < v1;) {           // copies of at most kFusedRowsPerCopy rows of one slot
+            const int ps = v / nr, r = v % nr;
+            const int cnt = min(min(v1 - v, nr - r), kFusedRowsPerCopy);
+            ensure_routed(ps);
+            if (!aborted())
+              copy(buf + (size_t)(v - v0) * lay.gu_row, slot_blob(ps) + (size_t)(ra + r) * lay.gu_row,
+                   (uint32_t)(cnt * lay.gu_row), &bar_full[st]);
+            v += cnt;
+          }
+        }
+        // down records of slots whose gate/up is dlag slots behind
+        const int slots_issued = v1 / nr;
+        while (dnext < slots_issued - dlag) issue_down(dnext++);
       }
+      while (dnext < NS) issue_down(dnext++);
       __syncwarp();
     } else if (warp == kFinalWarp) {
       // ------------------------------------------------------------------

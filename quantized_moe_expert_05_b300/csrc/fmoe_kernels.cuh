@@ -118,6 +118,10 @@ constexpr unsigned kExchangePollNs = FMOE_EXCHANGE_POLL_NS;
 #define FMOE_FUSED_TAIL_SLOTS 2
 #endif
 constexpr int kFusedTailSlots = FMOE_FUSED_TAIL_SLOTS;   // last slots whose down rows the gate/up warps do
+#ifndef FMOE_FUSED_ISSUE_LANES
+#define FMOE_FUSED_ISSUE_LANES 4
+#endif
+constexpr int kFusedIssueLanes = FMOE_FUSED_ISSUE_LANES;   // producer lanes that take turns issuing copies
 #ifndef FMOE_FUSED_ROWS_PER_COPY
 #define FMOE_FUSED_ROWS_PER_COPY 64
 #endif
