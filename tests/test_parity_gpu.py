@@ -369,6 +369,57 @@ def test_stack48_tokens(fm, stack48_layers):
         assert_close(h.cpu().numpy(), ref, what=f"stack48 token {t}")
 
 
+# ---------------------------------------------------------------------------
+# the bench's launch: a chain of Qwen-shaped blocks in one persistent launch
+# (one routed pool for every block, each block its own shared expert and gate)
+# ---------------------------------------------------------------------------
+def _qwen_chain_layers(fm, shape, n, pool):
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+    shared = torch.empty(n * nw, dtype=torch.int32, device="cuda")
+    synth.fill_pool(shared, shape, 0, shape.n_experts, n)
+    return [fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool, shared[l * nw:(l + 1) * nw],
+                     synth.shared_gate_vector(shape, l).cuda()) for l in range(n)]
+
+
+def _oracle_chain(shape, h0, logits):
+    """The chain as the oracle computes it: block l uses routed experts of the
+    common pool and shared expert n_experts + l with gate vector l."""
+    return oracle.stack_decode(lambda l, e: oracle_expert(shape, 0, e), h0, logits, shape.top_k, shape.eps,
+                               lambda l: oracle_expert(shape, 0, shape.n_experts + l),
+                               lambda l: synth.shared_gate_vector(shape, l).numpy().view(np.uint16))
+
+
+def test_qwen_chain_as_benched(fm, qwen_pools):
+    """Four chained Qwen 4-bit blocks against the oracle; then the 64-block
+    launch the bench times equals sixteen 4-block launches bit for bit (every
+    block runs the same code on the same input whichever launch it is in)."""
+    import dataclasses
+    shape = synth.QWEN_Q4
+    n = 64
+    layers = _qwen_chain_layers(fm, shape, n, qwen_pools[shape.name])
+    h0, logits = synth.stack_inputs(dataclasses.replace(shape, n_layers=n), 1)
+    ws = fm.new_workspace(layers[0], 1, shape.top_k, n)
+    h4 = h0[0].clone().cuda()
+    fm.stack_decode(layers[:4], logits[0, :4].contiguous().cuda(), h4, shape.top_k, shape.eps, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    ref, ids = _oracle_chain(dataclasses.replace(shape, n_layers=4), h0[0].numpy(), logits[0, :4].numpy())
+    assert_close(h4.cpu().numpy(), ref, what="4-block Qwen chain")
+    got_ids = fm.ws_routing(ws, layers[0], 4, shape.top_k)["ids"].cpu().numpy()
+    assert np.array_equal(got_ids, np.asarray(ids)), (got_ids, ids)
+
+    whole = h0[0].clone().cuda()
+    fm.stack_decode(layers, logits[0].cuda(), whole, shape.top_k, shape.eps, ws)
+    parts = h0[0].clone().cuda()
+    for l0 in range(0, n, 4):
+        fm.stack_decode(layers[l0:l0 + 4], logits[0, l0:l0 + 4].contiguous().cuda(), parts, shape.top_k,
+                        shape.eps, ws)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    assert torch.equal(whole, parts)
+    assert torch.isfinite(whole).all()
+
+
 def test_generator_cpu_gpu_identical():
     for shape, e in ((synth.QWEN_Q4, 7), (synth.QWEN_Q2, 300), (synth.STACK48, 511)):
         a = synth.expert_blob(shape, 3, e, device="cpu")
