@@ -16,7 +16,7 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 64          # quantisation group: 64 consecutive input columns of a row
-_ALIGN = 256        # every plane of a blob starts on a 256-byte boundary
+_ALIGN = 256        # the down records and the blob size are aligned to 256 bytes
 
 
 # ---------------------------------------------------------------------------
