@@ -105,8 +105,9 @@ size_t fmoe_expert_bytes(int bits, int hidden, int inter, int group);
 /*
  * Bytes of workspace a call needs for `layer`, T tokens, K routed experts and
  * L stacked layers (L = 1 for the single-block calls).  The workspace holds
- * intermediate activations, routing results, device-wide counters and the
- * device error word.  It must be 256-byte aligned and zeroed once before its
+ * intermediate activations, routing results, the batch plan, the words the
+ * persistent kernel's blocks exchange (tagged with a launch count kept in the
+ * workspace) and the device error word.  It must be 256-byte aligned and zeroed once before its
  * first use (fmoe_workspace_init); afterwards the library keeps it
  * consistent.  Calls that share a workspace must not overlap in time.
  */
@@ -263,7 +264,7 @@ fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected,
  * The first call on a device looks up the array's device address on that
  * device (the device current at the call); make that first call before any
  * stream capture.  Every call on a device uses the same array, and each call
- * clears its error word and counters first: calls that overlap on the GPU
+ * clears its error word and exit count first: calls that overlap on the GPU
  * (other streams, or other host threads) race on it and must be serialised
  * by the caller.  The routing result is not kept.
  */

@@ -32,7 +32,7 @@ constexpr int kSlice = 32;            // codes per lane slice (16 B at 4-bit, 8 
 constexpr int kXScaleExp = 64;        // products carry a factor 2^-64
 
 // error-word bits
-constexpr uint32_t kErrWaitTimeout = 1u;   // device-wide counter wait ran out
+constexpr uint32_t kErrWaitTimeout = 1u;   // a wait on words of other blocks (or a counter) ran out
 constexpr uint32_t kErrCopyTimeout = 2u;   // bulk-copy barrier wait ran out
 constexpr uint32_t kErrBadExpert = 4u;     // expert id outside [0, E)
 
