@@ -472,42 +472,53 @@ struct UnitShape {
 
 constexpr int kCopiesPerUnit = 4;
 
-// The producer side, run by one lane: stream the records of the block's
-// units [u0, u1) into the ring, in order.  Returns after its last copy has
-// landed (bounded), so that no copy outlives the block.
+// The producer side, run by the producer warp: stream the records of the
+// block's units [u0, u1) into the ring, in order.  Lane 0 waits for free
+// stages and declares each stage's bytes; the unit's copies are issued by
+// lanes 0.. kCopiesPerUnit-1, one each: the copies one thread issues are
+// carried out one after another, those of different threads side by side.
+// Returns after the last copy has landed (bounded), so that no copy outlives
+// the block.
 __device__ void batch_produce(const BatchArgs& a, BatchCtrl* ctl, uint8_t* ring, int nstage, int stage_bytes,
                               long long u0, long long u1, int n_rb, const UnitShape us) {
+  const int lane = threadIdx.x & 31;
   const uint32_t bytes = (uint32_t)(us.rows * us.rec_bytes);
+  const int per = (us.rows + kCopiesPerUnit - 1) / kCopiesPerUnit;
   int cur_item = -1, expert = 0;
   long long k = 0;
   for (long long u = u0; u < u1; ++u, ++k) {
     const int st = (int)(k % nstage);
     const uint32_t use = (uint32_t)(k / nstage);
-    if (use >= 1 && !mbar_wait(&ctl->empty[st], (use - 1) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
+    bool ok = true;
+    if (lane == 0 && use >= 1) ok = mbar_wait(&ctl->empty[st], (use - 1) & 1u, a.timeout_ns, a.err, &ctl->abort);
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
     const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
     if (item != cur_item) {
       expert = __ldcg(a.plan + kPlanHeader + item * kItemWords);
       cur_item = item;
     }
     const uint8_t* src = item_blob(a, expert) + us.part + (size_t)rb * us.rows * us.rec_bytes;
-    mbar_arrive_expect_tx(&ctl->full[st], bytes);
-    // a few copies per unit: the copy engine streams several at once
-    const int per = (us.rows + kCopiesPerUnit - 1) / kCopiesPerUnit;
-    for (int r0 = 0; r0 < us.rows; r0 += per) {
+    if (lane == 0) mbar_arrive_expect_tx(&ctl->full[st], bytes);
+    __syncwarp();
+    const int r0 = lane * per;
+    if (lane < kCopiesPerUnit && r0 < us.rows) {
       const uint32_t b = (uint32_t)((us.rows - r0 < per ? us.rows - r0 : per) * us.rec_bytes);
       bulk_g2s(ring + (size_t)st * stage_bytes + (size_t)r0 * us.rec_bytes, src + (size_t)r0 * us.rec_bytes, b,
                &ctl->full[st]);
     }
   }
   // drain: every stage's last copy has landed before the block may exit
-  const long long issued = k;
-  for (int st = 0; st < nstage && st < issued; ++st) {
-    const long long last = st + ((issued - 1 - st) / nstage) * nstage;
-    if (!mbar_wait_drain(&ctl->full[st], (uint32_t)(last / nstage) & 1u, a.timeout_ns)) {
-      atomicOr(a.err, kErrCopyTimeout);
-      ctl->abort = 1;
+  if (lane == 0) {
+    const long long issued = k;
+    for (int st = 0; st < nstage && st < issued; ++st) {
+      const long long last = st + ((issued - 1 - st) / nstage) * nstage;
+      if (!mbar_wait_drain(&ctl->full[st], (uint32_t)(last / nstage) & 1u, a.timeout_ns)) {
+        atomicOr(a.err, kErrCopyTimeout);
+        ctl->abort = 1;
+      }
     }
   }
+  __syncwarp();
 }
 
 // Work units of this block: a contiguous share of the units (item-major,
@@ -567,9 +578,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
   batch_init(ctl, geo.gu_nstage);
 
   if (warp == kBatchProducerWarp) {
-    if (lane == 0)
-      batch_produce(a, ctl, ring, geo.gu_nstage, geo.gu_stage_bytes, u0, u1, n_rb,
-                    UnitShape{0, a.lay.gu_row, geo.gu_rows});
+    batch_produce(a, ctl, ring, geo.gu_nstage, geo.gu_stage_bytes, u0, u1, n_rb,
+                  UnitShape{0, a.lay.gu_row, geo.gu_rows});
     return;
   }
   const RowAddr ra{(uint32_t)a.lay.gu_row, (uint32_t)a.lay.qh, (uint32_t)(2 * a.lay.qh), (uint32_t)a.lay.sh};
@@ -637,9 +647,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_down_kernel(BatchArgs 
   batch_init(ctl, geo.d_nstage);
 
   if (warp == kBatchProducerWarp) {
-    if (lane == 0)
-      batch_produce(a, ctl, ring, geo.d_nstage, geo.d_stage_bytes, u0, u1, n_rb,
-                    UnitShape{a.lay.d_off, a.lay.d_row, rows});
+    batch_produce(a, ctl, ring, geo.d_nstage, geo.d_stage_bytes, u0, u1, n_rb,
+                  UnitShape{a.lay.d_off, a.lay.d_row, rows});
     return;
   }
   const RowAddr ra{(uint32_t)(2 * a.lay.d_row), (uint32_t)a.lay.d_row, (uint32_t)a.lay.qi, (uint32_t)a.lay.d_row};
