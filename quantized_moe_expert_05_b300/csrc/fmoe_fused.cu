@@ -775,20 +775,25 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
 
 template <int BITS>
 static cudaError_t launch_fused_t(FusedParams& p, const FusedPlan& pl, cudaStream_t st) {
-  static int configured_smem = -1;
-  cudaError_t e;
-  if (configured_smem < (int)pl.smem) {
+  // the shared-memory limit and the residency check, once per device and size
+  // (function attributes belong to the device's context)
+  static int configured_smem[64];
+  static size_t checked_smem[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_smem[dev] < (int)pl.smem) {
     e = cudaFuncSetAttribute(fused_moe_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
-    configured_smem = (int)pl.smem;
+    configured_smem[dev] = (int)pl.smem;
   }
-  static size_t checked_smem = 0;
-  if (checked_smem != pl.smem) {
+  if (checked_smem[dev] != pl.smem) {
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_moe_kernel<BITS>, kFusedThreads, pl.smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    checked_smem = pl.smem;
+    checked_smem[dev] = pl.smem;
   }
   // cooperative: all blocks resident at once (every block waits for words
   // that the other blocks publish)
