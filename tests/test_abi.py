@@ -97,3 +97,34 @@ def test_workspace_bytes(fm):
     # h for T tokens x (K+1) slots x I floats fits
     assert b >= 16 * 5 * 1024 * 4
     assert fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 0, 4, 1) == 0
+
+
+def test_batched_workspace_holds_outputs_and_plan(fm):
+    L = fm.fmoe_layer()
+    L.bits, L.group, L.hidden, L.inter, L.n_experts, L.has_shared = 4, 64, 4096, 1024, 512, 1
+    b = fm.lib.fmoe_workspace_bytes(ctypes.byref(L), 16, 4, 1)
+    h = 16 * 5 * 1024 * 4           # h  [T][K+S][I]
+    y = 16 * 5 * 4096 * 4           # y  [T][K+S][H]
+    plan = (8 + 8 * (16 * 4 + 16)) * 4   # header + one item per (token, slot) at worst
+    assert b >= h + y + plan
+
+
+def test_new_entry_points_check_arguments(fm):
+    lib = fm.lib
+    L = fm.fmoe_layer()
+    L.bits, L.group, L.hidden, L.inter, L.n_experts, L.has_shared = 4, 64, 512, 128, 8, 0
+    L.experts = 4096 * 16
+    out = ctypes.c_void_p()
+    assert lib.fmoe_ws_batch_plan(None, ctypes.byref(L), 2, 2, ctypes.byref(out)) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_ws_batch_plan(256, ctypes.byref(L), 0, 2, ctypes.byref(out)) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_ws_batch_plan(256, ctypes.byref(L), 2, 2, None) == fm.ERR_INVALID_ARG
+    # a plan pointer inside the workspace, past its header
+    assert lib.fmoe_ws_batch_plan(4096, ctypes.byref(L), 2, 2, ctypes.byref(out)) == fm.OK
+    assert out.value > 4096 and out.value % 256 == 0
+    # expert_ffn: T out of range, misaligned ids
+    assert lib.fmoe_expert_ffn(ctypes.byref(L), 16, 17, 2, 16, 16, 256, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_expert_ffn(ctypes.byref(L), 2, 1, 2, 16, 16, 256, None) == fm.ERR_INVALID_ARG
+    # no-alloc block: K > E, null input, misaligned output
+    assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), 16, 16, 16, 32, 9, None, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), None, 16, 16, 32, 2, None, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), 16, 16, 16, 40, 2, None, None) == fm.ERR_INVALID_ARG
