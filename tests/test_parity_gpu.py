@@ -160,6 +160,36 @@ def test_zero_weight_invariance_on_gpu(fm):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_poisoned_outputs_and_scratch_are_fully_written(fm, T):
+    """Every output element and every scratch word a call reads is written by
+    the call: outputs and the whole workspace past its 256-byte header (error
+    word, exit count, launch count) start as NaN."""
+    shape = synth.BlockShape("tiny_shared_h512_e8_top2_i128_q4", 512, 128, 8, 2, True, 4, 0.002, 0.02, -0.1,
+                             0.0, seed=23)
+    layer = make_layer(fm, shape)
+    ws = fm.new_workspace(layer, 3, 2)
+    ws[256:].view(torch.float32).fill_(float("nan"))
+    inp = synth.block_inputs(shape, T, tag=90)
+    out = torch.full((T, shape.hidden), float("nan"), device="cuda")
+    fm.moe_block(layer, inp.x.cuda(), inp.logits.cuda(), inp.residual.cuda(), 2, ws, out=out)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    assert torch.isfinite(out).all()
+    ref = oracle_block(shape, 0, inp.x.numpy(), inp.logits.numpy(), inp.residual.numpy(), 2)
+    got = out.cpu().numpy()
+    for t in range(T):
+        assert_close(got[t], ref["out"][t], what=f"poisoned run, token {t}")
+
+    ws[256:].view(torch.float32).fill_(float("nan"))
+    ids = torch.tensor([[1, 5], [5, 1], [0, 7]][:T], dtype=torch.int32, device="cuda")
+    y = torch.full((T, 3, shape.hidden), float("nan"), device="cuda")
+    fm.expert_ffn(layer, ids, inp.x.cuda(), ws, y=y)
+    torch.cuda.synchronize()
+    assert fm.last_device_error(ws) == fm.OK
+    assert torch.isfinite(y).all()
+
+
 def test_out_aliases_residual(fm):
     shape = synth.TINY
     layer = make_layer(fm, shape)
