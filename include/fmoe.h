@@ -209,6 +209,29 @@ fmoe_status fmoe_ws_routing(void* ws, const fmoe_layer* layer /* host */, int T,
  */
 fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer /* host */, int T, int K, int32_t** plan);
 
+/*
+ * Test hook (host arithmetic only; no CUDA call): the launch geometry the
+ * library would use for a layer shape on a device with `sms` SMs and
+ * `smem_max` bytes of opt-in shared memory per block.  Writes FMOE_GEO_COUNT
+ * int64 values to `out` (indices below; byte counts and offsets of the
+ * persistent kernel's and the batched kernels' shared memory).  Returns
+ * FMOE_ERR_INVALID_ARG if out is null or n < FMOE_GEO_COUNT.
+ */
+enum {
+  FMOE_GEO_FUSED_OK, FMOE_GEO_FUSED_GRID, FMOE_GEO_FUSED_SMEM, FMOE_GEO_FUSED_CTRL_BYTES,
+  FMOE_GEO_FUSED_PART_OFF, FMOE_GEO_FUSED_STAGE_OFF, FMOE_GEO_FUSED_HS_OFF, FMOE_GEO_FUSED_HS_SLOT_BYTES,
+  FMOE_GEO_FUSED_DAREA_OFF, FMOE_GEO_FUSED_DSLOT_BYTES, FMOE_GEO_FUSED_RING_OFF, FMOE_GEO_FUSED_NSTAGE,
+  FMOE_GEO_FUSED_STAGE_BYTES, FMOE_GEO_FUSED_ROWS_PER_STAGE, FMOE_GEO_FUSED_NRMAX, FMOE_GEO_FUSED_NPARTS,
+  FMOE_GEO_FUSED_TAIL_ROWS,
+  FMOE_GEO_BATCH_GRID, FMOE_GEO_BATCH_G, FMOE_GEO_BATCH_GU_WARPS, FMOE_GEO_BATCH_GU_ROWS,
+  FMOE_GEO_BATCH_GU_NSTAGE, FMOE_GEO_BATCH_GU_STAGE_BYTES, FMOE_GEO_BATCH_GU_XS_BYTES, FMOE_GEO_BATCH_GU_SMEM,
+  FMOE_GEO_BATCH_D_ROWS, FMOE_GEO_BATCH_D_NSTAGE, FMOE_GEO_BATCH_D_STAGE_BYTES, FMOE_GEO_BATCH_D_XS_BYTES,
+  FMOE_GEO_BATCH_D_SMEM, FMOE_GEO_BATCH_CTRL_BYTES,
+  FMOE_GEO_COUNT
+};
+fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, int has_shared, int sms,
+                                       int smem_max, int64_t* out, int n);
+
 /* Static description of a status code (host). */
 const char* fmoe_status_string(fmoe_status s);
 

@@ -291,6 +291,48 @@ fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer, int T, int K, 
   return FMOE_OK;
 }
 
+fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, int has_shared, int sms,
+                                       int smem_max, int64_t* out, int n) {
+  if (out == nullptr || n < FMOE_GEO_COUNT) return FMOE_ERR_INVALID_ARG;
+  for (int i = 0; i < FMOE_GEO_COUNT; ++i) out[i] = 0;
+  if ((bits != 4 && bits != 2) || hidden <= 0 || inter <= 0 || hidden % kGroup || inter % kGroup)
+    return FMOE_OK;
+  const FusedPlan f = fused_plan_for(bits, hidden, inter, K, has_shared, sms, smem_max);
+  out[FMOE_GEO_FUSED_OK] = f.ok ? 1 : 0;
+  out[FMOE_GEO_FUSED_GRID] = f.grid;
+  out[FMOE_GEO_FUSED_SMEM] = (int64_t)f.smem;
+  out[FMOE_GEO_FUSED_CTRL_BYTES] = kCtrlBytes;
+  out[FMOE_GEO_FUSED_PART_OFF] = f.part_off;
+  out[FMOE_GEO_FUSED_STAGE_OFF] = f.stage_off;
+  out[FMOE_GEO_FUSED_HS_OFF] = f.hs_off;
+  out[FMOE_GEO_FUSED_HS_SLOT_BYTES] = f.hs_slot_bytes;
+  out[FMOE_GEO_FUSED_DAREA_OFF] = f.darea_off;
+  out[FMOE_GEO_FUSED_DSLOT_BYTES] = f.dslot_bytes;
+  out[FMOE_GEO_FUSED_RING_OFF] = f.ring_off;
+  out[FMOE_GEO_FUSED_NSTAGE] = f.nstage;
+  out[FMOE_GEO_FUSED_STAGE_BYTES] = f.stage_bytes;
+  out[FMOE_GEO_FUSED_ROWS_PER_STAGE] = f.rows_per_stage;
+  out[FMOE_GEO_FUSED_NRMAX] = f.nrmax;
+  out[FMOE_GEO_FUSED_NPARTS] = f.nparts;
+  out[FMOE_GEO_FUSED_TAIL_ROWS] = kMaxTailRows;
+  const BatchGeom g = batch_geometry_for(bits, hidden, inter, sms, smem_max);
+  out[FMOE_GEO_BATCH_GRID] = g.grid;
+  out[FMOE_GEO_BATCH_G] = g.G;
+  out[FMOE_GEO_BATCH_GU_WARPS] = g.gu_warps;
+  out[FMOE_GEO_BATCH_GU_ROWS] = g.gu_rows;
+  out[FMOE_GEO_BATCH_GU_NSTAGE] = g.gu_nstage;
+  out[FMOE_GEO_BATCH_GU_STAGE_BYTES] = g.gu_stage_bytes;
+  out[FMOE_GEO_BATCH_GU_XS_BYTES] = g.gu_xs_bytes;
+  out[FMOE_GEO_BATCH_GU_SMEM] = (int64_t)g.gu_smem;
+  out[FMOE_GEO_BATCH_D_ROWS] = kDownRowsPerWarp * kBatchConsumerWarps;
+  out[FMOE_GEO_BATCH_D_NSTAGE] = g.d_nstage;
+  out[FMOE_GEO_BATCH_D_STAGE_BYTES] = g.d_stage_bytes;
+  out[FMOE_GEO_BATCH_D_XS_BYTES] = g.d_xs_bytes;
+  out[FMOE_GEO_BATCH_D_SMEM] = (int64_t)g.d_smem;
+  out[FMOE_GEO_BATCH_CTRL_BYTES] = kBatchCtrlBytes;
+  return FMOE_OK;
+}
+
 const char* fmoe_status_string(fmoe_status s) {
   switch (s) {
     case FMOE_OK: return "ok";

@@ -459,7 +459,6 @@ struct BatchCtrl {
   int item[kItemWords];
   int abort;
 };
-constexpr int kBatchCtrlBytes = 256;
 static_assert(sizeof(BatchCtrl) <= kBatchCtrlBytes, "control area");
 
 // One work unit of an expert kernel: `rows` consecutive records of an
@@ -726,10 +725,18 @@ int batch_max_items(int T, int K, int S, int G) { return T * K + S * ((T + G - 1
 static size_t round_up128(size_t v) { return (v + 127) / 128 * 128; }
 
 BatchGeom batch_geometry(int bits, int H, int I, int device) {
-  BatchGeom g{};
   int sms = 0, smem_max = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return g;
-  if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return g;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+    cudaGetLastError();
+    return BatchGeom{};
+  }
+  return batch_geometry_for(bits, H, I, sms, smem_max);
+}
+
+BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max) {
+  BatchGeom g{};
+  if (sms < 1 || smem_max <= kBatchCtrlBytes) return g;
   const BlobLayout lay = blob_layout(bits, H, I);
   const size_t avail = (size_t)smem_max - kBatchCtrlBytes;
   const int d_rows = kDownRowsPerWarp * kBatchConsumerWarps;

@@ -724,15 +724,24 @@ static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 static int round_up_i(long long v, int a) { return (int)((v + a - 1) / a * a); }
 
 FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
+  int sms = 0, smem_max = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+    cudaGetLastError();
+    FusedPlan pl{};
+    pl.ok = false;
+    return pl;
+  }
+  return fused_plan_for(bits, H, I, K, S, sms, smem_max);
+}
+
+FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem_max) {
   FusedPlan pl{};
   pl.ok = false;
   const int tl = H / kSlice, tld = I / kSlice;
   if (H % kSlice || I % kSlice || !pow2(tl) || !pow2(tld)) return pl;
   if (tl < 4 || tl > 32 * kConsumerWarps || tld < 1) return pl;
-  if (K + S > kMaxSlots || K < 1) return pl;
-  int sms = 0, smem_max = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return pl;
-  if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return pl;
+  if (K + S > kMaxSlots || K < 1 || sms < 1) return pl;
   const int grid = sms;
   const int NS = K + S;
   const BlobLayout lay = blob_layout(bits, H, I);

@@ -49,6 +49,7 @@ constexpr int kBatchProducerWarp = kBatchConsumerWarps;
 constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 1);
 constexpr int kBatchMaxStages = 8;
 constexpr int kDownRowsPerWarp = 4;
+constexpr int kBatchCtrlBytes = 256;   // mbarriers, work range, item header at the start of shared memory
 
 // Largest number of plan items for T tokens, top-K, S shared experts, G
 // tokens per item.
@@ -56,6 +57,9 @@ int batch_max_items(int T, int K, int S, int G);
 // Geometry for a shape; grid == 0 if it does not fit (never for the shapes
 // the ABI accepts).
 BatchGeom batch_geometry(int bits, int H, int I, int device);
+// The same for a device with `sms` SMs and `smem_max` bytes of shared memory
+// per block (host arithmetic only).
+BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max);
 
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights,
                          const uint16_t* wsg, const float* x, int H, float* gate, cudaStream_t st);
@@ -183,6 +187,9 @@ struct FusedParams {
 // Plan the persistent launch for a shape; ok == false if the shape does not
 // fit the kernel's limits (the caller then uses the general kernels).
 FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device);
+// The same for a device with `sms` SMs and `smem_max` bytes of shared memory
+// per block (host arithmetic only).
+FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem_max);
 cudaError_t launch_fused(FusedParams& p, const FusedPlan& plan, cudaStream_t st);
 
 cudaError_t launch_wait_test(uint32_t* counter, uint32_t* err, int n_blocks, int expected,
