@@ -50,3 +50,22 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     ns = type("A", (), {"workload": "tiny", "chain": 1, "steps": 1, "warmup": 0, "gpus": 2})()
     assert bench.run_reference(ns) == 0
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference times the oracle on the host and prints one
+    JSON line with the reference arm's keys (tiny workload: a few seconds)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "RANK": "0"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["higher_is_better"] is True and line["steps"] == 2 and line["warmup"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"]
