@@ -294,15 +294,17 @@ def run_reference(args):
         return oracle.part_rows(blob, bits, H, I, name, n)
 
     def one(i, frac):
-        # the first frac of the rows of one expert's gate, up and down matrices
+        # the first frac of the intermediate columns of one expert: their gate
+        # and up rows and their down columns (a multiple of 64 columns)
         blob = blobs[i % len(blobs)]
-        ni, nh = max(1, int(I * frac)), max(1, int(H * frac))
+        ni = max(64, int(I * frac) // 64 * 64)
         wg = oracle.dequantize(rows(blob, "gate_q", ni), rows(blob, "gate_sb", ni), bits)
         wu = oracle.dequantize(rows(blob, "up_q", ni), rows(blob, "up_sb", ni), bits)
         h = oracle.silu(wg @ x) * (wu @ x)
-        wd = oracle.dequantize(rows(blob, "down_q", nh), rows(blob, "down_sb", nh), bits)
-        wd[:, :ni] @ h
-        return (2 * ni * (H * bits // 8 + H // 16) + nh * (I * bits // 8 + I // 16))
+        wd = oracle.dequantize_codes(oracle.unpack_codes(rows(blob, "down_q", ni), bits).T,
+                                     rows(blob, "down_sb", ni // 64).T)
+        wd @ h
+        return ni * (2 * (H * bits // 8 + H // 16) + H * bits // 8 + H // 16)
 
     # size the per-step sample so that warm-up + steps take about 90 s
     t0 = time.perf_counter()
@@ -318,7 +320,7 @@ def run_reference(args):
     el = time.perf_counter() - t0
     dt = el / max(args.steps, 1)
     gbs = nbytes / el / 1e9
-    desc = (f"per step the first {frac:.3f} of the rows of one active expert of a {shape.name} block "
+    desc = (f"per step the first {frac:.3f} of the intermediate columns of one active expert of a {shape.name} block "
             f"(dequantise + fp64 gate/up/down matvecs + SwiGLU, numpy/OpenBLAS), cycling over the "
             f"block's {len(blobs)} experts; value = packed bytes processed per second")
     line = {

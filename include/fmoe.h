@@ -29,7 +29,11 @@
  *   - fp32 activations are read and written as IEEE binary32.  Router logits
  *     must be finite (NaN/inf logits give unspecified ids).  Activations must
  *     stay below 2^40 in magnitude (the dot products pre-scale x by powers of
- *     two; larger values overflow to inf).
+ *     two; larger values overflow to inf).  The single-launch kernel (T = 1)
+ *     adds the partial outputs of its blocks in fixed point with 2^-28
+ *     resolution: a block's share of an output element beyond 2^19 in
+ *     magnitude is clamped and reported (FMOE_ERR_RANGE from
+ *     fmoe_last_device_error).
  *
  * Packed expert blob (one per expert, contiguous, 256-byte aligned):
  *   gate/up records, r = 0..I-1, each padded to a multiple of 16 bytes:
@@ -39,13 +43,18 @@
  *     up_q    [H*bits/32] uint32   codes of up row r
  *     gate_sb [H/64]      uint32   bits 0..15 scale (bf16), 16..31 bias (bf16)
  *     up_sb   [H/64]      uint32
- *   down records, j = 0..H-1, from the next 256-byte boundary, each padded
- *   to a multiple of 16 bytes:
- *     down_q  [I*bits/32] uint32
- *     down_sb [I/64]      uint32
- *   The dequantised weight of row r, column c is q * scale[r][c/64] +
- *   bias[r][c/64]; gate/up rows have H columns, down rows have I columns.
- *   A range of rows of a matrix, with its scales, is one contiguous byte
+ *   the down projection by column, i = 0..I-1, from the next 256-byte
+ *   boundary, H*bits/8 bytes each:
+ *     down_q  [H*bits/32] uint32   codes of column i; row j at bits
+ *                                  (j mod 32/bits)*bits of word j/(32/bits)
+ *   its scale/bias words by group of 64 columns, g = 0..I/64-1, from the
+ *   next 256-byte boundary, H words each:
+ *     down_sb [H]         uint32   word j: row j's scale and bias for
+ *                                  columns 64g .. 64g+63
+ *   The dequantised weight of row r, column c of a matrix is q * scale[r][c/64]
+ *   + bias[r][c/64]; gate/up rows have H columns, the down projection has H
+ *   rows and I columns.  A range of gate/up rows (with their scales), a range
+ *   of down columns and a range of down groups are each one contiguous byte
  *   range.  Blob size: fmoe_expert_bytes() (a multiple of 256); the routed
  *   experts of a layer sit at stride fmoe_expert_bytes() from `experts`.
  */
@@ -64,7 +73,8 @@ typedef enum {
   FMOE_ERR_INVALID_ARG = 1,
   FMOE_ERR_UNSUPPORTED = 2,
   FMOE_ERR_CUDA = 3,
-  FMOE_ERR_TIMEOUT = 4
+  FMOE_ERR_TIMEOUT = 4,
+  FMOE_ERR_RANGE = 5
 } fmoe_status;
 
 /* Largest sizes this build accepts. */
@@ -105,11 +115,14 @@ size_t fmoe_expert_bytes(int bits, int hidden, int inter, int group);
 /*
  * Bytes of workspace a call needs for `layer`, T tokens, K routed experts and
  * L stacked layers (L = 1 for the single-block calls).  The workspace holds
- * intermediate activations, routing results, the batch plan, the words the
- * persistent kernel's blocks exchange (tagged with a launch count kept in the
- * workspace) and the device error word.  It must be 256-byte aligned and zeroed once before its
- * first use (fmoe_workspace_init); afterwards the library keeps it
- * consistent.  Calls that share a workspace must not overlap in time.
+ * intermediate activations, routing results, the batch plan, the device
+ * error word and, in its first 256 + 24*H bytes (rounded up to a multiple of
+ * 256), state that the single-launch kernel keeps between calls: a layer
+ * count and three fixed-point accumulators of H 64-bit words through which
+ * its blocks add up their partial outputs.  The workspace must be 256-byte
+ * aligned and zeroed once before its first use (fmoe_workspace_init);
+ * afterwards the library keeps it consistent.  Calls that share a workspace
+ * must not overlap in time.
  */
 size_t fmoe_workspace_bytes(const fmoe_layer* layer /* host */, int T, int K, int L);
 
@@ -154,10 +167,10 @@ fmoe_status fmoe_expert_ffn(const fmoe_layer* layer /* host */, const int32_t* i
  * (the sigmoid term only if layer->has_shared).
  *   x, residual, out  fp32 [T][H];  router_logits fp32 [T][E]
  *   out may alias residual; it must not overlap x or router_logits.
- * T = 1 runs as one persistent launch when the shape fits it; otherwise
- * (and for every T > 1) four launches: plan, gate/up, down, combine, in
- * which each distinct expert among the T*K picks is read once (see
- * fmoe_ws_batch_plan).  The routing result is left in the workspace (see
+ * T = 1 runs as one persistent launch when the shape fits it (H/32 a power
+ * of two, H >= 128); otherwise (and for every T > 1) four launches: plan,
+ * gate/up, down, combine, in which each distinct expert among the T*K picks
+ * is read once (see fmoe_ws_batch_plan).  The routing result is left in the workspace (see
  * fmoe_ws_routing).
  */
 fmoe_status fmoe_moe_block(const fmoe_layer* layer /* host */, const float* x,
@@ -179,7 +192,10 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer /* host */, const float* x,
  * No layer's routed experts are read before the previous layer's output is
  * complete (their ids depend on it); a layer's shared expert, whose identity
  * is fixed, may be requested as soon as the reading block has finished its
- * share of the previous layer.
+ * share of the previous layer.  Shapes the single-launch kernel takes run as
+ * one launch per 64 layers; other shapes run per layer as an RMSNorm launch
+ * followed by the batched block.  The routing result of layer l is left at
+ * row l of the workspace's ids/weights/gate (fmoe_ws_routing with T = L).
  */
 fmoe_status fmoe_stack_decode(const fmoe_layer* layers /* host */, int L,
                               const float* logits, float* h, int K, float eps,
@@ -219,26 +235,39 @@ fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer /* host */, int
  */
 enum {
   FMOE_GEO_FUSED_OK, FMOE_GEO_FUSED_GRID, FMOE_GEO_FUSED_SMEM, FMOE_GEO_FUSED_CTRL_BYTES,
-  FMOE_GEO_FUSED_PART_OFF, FMOE_GEO_FUSED_STAGE_OFF, FMOE_GEO_FUSED_HS_OFF, FMOE_GEO_FUSED_HS_SLOT_BYTES,
-  FMOE_GEO_FUSED_DAREA_OFF, FMOE_GEO_FUSED_DSLOT_BYTES, FMOE_GEO_FUSED_RING_OFF, FMOE_GEO_FUSED_NSTAGE,
-  FMOE_GEO_FUSED_STAGE_BYTES, FMOE_GEO_FUSED_ROWS_PER_STAGE, FMOE_GEO_FUSED_NRMAX, FMOE_GEO_FUSED_NPARTS,
-  FMOE_GEO_FUSED_TAIL_ROWS,
+  FMOE_GEO_FUSED_XS_OFF, FMOE_GEO_FUSED_PART_OFF, FMOE_GEO_FUSED_HBUF_OFF, FMOE_GEO_FUSED_HBUF_STRIDE,
+  FMOE_GEO_FUSED_DAREA_OFF, FMOE_GEO_FUSED_DAREA_BYTES, FMOE_GEO_FUSED_RING_OFF, FMOE_GEO_FUSED_NSTAGE,
+  FMOE_GEO_FUSED_STAGE_BYTES, FMOE_GEO_FUSED_ROWS_PER_STAGE, FMOE_GEO_FUSED_NPARTS, FMOE_GEO_FUSED_LEN_MAX,
   FMOE_GEO_BATCH_GRID, FMOE_GEO_BATCH_G, FMOE_GEO_BATCH_GU_WARPS, FMOE_GEO_BATCH_GU_ROWS,
   FMOE_GEO_BATCH_GU_NSTAGE, FMOE_GEO_BATCH_GU_STAGE_BYTES, FMOE_GEO_BATCH_GU_XS_BYTES, FMOE_GEO_BATCH_GU_SMEM,
-  FMOE_GEO_BATCH_D_ROWS, FMOE_GEO_BATCH_D_NSTAGE, FMOE_GEO_BATCH_D_STAGE_BYTES, FMOE_GEO_BATCH_D_XS_BYTES,
-  FMOE_GEO_BATCH_D_SMEM, FMOE_GEO_BATCH_CTRL_BYTES,
+  FMOE_GEO_BATCH_D_ROWS, FMOE_GEO_BATCH_D_H_BYTES, FMOE_GEO_BATCH_D_SMEM, FMOE_GEO_BATCH_CTRL_BYTES,
   FMOE_GEO_COUNT
 };
 fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, int has_shared, int sms,
                                        int smem_max, int64_t* out, int n);
+
+/*
+ * Test hook (host arithmetic only; no CUDA call): the intermediate columns
+ * that block `block` of `sms` owns in the single-launch kernel, as pieces of
+ * one slot each.  Writes out[0] = the number of pieces and, for piece q,
+ * out[1+8q .. 8+8q] = slot (0 = the shared expert when has_shared), first
+ * column, column count, first local index, byte offsets of its codes and of
+ * its (scale,bias) words in the block's down area, first 64-column group,
+ * group count.  n must be at least 33.  FMOE_ERR_INVALID_ARG for a bad shape
+ * or block.
+ */
+fmoe_status fmoe_debug_block_pieces(int bits, int hidden, int inter, int K, int has_shared, int sms,
+                                    int block, int64_t* out, int n);
 
 /* Static description of a status code (host). */
 const char* fmoe_status_string(fmoe_status s);
 
 /*
  * Synchronise `stream`, then read and clear the workspace's device error
- * word: FMOE_OK, or FMOE_ERR_TIMEOUT if a device-side wait gave up since the
- * last call.  After a timeout the workspace must be re-initialised with
+ * word: FMOE_OK; FMOE_ERR_TIMEOUT if a device-side wait gave up since the
+ * last call; FMOE_ERR_INVALID_ARG if fmoe_expert_ffn met an expert id
+ * outside [0, E); FMOE_ERR_RANGE if a partial sum left the fixed-point
+ * range.  After a timeout the workspace must be re-initialised with
  * fmoe_workspace_init before reuse.
  */
 fmoe_status fmoe_last_device_error(void* ws, void* stream);
@@ -258,7 +287,7 @@ fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected,
  * Every GPU that loads the library holds this much device memory for it
  * until the process exits.
  */
-#define FMOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+#define FMOE_NOALLOC_SCRATCH_BYTES (128u * 1024u)
 
 /*
  * fmoe_moe_block for one token (T = 1) without a caller workspace.
@@ -279,17 +308,19 @@ fmoe_status fmoe_debug_wait_test(void* ws, int n_blocks, int expected,
  *                 valid).  Written asynchronously on `stream`.
  *
  * Returns FMOE_ERR_INVALID_ARG (and enqueues nothing) for the argument
- * errors of fmoe_moe_block and when the shape's scratch
- * (fmoe_workspace_bytes(layer, 1, K, 1)) exceeds FMOE_NOALLOC_SCRATCH_BYTES;
- * FMOE_ERR_UNSUPPORTED for shapes the single-launch kernel does not cover;
- * FMOE_ERR_CUDA if the set-up or a launch fails.
+ * errors of fmoe_moe_block and when the kernel's scratch (256 + 24*H bytes,
+ * rounded up to 256: 98,560 bytes at H = 4096, so H up to 5,440) exceeds
+ * FMOE_NOALLOC_SCRATCH_BYTES; FMOE_ERR_UNSUPPORTED for shapes the
+ * single-launch kernel does not cover; FMOE_ERR_CUDA if the set-up or a
+ * launch fails.
  *
- * The first call on a device looks up the array's device address on that
- * device (the device current at the call); make that first call before any
- * stream capture.  Every call on a device uses the same array, and each call
- * clears its error word and exit count first: calls that overlap on the GPU
- * (other streams, or other host threads) race on it and must be serialised
- * by the caller.  The routing result is not kept.
+ * Each call asks the runtime for the array's device address on the current
+ * device (cudaGetSymbolAddress); the first call on a device loads the
+ * library's device code there, so make that first call before any stream
+ * capture.  Every call on a device uses the same array and clears it (its
+ * error word, counters and accumulators) before its launch: calls that
+ * overlap on the GPU (other streams, or other host threads) race on it and
+ * must be serialised by the caller.  The routing result is not kept.
  */
 fmoe_status fmoe_moe_block_noalloc(const fmoe_layer* layer /* host */, const float* x,
                                    const float* router_logits, const float* residual,

@@ -10,6 +10,9 @@ What is computed (all in fp64; fp32 and bf16 inputs are widened exactly):
 
 * unpack      element c of a packed row is bits [(c mod m)*bits, +bits) of
               word floor(c/m), m = 32/bits (lowest bits first)
+* layout      gate/up rows as records; the down projection by column, its
+              (scale,bias) words by group of 64 columns (this project's byte
+              order; the pages fix only one contiguous blob per expert)
 * dequantise  W[r, c] = q[r, c] * s[r, c//64] + b[r, c//64]
               ("nibble * scale + bias", flash-moe write-up on discuss.pytorch.kr,
               section "FMA-optimised dequant kernel")
@@ -37,6 +40,7 @@ from .moe import (  # noqa: F401
     unpack_codes,
     bf16_to_f64,
     dequantize,
+    dequantize_codes,
     expert_weights,
     silu,
     sigmoid,

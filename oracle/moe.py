@@ -16,7 +16,7 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 64          # quantisation group: 64 consecutive input columns of a row
-_ALIGN = 256        # the down records and the blob size are aligned to 256 bytes
+_ALIGN = 256        # the down parts and the blob size are aligned to 256 bytes
 
 
 # ---------------------------------------------------------------------------
@@ -27,31 +27,36 @@ def layout(bits: int, hidden: int, inter: int) -> tuple:
 
     Gate/up row r (r < I) is one record of gate codes, up codes, gate
     (scale,bias) words and up (scale,bias) words, padded to a multiple of 16
-    bytes; the H down rows follow from the next 256-byte boundary, each a
-    record of down codes then down (scale,bias) words, padded to 16 bytes; the
-    blob is padded to a multiple of 256 bytes.  Returns
+    bytes.  The down projection follows from the next 256-byte boundary,
+    stored by column: column i (i < I) is H*bits/8 bytes whose word w holds
+    the codes of rows w*(32/bits) .. (w+1)*(32/bits)-1 of that column.  Its
+    (scale,bias) words follow from the next 256-byte boundary, by group:
+    group g (columns 64g .. 64g+63) is H words, word j for row j.  The blob
+    is padded to a multiple of 256 bytes.  Returns
     (dict name -> (offset of row 0, row stride, rows, 32-bit words per row),
-    blob_bytes), all in bytes except the word count.
+    blob_bytes), all in bytes except the word count; for the two down parts
+    a "row" is a column (down_q) or a group (down_sb).
     Pinned by the expert-size pin (6.75 MiB per 4-bit expert of the
-    397B model, [FM] "SSD expert streaming").
+    397B model, [FM] "SSD expert streaming") and by blobs built field by
+    field from chosen codes.
     """
     if bits not in (2, 4):
         raise ValueError("bits must be 2 or 4")
     per_word = 32 // bits
     qh, sh = hidden // per_word * 4, hidden // GROUP * 4       # bytes of one gate/up row's parts
-    qi, si = inter // per_word * 4, inter // GROUP * 4         # bytes of one down row's parts
     gu_stride = -(-(2 * qh + 2 * sh) // 16) * 16
-    d_stride = -(-(qi + si) // 16) * 16
-    d_base = -(-(inter * gu_stride) // _ALIGN) * _ALIGN
+    dq_base = -(-(inter * gu_stride) // _ALIGN) * _ALIGN
+    dcol = hidden // per_word * 4                              # bytes of one down column
+    dsb_base = -(-(dq_base + inter * dcol) // _ALIGN) * _ALIGN
     out = {
         "gate_q": (0, gu_stride, inter, qh // 4),
         "up_q": (qh, gu_stride, inter, qh // 4),
         "gate_sb": (2 * qh, gu_stride, inter, sh // 4),
         "up_sb": (2 * qh + sh, gu_stride, inter, sh // 4),
-        "down_q": (d_base, d_stride, hidden, qi // 4),
-        "down_sb": (d_base + qi, d_stride, hidden, si // 4),
+        "down_q": (dq_base, dcol, inter, hidden // per_word),
+        "down_sb": (dsb_base, hidden * 4, inter // GROUP, hidden),
     }
-    return out, -(-(d_base + hidden * d_stride) // _ALIGN) * _ALIGN
+    return out, -(-(dsb_base + inter // GROUP * hidden * 4) // _ALIGN) * _ALIGN
 
 
 def unpack_codes(words: np.ndarray, bits: int) -> np.ndarray:
@@ -76,13 +81,19 @@ def bf16_to_f64(b16: np.ndarray) -> np.ndarray:
 
 
 def dequantize(q_words: np.ndarray, sb_words: np.ndarray, bits: int) -> np.ndarray:
-    """W[r, c] = q[r, c] * s[r, c//64] + b[r, c//64] in fp64.
+    """W[r, c] = q[r, c] * s[r, c//64] + b[r, c//64] in fp64, from packed rows.
 
     [FM] "FMA-optimised dequant kernel": the weight is nibble*scale+bias.
     sb word g of a row holds scale (low 16 bits, bf16) and bias (high 16).
     Pinned by hand-worked dequant examples and the FMA identity.
     """
-    q = unpack_codes(q_words, bits).astype(np.float64)
+    return dequantize_codes(unpack_codes(q_words, bits), sb_words)
+
+
+def dequantize_codes(q: np.ndarray, sb_words: np.ndarray) -> np.ndarray:
+    """W[r, c] = q[r, c] * s[r, c//64] + b[r, c//64] from integer codes q [rows][n]
+    and (scale,bias) words [rows][n/64]."""
+    q = np.asarray(q).astype(np.float64)
     sb = np.asarray(sb_words, dtype=np.uint32)
     s = bf16_to_f64(sb & 0xFFFF)
     b = bf16_to_f64(sb >> 16)
@@ -105,14 +116,19 @@ def part_rows(blob: np.ndarray, bits: int, hidden: int, inter: int, name: str, n
 
 
 def expert_weights(blob: np.ndarray, bits: int, hidden: int, inter: int) -> tuple:
-    """(Wg [I][H], Wu [I][H], Wd [H][I]) dequantised from one blob (fp64)."""
+    """(Wg [I][H], Wu [I][H], Wd [H][I]) dequantised from one blob (fp64).
+
+    The down codes are stored by column and its (scale,bias) words by group
+    (see layout); both are turned to row-major [H][...] before the same
+    dequantisation as the gate and up rows.
+    """
 
     def plane(name):
         return part_rows(blob, bits, hidden, inter, name)
 
     wg = dequantize(plane("gate_q"), plane("gate_sb"), bits)
     wu = dequantize(plane("up_q"), plane("up_sb"), bits)
-    wd = dequantize(plane("down_q"), plane("down_sb"), bits)
+    wd = dequantize_codes(unpack_codes(plane("down_q"), bits).T, plane("down_sb").T)
     return wg, wu, wd
 
 

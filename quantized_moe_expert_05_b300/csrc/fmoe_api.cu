@@ -11,7 +11,7 @@ namespace {
 
 constexpr unsigned long long kTimeoutNs = 200ull * 1000 * 1000;   // 200 ms per device-side wait
 
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool aligned(const void* p, size_t a) { return host_aligned(p, a); }
 
 fmoe_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return FMOE_OK;
@@ -19,40 +19,19 @@ fmoe_status from_cuda(cudaError_t e) {
   return FMOE_ERR_CUDA;
 }
 
-// Shape checks common to every call that reads expert blobs.
-fmoe_status check_layer(const fmoe_layer* L, bool need_ptrs) {
-  if (L == nullptr) return FMOE_ERR_INVALID_ARG;
-  if (L->bits != 4 && L->bits != 2) return FMOE_ERR_UNSUPPORTED;
-  if (L->group != kGroup) return FMOE_ERR_UNSUPPORTED;
-  if (L->hidden <= 0 || L->inter <= 0 || L->hidden % kGroup || L->inter % kGroup) return FMOE_ERR_INVALID_ARG;
-  if (L->hidden > FMOE_MAX_HIDDEN || L->inter > FMOE_MAX_INTER) return FMOE_ERR_UNSUPPORTED;
-  if (L->n_experts <= 0 || L->n_experts > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
-  if (L->has_shared != 0 && L->has_shared != 1) return FMOE_ERR_INVALID_ARG;
-  if (need_ptrs) {
-    if (L->experts == nullptr || !aligned(L->experts, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
-    if (L->has_shared) {
-      if (L->shared == nullptr || !aligned(L->shared, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
-      if (L->shared_gate_w == nullptr || !aligned(L->shared_gate_w, 16)) return FMOE_ERR_INVALID_ARG;
-    }
-  }
-  return FMOE_OK;
-}
-
-bool vec_ok(const void* p) { return p != nullptr && aligned(p, 16); }
-
 struct Ws {
   WsLayout lay;
   uint8_t* base;
   uint32_t* err() const { return reinterpret_cast<uint32_t*>(base + lay.err); }
   uint32_t* exit_ctr() const { return reinterpret_cast<uint32_t*>(base + lay.exit_ctr); }
-  uint32_t* epoch() const { return reinterpret_cast<uint32_t*>(base + lay.epoch); }
-  unsigned long long* hll() const { return reinterpret_cast<unsigned long long*>(base + lay.hll); }
-  unsigned long long* hbufll() const { return reinterpret_cast<unsigned long long*>(base + lay.hbufll); }
+  uint32_t* lbase() const { return reinterpret_cast<uint32_t*>(base + lay.lbase); }
+  unsigned long long* acc() const { return reinterpret_cast<unsigned long long*>(base + lay.acc); }
   int32_t* ids() const { return reinterpret_cast<int32_t*>(base + lay.ids); }
   float* weights() const { return reinterpret_cast<float*>(base + lay.weights); }
   float* gate() const { return reinterpret_cast<float*>(base + lay.gate); }
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
   float* y() const { return reinterpret_cast<float*>(base + lay.y); }
+  float* xn() const { return reinterpret_cast<float*>(base + lay.xn); }
   int32_t* plan() const { return reinterpret_cast<int32_t*>(base + lay.plan); }
 };
 
@@ -87,6 +66,16 @@ BatchArgs batch_args(const fmoe_layer* L, int T, int K, const Ws& w) {
   return a;
 }
 
+// The workspace fields of the persistent kernel.
+void fused_ws(FusedParams& p, const Ws& w) {
+  p.hmid = w.h();
+  p.acc = w.acc();
+  p.lbase = w.lbase();
+  p.exit_ctr = w.exit_ctr();
+  p.err = w.err();
+  p.timeout_ns = kTimeoutNs;
+}
+
 int current_device() {
   int d = 0;
   cudaGetDevice(&d);
@@ -115,7 +104,7 @@ fmoe_status fmoe_workspace_init(void* ws, size_t bytes, void* stream) {
 }
 
 fmoe_status fmoe_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, void* stream) {
-  if (!vec_ok(logits) || ids == nullptr || weights == nullptr) return FMOE_ERR_INVALID_ARG;
+  if (!host_vec_ok(logits) || ids == nullptr || weights == nullptr) return FMOE_ERR_INVALID_ARG;
   if (!aligned(ids, 4) || !aligned(weights, 4)) return FMOE_ERR_INVALID_ARG;
   if (T < 1 || T > FMOE_MAX_TOKENS || E < 1 || E > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
   if (K < 1 || K > E || K > FMOE_MAX_TOPK) return FMOE_ERR_INVALID_ARG;
@@ -129,7 +118,7 @@ fmoe_status fmoe_expert_ffn(const fmoe_layer* layer, const int32_t* ids, int T, 
   if (s != FMOE_OK) return s;
   if (T < 1 || T > FMOE_MAX_TOKENS || K < 1 || K > FMOE_MAX_TOPK || K > layer->n_experts)
     return FMOE_ERR_INVALID_ARG;
-  if (ids == nullptr || !aligned(ids, 4) || !vec_ok(x) || !vec_ok(y) || ws == nullptr || !aligned(ws, 256))
+  if (ids == nullptr || !aligned(ids, 4) || !host_vec_ok(x) || !host_vec_ok(y) || ws == nullptr || !aligned(ws, 256))
     return FMOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ws w = carve(ws, layer, T, K, 1);
@@ -146,20 +135,9 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float*
   if (s != FMOE_OK) return s;
   if (T < 1 || T > FMOE_MAX_TOKENS || K < 1 || K > FMOE_MAX_TOPK || K > layer->n_experts)
     return FMOE_ERR_INVALID_ARG;
-  if (!vec_ok(x) || !vec_ok(router_logits) || !vec_ok(residual) || !vec_ok(out) || ws == nullptr ||
-      !aligned(ws, 256))
-    return FMOE_ERR_INVALID_ARG;
-  const size_t H = layer->hidden;
-  // out may alias residual but must not overlap x or the logits
-  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
-    const char* pa = static_cast<const char*>(a);
-    const char* pb = static_cast<const char*>(b);
-    return pa < pb + nb && pb < pa + na;
-  };
-  if (overlap(out, T * H * 4, x, T * H * 4) ||
-      overlap(out, T * H * 4, router_logits, (size_t)T * layer->n_experts * 4))
-    return FMOE_ERR_INVALID_ARG;
-  if (out != residual && overlap(out, T * H * 4, residual, T * H * 4)) return FMOE_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
+  s = check_block_args(layer, x, router_logits, residual, out, T);
+  if (s != FMOE_OK) return s;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ws w = carve(ws, layer, T, K, 1);
@@ -169,34 +147,17 @@ fmoe_status fmoe_moe_block(const fmoe_layer* layer, const float* x, const float*
     FusedPlan pl = fused_plan(layer->bits, layer->hidden, layer->inter, K, S, current_device());
     if (pl.ok) {
       FusedParams p{};
-      p.bits = layer->bits;
-      p.H = layer->hidden;
-      p.I = layer->inter;
-      p.E = layer->n_experts;
-      p.K = K;
-      p.S = S;
-      p.L = 1;
+      fused_params_for(p, layer, 1, K);
+      fused_ws(p, w);
       p.norm = 0;
       p.eps = 0.f;
-      p.lay = blob_layout(layer->bits, layer->hidden, layer->inter);
-      p.blob = p.lay.bytes;
       p.x = x;
       p.residual = residual;
       p.out = out;
       p.logits = router_logits;
-      p.hmid = w.h();
-      p.hll = w.hll();
-      p.hbufll = w.hbufll();
       p.ids_out = w.ids();
       p.w_out = w.weights();
       p.gate_out = w.gate();
-      p.exit_ctr = w.exit_ctr();
-      p.epoch = w.epoch();
-      p.err = w.err();
-      p.timeout_ns = kTimeoutNs;
-      p.layer[0].experts = static_cast<const uint8_t*>(layer->experts);
-      p.layer[0].shared = static_cast<const uint8_t*>(layer->shared);
-      p.layer[0].wsg = layer->shared_gate_w;
       return from_cuda(launch_fused(p, pl, st));
     }
   }
@@ -225,48 +186,48 @@ fmoe_status fmoe_stack_decode(const fmoe_layer* layers, int L, const float* logi
       return FMOE_ERR_INVALID_ARG;
   }
   if (K < 1 || K > FMOE_MAX_TOPK || K > layers[0].n_experts) return FMOE_ERR_INVALID_ARG;
-  if (!vec_ok(logits) || !vec_ok(h) || ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
+  if (!host_vec_ok(logits) || !host_vec_ok(h) || ws == nullptr || !aligned(ws, 256)) return FMOE_ERR_INVALID_ARG;
   if (!(eps >= 0.f)) return FMOE_ERR_INVALID_ARG;
   const fmoe_layer& L0 = layers[0];
   const int S = L0.has_shared;
-  FusedPlan pl = fused_plan(L0.bits, L0.hidden, L0.inter, K, S, current_device());
-  if (!pl.ok) return FMOE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Ws w = carve(ws, &L0, 1, K, L);
-  for (int l0 = 0; l0 < L; l0 += kMaxFusedLayers) {
-    const int n = (L - l0) < kMaxFusedLayers ? (L - l0) : kMaxFusedLayers;
-    FusedParams p{};
-    p.bits = L0.bits;
-    p.H = L0.hidden;
-    p.I = L0.inter;
-    p.E = L0.n_experts;
-    p.K = K;
-    p.S = S;
-    p.L = n;
-    p.norm = 1;
-    p.eps = eps;
-    p.lay = blob_layout(L0.bits, L0.hidden, L0.inter);
-    p.blob = p.lay.bytes;
-    p.x = nullptr;
-    p.residual = nullptr;
-    p.out = h;
-    p.logits = logits + (size_t)l0 * L0.n_experts;
-    p.hmid = w.h();
-    p.hll = w.hll();
-    p.hbufll = w.hbufll();
-    p.ids_out = w.ids() + (size_t)l0 * K;
-    p.w_out = w.weights() + (size_t)l0 * K;
-    p.gate_out = w.gate() + l0;
-    p.exit_ctr = w.exit_ctr();
-    p.epoch = w.epoch();
-    p.err = w.err();
-    p.timeout_ns = kTimeoutNs;
-    for (int i = 0; i < n; ++i) {
-      p.layer[i].experts = static_cast<const uint8_t*>(layers[l0 + i].experts);
-      p.layer[i].shared = static_cast<const uint8_t*>(layers[l0 + i].shared);
-      p.layer[i].wsg = layers[l0 + i].shared_gate_w;
+  FusedPlan pl = fused_plan(L0.bits, L0.hidden, L0.inter, K, S, current_device());
+  if (pl.ok) {
+    for (int l0 = 0; l0 < L; l0 += kMaxFusedLayers) {
+      const int n = (L - l0) < kMaxFusedLayers ? (L - l0) : kMaxFusedLayers;
+      FusedParams p{};
+      fused_params_for(p, layers + l0, n, K);
+      fused_ws(p, w);
+      p.norm = 1;
+      p.eps = eps;
+      p.x = nullptr;
+      p.residual = nullptr;
+      p.out = h;
+      p.logits = logits + (size_t)l0 * L0.n_experts;
+      p.ids_out = w.ids() + (size_t)l0 * K;
+      p.w_out = w.weights() + (size_t)l0 * K;
+      p.gate_out = w.gate() + l0;
+      cudaError_t e = launch_fused(p, pl, st);
+      if (e != cudaSuccess) return from_cuda(e);
     }
-    cudaError_t e = launch_fused(p, pl, st);
+    return FMOE_OK;
+  }
+  // general path (shapes the persistent kernel does not take): per layer an
+  // RMSNorm launch, then the batched block with residual and output h
+  for (int l = 0; l < L; ++l) {
+    cudaError_t e = launch_rmsnorm(h, w.xn(), L0.hidden, eps, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    BatchArgs a = batch_args(&layers[l], 1, K, w);
+    a.logits = logits + (size_t)l * L0.n_experts;
+    a.wsg = S ? layers[l].shared_gate_w : nullptr;
+    a.ids = w.ids() + (size_t)l * K;
+    a.weights = w.weights() + (size_t)l * K;
+    a.gate = w.gate() + l;
+    a.x = w.xn();
+    a.residual = h;
+    a.out = h;
+    e = launch_batch(a, a.y, st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return FMOE_OK;
@@ -302,19 +263,18 @@ fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, i
   out[FMOE_GEO_FUSED_GRID] = f.grid;
   out[FMOE_GEO_FUSED_SMEM] = (int64_t)f.smem;
   out[FMOE_GEO_FUSED_CTRL_BYTES] = kCtrlBytes;
+  out[FMOE_GEO_FUSED_XS_OFF] = f.xs_off;
   out[FMOE_GEO_FUSED_PART_OFF] = f.part_off;
-  out[FMOE_GEO_FUSED_STAGE_OFF] = f.stage_off;
-  out[FMOE_GEO_FUSED_HS_OFF] = f.hs_off;
-  out[FMOE_GEO_FUSED_HS_SLOT_BYTES] = f.hs_slot_bytes;
+  out[FMOE_GEO_FUSED_HBUF_OFF] = f.hbuf_off;
+  out[FMOE_GEO_FUSED_HBUF_STRIDE] = f.hb;
   out[FMOE_GEO_FUSED_DAREA_OFF] = f.darea_off;
-  out[FMOE_GEO_FUSED_DSLOT_BYTES] = f.dslot_bytes;
+  out[FMOE_GEO_FUSED_DAREA_BYTES] = f.darea_bytes;
   out[FMOE_GEO_FUSED_RING_OFF] = f.ring_off;
   out[FMOE_GEO_FUSED_NSTAGE] = f.nstage;
   out[FMOE_GEO_FUSED_STAGE_BYTES] = f.stage_bytes;
-  out[FMOE_GEO_FUSED_ROWS_PER_STAGE] = f.rows_per_stage;
-  out[FMOE_GEO_FUSED_NRMAX] = f.nrmax;
+  out[FMOE_GEO_FUSED_ROWS_PER_STAGE] = f.R;
   out[FMOE_GEO_FUSED_NPARTS] = f.nparts;
-  out[FMOE_GEO_FUSED_TAIL_ROWS] = kMaxTailRows;
+  out[FMOE_GEO_FUSED_LEN_MAX] = f.len_max;
   const BatchGeom g = batch_geometry_for(bits, hidden, inter, sms, smem_max);
   out[FMOE_GEO_BATCH_GRID] = g.grid;
   out[FMOE_GEO_BATCH_G] = g.G;
@@ -324,12 +284,29 @@ fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, i
   out[FMOE_GEO_BATCH_GU_STAGE_BYTES] = g.gu_stage_bytes;
   out[FMOE_GEO_BATCH_GU_XS_BYTES] = g.gu_xs_bytes;
   out[FMOE_GEO_BATCH_GU_SMEM] = (int64_t)g.gu_smem;
-  out[FMOE_GEO_BATCH_D_ROWS] = kDownRowsPerWarp * kBatchConsumerWarps;
-  out[FMOE_GEO_BATCH_D_NSTAGE] = g.d_nstage;
-  out[FMOE_GEO_BATCH_D_STAGE_BYTES] = g.d_stage_bytes;
-  out[FMOE_GEO_BATCH_D_XS_BYTES] = g.d_xs_bytes;
-  out[FMOE_GEO_BATCH_D_SMEM] = (int64_t)g.d_smem;
+  out[FMOE_GEO_BATCH_D_ROWS] = 32 * (32 / bits);
+  out[FMOE_GEO_BATCH_D_H_BYTES] = g.bd_h_bytes;
+  out[FMOE_GEO_BATCH_D_SMEM] = (int64_t)g.bd_smem;
   out[FMOE_GEO_BATCH_CTRL_BYTES] = kBatchCtrlBytes;
+  return FMOE_OK;
+}
+
+fmoe_status fmoe_debug_block_pieces(int bits, int hidden, int inter, int K, int has_shared, int sms, int block,
+                                    int64_t* out, int n) {
+  if (out == nullptr || n < 1 + 8 * kMaxPieces) return FMOE_ERR_INVALID_ARG;
+  if ((bits != 4 && bits != 2) || hidden <= 0 || inter <= 0 || hidden % kGroup || inter % kGroup || K < 1 ||
+      (has_shared != 0 && has_shared != 1) || sms < 1 || block < 0 || block >= sms)
+    return FMOE_ERR_INVALID_ARG;
+  const BlobLayout lay = blob_layout(bits, hidden, inter);
+  Piece pc[kMaxPieces];
+  int darea = 0;
+  const int np = block_pieces(K + has_shared, inter, block, sms, lay, pc, kMaxPieces, darea);
+  for (int i = 0; i < 1 + 8 * kMaxPieces; ++i) out[i] = 0;
+  out[0] = np;
+  for (int q = 0; q < np && q < kMaxPieces; ++q) {
+    const int64_t v[8] = {pc[q].slot, pc[q].i0, pc[q].cnt, pc[q].loc, pc[q].col_off, pc[q].sb_off, pc[q].g0, pc[q].ng};
+    for (int k = 0; k < 8; ++k) out[1 + 8 * q + k] = v[k];
+  }
   return FMOE_OK;
 }
 
@@ -340,6 +317,7 @@ const char* fmoe_status_string(fmoe_status s) {
     case FMOE_ERR_UNSUPPORTED: return "unsupported shape or format";
     case FMOE_ERR_CUDA: return "CUDA launch or runtime error";
     case FMOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case FMOE_ERR_RANGE: return "a partial output sum exceeded the fixed-point range (|v| > 2^19)";
   }
   return "unknown status";
 }
@@ -358,6 +336,7 @@ fmoe_status fmoe_last_device_error(void* ws, void* stream) {
   }
   if (word & (kErrWaitTimeout | kErrCopyTimeout)) return FMOE_ERR_TIMEOUT;
   if (word & kErrBadExpert) return FMOE_ERR_INVALID_ARG;
+  if (word & kErrRange) return FMOE_ERR_RANGE;
   return FMOE_OK;
 }
 

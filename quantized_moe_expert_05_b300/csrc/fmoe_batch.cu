@@ -15,19 +15,23 @@
 //                        tokens that picked it, in groups of G <= 4
 //   batch_gateup_kernel  h[t][k] = silu(Wg x_t) * (Wu x_t) for every (expert,
 //                        token group) item, 2 intermediate rows per warp
-//   batch_down_kernel    y[t][k] = Wd h[t][k], 4 output rows per warp
+//   batch_down_kernel    y[t][k] = Wd h[t][k]; a unit is 256 (4-bit) or 512
+//                        (2-bit) output rows, the down projection being
+//                        stored by column
 //   batch_combine_kernel out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
 // The two expert kernels run one block per SM over a contiguous share of
-// (item, row block) work units: a producer warp streams each unit's packed
-// rows (one contiguous range of the blob) into a shared-memory ring with
-// bulk asynchronous copies (TMA engine, mbarrier completion), eight consumer
-// warps compute from the ring.
+// (item, row block) work units.  In the gate/up kernel a producer warp
+// streams each unit's packed rows (one contiguous range of the blob) into a
+// shared-memory ring with bulk asynchronous copies (TMA engine, mbarrier
+// completion) and eight consumer warps compute from the ring; in the down
+// kernel each of eight warps streams its own columns' slices with cp.async.
 //
 // Sources: flash-moe write-up (discuss.pytorch.kr): "per-layer pipeline"
 // (softmax + top-K routing, expert forward, combine), "hand-written Metal
 // compute shaders" (dequant matvec, fused SwiGLU, MoE combine + residual +
 // sigmoid gate), "FMA-optimised dequant kernel" (code * scale + bias).
 #include <algorithm>
+#include <mutex>
 
 #include "fmoe_async.cuh"
 #include "fmoe_kernels.cuh"
@@ -291,6 +295,29 @@ __device__ __forceinline__ SliceCodes<BITS> smem_codes(const uint8_t* row, int s
   return q;
 }
 
+// acc[r] += code[r] * h for the rows of one 32-bit code word of a down column
+// (codes masked in place, h pre-scaled per position; hv: 2 pairs at 4-bit,
+// 4 at 2-bit).
+template <int BITS>
+__device__ __forceinline__ void down_word_bd(uint32_t w, const float2* hv, float2* acc) {
+  const uint32_t hi = w >> 16;
+  if constexpr (BITS == 4) {
+    acc[0] = __ffma2_rn(mk2(w, 0xFu, 0xF0u), hv[0], acc[0]);
+    acc[1] = __ffma2_rn(mk2(w, 0xF00u, 0xF000u), hv[1], acc[1]);
+    acc[2] = __ffma2_rn(mk2(hi, 0xFu, 0xF0u), hv[0], acc[2]);
+    acc[3] = __ffma2_rn(mk2(hi, 0xF00u, 0xF000u), hv[1], acc[3]);
+  } else {
+    acc[0] = __ffma2_rn(mk2(w, 0x3u, 0xCu), hv[0], acc[0]);
+    acc[1] = __ffma2_rn(mk2(w, 0x30u, 0xC0u), hv[1], acc[1]);
+    acc[2] = __ffma2_rn(mk2(w, 0x300u, 0xC00u), hv[2], acc[2]);
+    acc[3] = __ffma2_rn(mk2(w, 0x3000u, 0xC000u), hv[3], acc[3]);
+    acc[4] = __ffma2_rn(mk2(hi, 0x3u, 0xCu), hv[0], acc[4]);
+    acc[5] = __ffma2_rn(mk2(hi, 0x30u, 0xC0u), hv[1], acc[5]);
+    acc[6] = __ffma2_rn(mk2(hi, 0x300u, 0xC00u), hv[2], acc[6]);
+    acc[7] = __ffma2_rn(mk2(hi, 0x3000u, 0xC000u), hv[3], acc[7]);
+  }
+}
+
 // Sum over the 32 lanes of 16 values per lane; lane L receives the total of
 // value index L >> 1 (lanes 2i and 2i+1 both hold total i).
 __device__ __forceinline__ float reduce16(float (&v)[16]) {
@@ -446,15 +473,11 @@ __device__ __forceinline__ const uint8_t* item_blob(const BatchArgs& a, int expe
   return expert >= 0 ? a.experts + (size_t)expert * a.blob : a.shared;
 }
 
-// named barrier over the consumer warps only (per-thread count)
-__device__ __forceinline__ void batch_consumer_sync() {
-  asm volatile("barrier.sync 1, %0;" ::"n"(kBatchConsumerWarps * 32) : "memory");
-}
-
 // Shared control area of the expert kernels.
 struct BatchCtrl {
   uint64_t full[kBatchMaxStages];
   uint64_t empty[kBatchMaxStages];
+  uint64_t cbar;            // the consumer warps among themselves
   long long range[2];
   int item[kItemWords];
   int abort;
@@ -550,6 +573,7 @@ __device__ __forceinline__ void batch_init(BatchCtrl* ctl, int nstage) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], kBatchConsumerWarps);
     }
+    mbar_init(&ctl->cbar, kBatchConsumerWarps);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -582,17 +606,27 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
     return;
   }
   const RowAddr ra{(uint32_t)a.lay.gu_row, (uint32_t)a.lay.qh, (uint32_t)(2 * a.lay.qh), (uint32_t)a.lay.sh};
+  // the consumer warps at one point: every warp arrives once per use, whole
+  // (after __syncwarp); the wait is bounded
+  uint32_t nsync = 0;
+  auto cons_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->cbar);
+    const bool ok = mbar_wait(&ctl->cbar, nsync & 1u, a.timeout_ns, a.err, &ctl->abort);
+    ++nsync;
+    return ok;
+  };
   int cur = -1;
   long long k = 0;
   for (long long u = u0; u < u1; ++u, ++k) {
     const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
     if (item != cur) {
-      batch_consumer_sync();
+      if (!cons_sync()) break;
       if (threadIdx.x < kItemWords) ctl->item[threadIdx.x] = __ldcg(a.plan + kPlanHeader + item * kItemWords + threadIdx.x);
-      batch_consumer_sync();
+      if (!cons_sync()) break;
       stage_inputs<BITS>(xs4, xsum, ctl->item[1], NSL, kBatchConsumerWarps * 32,
                          [&](int i) { return a.x + (size_t)(ctl->item[2 + i] >> 8) * a.H; });
-      batch_consumer_sync();
+      if (!cons_sync()) break;
       cur = item;
     }
     const int st = (int)(k % geo.gu_nstage);
@@ -625,67 +659,189 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
 }
 
 // ---------------------------------------------------------------------------
-// down: unit = (item, 4 * consumer warps output rows); warp w takes records
-// 4w .. 4w+3 of the unit
+// down: unit = (item, kBdRows output rows).  The down projection is stored by
+// column, so a unit's codes are a 128-byte slice of every column (32 lanes x
+// one code word).  Warp w owns the columns [I*w/8, I*(w+1)/8) and streams
+// their slices through its own ring with 16-byte cp.async copies (a warp's
+// copies of one stage are one commit group); lane l accumulates rows
+// r0 + l*RW .. r0 + l*RW + RW-1 for each of the item's tokens, applies each
+// 64-column group's scale and bias, and the eight warps' partial sums are
+// added in a fixed order at the end of the unit.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16_bd(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_bd() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_bd() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+struct BdCtrl {
+  uint64_t cbar;            // the down warps among themselves
+  long long range[2];
+  int item[kItemWords];
+  int abort;
+};
+static_assert(sizeof(BdCtrl) <= kBdCtrlBytes, "control area");
+
 template <int BITS>
-__global__ void __launch_bounds__(kBatchThreads, 1) batch_down_kernel(BatchArgs a, float* __restrict__ y) {
+__global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, float* __restrict__ y) {
   extern __shared__ __align__(128) uint8_t smem[];
-  BatchCtrl* ctl = reinterpret_cast<BatchCtrl*>(smem);
-  const BatchGeom& geo = a.geo;
-  const int NSL = a.I / kSlice;
-  float4* xs4 = reinterpret_cast<float4*>(smem + kBatchCtrlBytes);
-  float* xsum = reinterpret_cast<float*>(xs4 + geo.G * 8 * (NSL + 1));
-  uint8_t* ring = smem + kBatchCtrlBytes + geo.d_xs_bytes;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NS = a.K + a.S;
-  const int rows = kDownRowsPerWarp * kBatchConsumerWarps;
-  const int n_rb = a.H / rows;
+  constexpr int RW = 32 / BITS;                    // rows per code word
+  constexpr int RB = 32 * RW;                      // rows per unit
+  constexpr int NV = BITS == 4 ? 4 : 8;            // pre-scaled copies of h per column
+  constexpr int SLICE = 128;                       // bytes of a column's slice of a unit
+  constexpr int G = kMaxTokGroup;
+  BdCtrl* ctl = reinterpret_cast<BdCtrl*>(smem);
+  const int I = a.I, H = a.H, NS = a.K + a.S;
+  float* hsm = reinterpret_cast<float*>(smem + kBdCtrlBytes);                 // [G][I] h of the item's tokens
+  uint8_t* ring = smem + kBdCtrlBytes + a.geo.bd_h_bytes;                     // [warp][stage][col][SLICE]
+  float* xbuf = reinterpret_cast<float*>(ring + (size_t)kBdWarps * kBdStages * kBdCols * SLICE);   // [warp][RB][G]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_rb = (H + RB - 1) / RB;
   long long u0, u1;
   block_share(a, n_rb, ctl->range, u0, u1);
-  batch_init(ctl, geo.d_nstage);
-
-  if (warp == kBatchProducerWarp) {
-    batch_produce(a, ctl, ring, geo.d_nstage, geo.d_stage_bytes, u0, u1, n_rb,
-                  UnitShape{a.lay.d_off, a.lay.d_row, rows});
-    return;
+  if (tid == 0) {
+    mbar_init(&ctl->cbar, kBdWarps);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const RowAddr ra{(uint32_t)(2 * a.lay.d_row), (uint32_t)a.lay.d_row, (uint32_t)a.lay.qi, (uint32_t)a.lay.d_row};
+  __syncthreads();
+  volatile int* abort = &ctl->abort;
+  uint32_t nsync = 0;
+  // all eight warps at one point (bounded)
+  auto cons_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->cbar);
+    const bool ok = mbar_wait(&ctl->cbar, nsync & 1u, a.timeout_ns, a.err, abort);
+    ++nsync;
+    return ok;
+  };
+  const int ca = (int)((long long)I * warp / kBdWarps), cb = (int)((long long)I * (warp + 1) / kBdWarps);
+  const int nch = (cb - ca + kBdCols - 1) / kBdCols;
+  uint8_t* wring = ring + (size_t)warp * kBdStages * kBdCols * SLICE;
   int cur = -1;
-  long long k = 0;
-  for (long long u = u0; u < u1; ++u, ++k) {
+  for (long long u = u0; u < u1; ++u) {
     const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
+    const int r0 = rb * RB;
     if (item != cur) {
-      batch_consumer_sync();
-      if (threadIdx.x < kItemWords) ctl->item[threadIdx.x] = __ldcg(a.plan + kPlanHeader + item * kItemWords + threadIdx.x);
-      batch_consumer_sync();
-      stage_inputs<BITS>(xs4, xsum, ctl->item[1], NSL, kBatchConsumerWarps * 32, [&](int i) {
-        const int pr = ctl->item[2 + i];
-        return a.h + ((size_t)(pr >> 8) * NS + (pr & 255)) * a.I;
-      });
-      batch_consumer_sync();
+      if (!cons_sync()) break;                     // every warp is done with the previous item
+      if (tid < kItemWords) ctl->item[tid] = __ldcg(a.plan + kPlanHeader + item * kItemWords + tid);
+      if (!cons_sync()) break;
+      const int n = ctl->item[1];
+      for (int idx = tid; idx < n * I; idx += kBdThreads) {
+        const int t = idx / I, i = idx - t * I;
+        const int pr = ctl->item[2 + t];
+        hsm[t * I + i] = __ldcg(a.h + ((size_t)(pr >> 8) * NS + (pr & 255)) * I + i);
+      }
+      if (!cons_sync()) break;
       cur = item;
     }
-    const int st = (int)(k % geo.d_nstage);
-    if (!mbar_wait(&ctl->full[st], (uint32_t)(k / geo.d_nstage) & 1u, a.timeout_ns, a.err, &ctl->abort)) break;
     const int n = ctl->item[1];
-    float acc[4][kMaxTokGroup] = {};
-    rows_dot_n<BITS>(n, ring + (size_t)st * geo.d_stage_bytes + (size_t)(kDownRowsPerWarp * warp) * a.lay.d_row,
-                     ra, xs4, xsum, NSL, acc);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->empty[st]);
-    float v[16];
+    const uint8_t* blob = item_blob(a, ctl->item[0]);
+    const uint8_t* dq = blob + a.lay.dq_off + (size_t)r0 * BITS / 8;
+    const int vb = min(SLICE, (H - r0) * BITS / 8);   // valid bytes of a column's slice (a multiple of 16)
+    const bool row_ok = lane * 4 < vb;
+    auto issue = [&](int ch) {
+      uint8_t* stg = wring + (size_t)(ch % kBdStages) * kBdCols * SLICE;
+      if (ch < nch) {
+        for (int k = lane; k < kBdCols * (SLICE / 16); k += 32) {
+          const int col = k / (SLICE / 16), part = k % (SLICE / 16);
+          const int i = ca + ch * kBdCols + col;
+          if (i < cb && part * 16 < vb) cp_async16_bd(stg + col * SLICE + part * 16, dq + (size_t)i * a.lay.dcol + part * 16);
+        }
+      }
+      cp_async_commit_bd();
+    };
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int ch = 0; ch < kBdStages - 1; ++ch) issue(ch);
+
+    float2 acc[G][RW / 2];
+    float outp[RW][G];
+    float hs[G];
 #pragma unroll
-      for (int t = 0; t < kMaxTokGroup; ++t) v[r * kMaxTokGroup + t] = acc[r][t];
-    const float tot = reduce16(v);
-    const int tok = (lane >> 1) & 3;
-    if ((lane & 1) == 0 && tok < n) {
-      const int pr = ctl->item[2 + tok];
-      y[((size_t)(pr >> 8) * NS + (pr & 255)) * a.H + rb * rows + kDownRowsPerWarp * warp + (lane >> 3)] = tot;
+    for (int t = 0; t < G; ++t) {
+      hs[t] = 0.f;
+#pragma unroll
+      for (int r = 0; r < RW / 2; ++r) acc[t][r] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < RW; ++r) outp[r][t] = 0.f;
     }
+    // (scale, bias) words of the lane's rows for group g
+    uint32_t sbv[RW];
+    auto load_sb = [&](int g) {
+      const uint4* src = reinterpret_cast<const uint4*>(blob + a.lay.dsb_off + (size_t)g * a.lay.dsb_group +
+                                                        (size_t)(r0 + RW * lane) * 4);
+#pragma unroll
+      for (int q = 0; q < RW / 4; ++q) {
+        const uint4 v = row_ok ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+        sbv[4 * q] = v.x; sbv[4 * q + 1] = v.y; sbv[4 * q + 2] = v.z; sbv[4 * q + 3] = v.w;
+      }
+    };
+    auto fold = [&]() {
+#pragma unroll
+      for (int t = 0; t < G; ++t) {
+#pragma unroll
+        for (int r = 0; r < RW / 2; ++r) {
+          outp[2 * r][t] += fmaf(bf16lo(sbv[2 * r]) * 18446744073709551616.0f, acc[t][r].x, bf16hi(sbv[2 * r]) * hs[t]);
+          outp[2 * r + 1][t] +=
+              fmaf(bf16lo(sbv[2 * r + 1]) * 18446744073709551616.0f, acc[t][r].y, bf16hi(sbv[2 * r + 1]) * hs[t]);
+          acc[t][r] = make_float2(0.f, 0.f);
+        }
+        hs[t] = 0.f;
+      }
+    };
+    int g_cur = ca / kGroup;
+    if (ca < cb) load_sb(g_cur);
+    for (int ch = 0; ch < nch; ++ch) {
+      issue(ch + kBdStages - 1);
+      cp_async_wait_bd<kBdStages - 1>();
+      __syncwarp();
+      const uint8_t* stg = wring + (size_t)(ch % kBdStages) * kBdCols * SLICE;
+      const int ncol = min(kBdCols, cb - ca - ch * kBdCols);
+      for (int col = 0; col < ncol; ++col) {
+        const int i = ca + ch * kBdCols + col;
+        if ((i >> 6) != g_cur) {
+          fold();
+          g_cur = i >> 6;
+          load_sb(g_cur);
+        }
+        const uint32_t w = row_ok ? reinterpret_cast<const uint32_t*>(stg + col * SLICE)[lane] : 0u;
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+          if (t < n) {
+            const float hh = hsm[t * I + i];
+            hs[t] += hh;
+            float2 hv[NV / 2];
+#pragma unroll
+            for (int q = 0; q < NV / 2; ++q) hv[q] = make_float2(hh * pos_scale<BITS>(2 * q), hh * pos_scale<BITS>(2 * q + 1));
+            down_word_bd<BITS>(w, hv, acc[t]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    cp_async_wait_bd<0>();
+    if (ca < cb) fold();
+    // the eight warps' partial sums, added in warp order
+    float* xb = xbuf + (size_t)warp * RB * G;
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+      for (int t = 0; t < G; ++t) xb[(RW * lane + r) * G + t] = outp[r][t];
+    if (!cons_sync()) break;
+    for (int idx = tid; idx < RB * n; idx += kBdThreads) {
+      const int row = idx / n, t = idx - row * n;
+      if (r0 + row < H) {
+        float v = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kBdWarps; ++w2) v += xbuf[((size_t)w2 * RB + row) * G + t];
+        const int pr = ctl->item[2 + t];
+        y[((size_t)(pr >> 8) * NS + (pr & 255)) * H + r0 + row] = v;
+      }
+    }
+    if (!cons_sync()) break;
   }
+  cp_async_wait_bd<0>();
 }
 
 // out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
@@ -707,6 +863,36 @@ __global__ void batch_combine_kernel(BatchArgs a) {
   for (int k = 0; k < a.K; ++k) add(a.weights[t * a.K + k], k);
   if (a.S) add(a.gate[t], a.K);
   reinterpret_cast<float4*>(a.out)[idx] = acc;
+}
+
+// x = h / sqrt(mean(h^2) + eps) (unit weight): one block, a fixed summation
+// order (the general path of a stack; the persistent kernel normalises in
+// its own prologue)
+constexpr int kNormThreads = 1024;
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ h, float* __restrict__ x,
+                                                               int H, float eps) {
+  __shared__ float s_part[kNormThreads / 32];
+  __shared__ float s_rinv;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < H; j += kNormThreads) {
+    const float v = __ldcg(h + j);
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kNormThreads / 32; ++w) t += s_part[w];
+    s_rinv = 1.0f / sqrtf(t / (float)H + eps);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < H; j += kNormThreads) x[j] = __ldcg(h + j) * s_rinv;
+}
+
+cudaError_t launch_rmsnorm(const float* h, float* x, int H, float eps, cudaStream_t st) {
+  rmsnorm_kernel<<<1, kNormThreads, 0, st>>>(h, x, H, eps);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -739,14 +925,16 @@ BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max) {
   if (sms < 1 || smem_max <= kBatchCtrlBytes) return g;
   const BlobLayout lay = blob_layout(bits, H, I);
   const size_t avail = (size_t)smem_max - kBatchCtrlBytes;
-  const int d_rows = kDownRowsPerWarp * kBatchConsumerWarps;
-  if (H % d_rows) return g;
+  const size_t bd_ring = (size_t)kBdWarps * kBdStages * kBdCols * 128;
+  const int rb = 32 * (32 / bits);                  // output rows per down unit
   // the most tokens per item, then the most gate/up warps, for which two
-  // ring stages fit next to the staged inputs of both kernels
+  // gate/up ring stages fit next to the staged inputs, and the down kernel's
+  // staged h, ring and partial sums fit
   for (int G = kMaxTokGroup; G >= 1; G /= 2) {
-    const size_t gx = round_up128(staged_bytes(H, G)), dx = round_up128(staged_bytes(I, G));
-    const size_t d_stage = round_up128((size_t)d_rows * lay.d_row);
-    if (dx + 2 * d_stage > avail) continue;
+    const size_t gx = round_up128(staged_bytes(H, G));
+    const size_t bdh = round_up128((size_t)G * I * 4);
+    const size_t bd_smem = kBdCtrlBytes + bdh + bd_ring + (size_t)kBdWarps * rb * kMaxTokGroup * 4;
+    if (bd_smem > (size_t)smem_max) continue;
     for (int w = kBatchConsumerWarps; w >= 1; w /= 2) {
       const size_t gu_stage = round_up128((size_t)2 * w * lay.gu_row);
       if (I % (2 * w) || gx + 2 * gu_stage > avail) continue;
@@ -757,10 +945,8 @@ BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max) {
       g.gu_nstage = (int)std::min<size_t>(kBatchMaxStages, (avail - gx) / gu_stage);
       g.gu_xs_bytes = (int)gx;
       g.gu_smem = kBatchCtrlBytes + gx + (size_t)g.gu_nstage * gu_stage;
-      g.d_stage_bytes = (int)d_stage;
-      g.d_nstage = (int)std::min<size_t>(kBatchMaxStages, (avail - dx) / d_stage);
-      g.d_xs_bytes = (int)dx;
-      g.d_smem = kBatchCtrlBytes + dx + (size_t)g.d_nstage * d_stage;
+      g.bd_h_bytes = (int)bdh;
+      g.bd_smem = bd_smem;
       g.grid = sms;
       return g;
     }
@@ -780,6 +966,7 @@ static cudaError_t allow_smem(Kern k, size_t bytes, size_t& done) {
 // per device: gate/up 4-bit, 2-bit; down 4-bit, 2-bit (function attributes
 // belong to the device's context)
 static size_t g_smem_set[64][4];
+static std::mutex g_smem_mu;
 
 cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
   int dev = 0;
@@ -789,6 +976,7 @@ cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
   a.geo = batch_geometry(a.bits, a.H, a.I, dev);
   if (a.geo.grid == 0) return cudaErrorInvalidValue;
   size_t* set = g_smem_set[dev];
+  std::lock_guard<std::mutex> lock(g_smem_mu);
 
   batch_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -804,11 +992,11 @@ cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (a.bits == 4) {
-    if ((e = allow_smem(batch_down_kernel<4>, g.d_smem, set[2])) != cudaSuccess) return e;
-    batch_down_kernel<4><<<g.grid, kBatchThreads, g.d_smem, st>>>(a, y);
+    if ((e = allow_smem(batch_down_kernel<4>, g.bd_smem, set[2])) != cudaSuccess) return e;
+    batch_down_kernel<4><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y);
   } else {
-    if ((e = allow_smem(batch_down_kernel<2>, g.d_smem, set[3])) != cudaSuccess) return e;
-    batch_down_kernel<2><<<g.grid, kBatchThreads, g.d_smem, st>>>(a, y);
+    if ((e = allow_smem(batch_down_kernel<2>, g.bd_smem, set[3])) != cudaSuccess) return e;
+    batch_down_kernel<2><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -5,112 +5,67 @@
 // per layer as GPU command buffers submitted without waiting; the slotstream
 // write-up (simpler24.com, "the disk was not the slow part") measured batch-1
 // quantised matmuls at 20 % of memory bandwidth because of dispatch cost.
-// Here one cooperative launch (one block per SM) runs every layer.  Block c
-// owns intermediate rows [I*c/n, I*(c+1)/n) and output rows [H*c/n, H*(c+1)/n)
-// of every selected expert ("slot"); its warps have fixed roles:
+// Here one cooperative launch (one block per SM) runs every layer.
 //
-//   producer       one lane issues every bulk asynchronous copy (TMA engine,
-//                  mbarrier completion) of the block's packed rows in the
-//                  order they are consumed: gate/up records through a ring
-//                  of stages, each slot's down records into its own area.
-//                  The shared expert needs no routing, so its rows go first.
-//   12 gate/up     dequantised gate/up dot products of the ring's stages
-//   warps          against the layer input (pre-scaled, in shared memory);
-//                  partial sums per row; a stage is released through an
-//                  mbarrier, never a block barrier.
-//   finaliser      h = silu(gate) * up for the block's rows, published to L2
-//   2 exchange     gather each slot's full h from L2 into shared memory,
-//   warps          pre-scaled for the down projection (even / odd slots); the
-//                  second also routes: it computes the next layer's top-K at
-//                  the end of the current layer and publishes the ids once
-//                  that layer's input is complete.
-//   4 down warps   fold w_slot * (down_row . h_slot) into per-row sums as each
-//                  slot's h arrives; finally out[j] = residual[j] + sum.
+// Ownership.  The K+S selected experts ("slots"; slot 0 is the shared expert
+// when there is one) have NS*I intermediate columns in all.  Block c of n
+// owns the contiguous range [NS*I*c/n, NS*I*(c+1)/n) of them in slot-major
+// order: for each owned column i of a slot it computes the gate and up row
+// dot products, h[i] = w_slot * silu(gate . x) * (up . x), and the column's
+// contribution Wd[:, i] * h[i] to all H outputs.  h never leaves the block;
+// the down projection is stored by column so that a block's columns are one
+// contiguous byte range.  Every byte of the selected experts is read by one
+// block (the down (scale,bias) words of a 64-column group by each block that
+// owns a column of it).
 //
-// Blocks exchange data without counters or barriers: every value published
-// to another block (h rows, and the layer outputs of a stack) is stored as
-// one 64-bit (value, tag) word whose tag names the launch and layer, so a
-// reader knows a value is current from the load that fetches it (the
-// low-latency protocol idea of NCCL's LL transport).  A layer's routed
-// experts are requested only once its input is complete (their ids are
-// published then); the shared expert, which needs no routing, may be
-// requested as soon as this block has finished the previous layer.  Every wait is bounded (%globaltimer); a wait
-// that runs out records the time-out in the workspace error word, and every
-// later wait of the block returns at once, so the launch always ends.
+// One exchange per layer.  Each block adds its H partial outputs into an
+// accumulator with 64-bit integer atomics in fixed point (value << 8 | count
+// of contributions, see fmoe_internal.cuh): the sum does not depend on the
+// order of arrival, and a word is complete when its count equals the number
+// of blocks, so readers need no counter or flag.  Every block then reads the
+// whole sum as the next layer's input (residual + sum, RMS-normalised for a
+// stack).  Three accumulators rotate: layer l adds into A[l%3] while each
+// block clears its own slice of A[(l+1)%3]; A[(l+1)%3] was last read at the
+// start of layer l-1, which every block finished before its layer-l-1 sums
+// (and so before the clear) could be complete.
+//
+// Warp roles:
+//   12 gate/up warps   dequantised gate/up dot products of the ring's stages
+//                      against the layer input (pre-scaled, in registers);
+//                      partial sums per row into shared memory
+//   8 down warps       each thread owns H/256 output rows; for every owned
+//                      column, in order, folds its codes times h into
+//                      per-row sums, applies the group's scale and bias per
+//                      64-column group, and at the end of the layer adds the
+//                      rows into the accumulator
+//   producer           one warp; its lanes take turns issuing the bulk
+//                      asynchronous copies (TMA engine, mbarrier completion):
+//                      gate/up records through a ring of stages, the block's
+//                      down columns and their (scale,bias) words into the
+//                      down area.  The shared expert needs no routing, so a
+//                      block that owns shared columns requests them for the
+//                      next layer as soon as ring stages are free.
+//   finaliser          routes (top-K of the next layer at the end of the
+//                      current one, published once the layer input is
+//                      complete), clears the block's accumulator slice,
+//                      turns each stage's partial sums into h
+// The first 20 warps also gather each layer's input from the accumulator.
+//
+// No layer's routed experts are requested before its input is complete.
+// Every wait is bounded (%globaltimer); a wait that runs out records the
+// time-out in the workspace error word, and every later wait of the block
+// returns at once, so the launch always ends.  Block-wide barriers appear
+// only at the top level (after set-up, before exit), reached once by every
+// thread; everything else synchronises through mbarriers or release/acquire
+// counters.
+#include <mutex>
+
 #include "fmoe_async.cuh"
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
 
 namespace {
-
-// (value, tag) words: a float and the tag of the launch and layer that wrote
-// it, stored and loaded as one 64-bit access so that a reader sees either the
-// old pair or the new one, never a mix.
-__device__ __forceinline__ void ll_store(unsigned long long* p, float v, uint32_t tag) {
-  const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
-}
-
-__device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
-__device__ __forceinline__ float ll_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
-__device__ __forceinline__ bool ll_is(unsigned long long w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
-
-// Eight consecutive (value, tag) words (16-byte aligned) once all carry
-// `tag` (one thread, bounded wait).
-__device__ __forceinline__ void ll_wait8(const unsigned long long* p, uint32_t tag, float4& v0, float4& v1,
-                                         unsigned long long timeout_ns, uint32_t* err, volatile int* abort) {
-  uint64_t t0 = 0;
-  bool started = false;
-  while (true) {
-    unsigned long long w[8];
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) ll_load2(p + i, w[i], w[i + 1]);
-    bool ok = true;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ok = ok && ll_is(w[i], tag);
-    v0 = make_float4(ll_value(w[0]), ll_value(w[1]), ll_value(w[2]), ll_value(w[3]));
-    v1 = make_float4(ll_value(w[4]), ll_value(w[5]), ll_value(w[6]), ll_value(w[7]));
-    if (ok || *abort) return;
-    const uint64_t t = global_timer_ns();
-    if (!started) {
-      t0 = t;
-      started = true;
-    } else if (t - t0 > timeout_ns) {
-      atomicOr(err, kErrWaitTimeout);
-      *abort = 1;
-      return;
-    }
-    __nanosleep(kInputPollNs);
-  }
-}
-
-// 16-byte global -> shared copy that holds no registers (completion by
-// cp.async.wait_all).  Each 8-byte (value, tag) word of the pair is copied
-// whole: an aligned 16-byte read returns every 8-byte half as it was at one
-// time.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Block-wide barrier.  The warps of this kernel take different paths and
-// reach it after divergent code (a lane running a loop alone, a row owner
-// storing); each warp first reconverges all of its lanes, so that the barrier
-// counts whole warps that arrive once each.
-__device__ __forceinline__ void cta_sync() {
-  __syncwarp();
-  asm volatile("barrier.sync 0;" ::: "memory");
-}
-
-// named barrier over the consumer warps only (reconverged, as above)
-__device__ __forceinline__ void consumer_sync() {
-  __syncwarp();
-  asm volatile("barrier.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
 
 // Reduce four values over `width` consecutive lanes (a power of two, 4..32)
 // with a transposed butterfly: on return the group's lane 0 holds sum(a),
@@ -128,384 +83,258 @@ __device__ __forceinline__ float quad_reduce(float a, float b, float c, float d,
   return y;
 }
 
-}  // namespace
+__device__ __forceinline__ void ld_relaxed_v2(const unsigned long long* p, unsigned long long& a,
+                                              unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 
-// Slice s of a slot's staged h (float4 j of slice s at j*hstride + s, already
-// pre-scaled): the 32 values as pairs, and their plain sum, taken from the
-// pre-scaled values one position class at a time (an exact power-of-two
-// rescaling each).
-template <int BITS>
-__device__ __forceinline__ float staged_h_slice(const float4* hs4, int hstride, int s, SliceX& hs) {
-  float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
-  float2 c45 = make_float2(0.f, 0.f), c67 = make_float2(0.f, 0.f);
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_shared(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// Eight consecutive accumulator words (16-byte aligned) once every count is
+// `need`; their sums in s.  One thread, bounded.  Returns false if the block
+// gave up.
+__device__ __forceinline__ bool poll8(const unsigned long long* p, int need, float (&s)[8],
+                                      unsigned long long timeout_ns, uint32_t* err, volatile int* abort) {
+  uint64_t t0 = 0;
+  bool started = false;
+  while (true) {
+    unsigned long long w[8];
 #pragma unroll
-  for (int j = 0; j < kSlice / 4; ++j) {
-    const float4 v = hs4[(size_t)j * hstride + s];
-    hs[2 * j] = make_float2(v.x, v.y);
-    hs[2 * j + 1] = make_float2(v.z, v.w);
-    if (BITS == 4 || (j & 1) == 0) {
-      c01 = __fadd2_rn(c01, hs[2 * j]);
-      c23 = __fadd2_rn(c23, hs[2 * j + 1]);
-    } else {
-      c45 = __fadd2_rn(c45, hs[2 * j]);
-      c67 = __fadd2_rn(c67, hs[2 * j + 1]);
+    for (int i = 0; i < 8; i += 2) ld_relaxed_v2(p + i, w[i], w[i + 1]);
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ok = ok && fix_count(w[i]) == need;
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] = fix_value(w[i]);
+      return true;
+    }
+    if (*abort) return false;
+    const uint64_t t = global_timer_ns();
+    if (!started) {
+      t0 = t;
+      started = true;
+    } else if (t - t0 > timeout_ns) {
+      atomicOr(err, kErrWaitTimeout);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(kPollNs);
+  }
+}
+
+// Wait (bounded) until a release counter in shared memory reaches `target`.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, unsigned long long timeout_ns,
+                                           uint32_t* err, volatile int* abort) {
+  if (ld_acquire_shared(ctr) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(32);
+    if (ld_acquire_shared(ctr) >= target) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      atomicOr(err, kErrWaitTimeout);
+      *abort = 1;
+      return false;
     }
   }
-  float hsm = (c01.x * inv_pos_scale<BITS>(0) + c01.y * inv_pos_scale<BITS>(1)) +
-              (c23.x * inv_pos_scale<BITS>(2) + c23.y * inv_pos_scale<BITS>(3));
-  if (BITS == 2)
-    hsm += (c45.x * inv_pos_scale<BITS>(4) + c45.y * inv_pos_scale<BITS>(5)) +
-           (c67.x * inv_pos_scale<BITS>(6) + c67.y * inv_pos_scale<BITS>(7));
-  return hsm;
 }
 
-// w * (down row r . h) over slice s: the row's record in shared memory.
+// Positions of the 8 elements e..e+7 (e a multiple of 8) in the slice-major
+// input layout: float4 j of slice s at j*tl + s.
+__device__ __forceinline__ int xs_pos4(int e, int tl) { return ((e & 31) >> 2) * tl + (e >> 5); }
+
+}  // namespace
+
+// Down-projection step of one column for one 32-bit word of codes (rows
+// 32/BITS of them): acc[r] += code[r] * h, the codes masked in place and h
+// pre-scaled per position (hv: BITS == 4: 4 values, 2: 8 values).
 template <int BITS>
-__device__ __forceinline__ float down_slice(const uint8_t* rec, const BlobLayout& lay, int s, const SliceX& hs,
-                                            float hsm, float w, float acc) {
-  SliceCodes<BITS> q;
-  if constexpr (BITS == 4) q.v = *reinterpret_cast<const uint4*>(rec + (size_t)s * 16);
-  else q.v = *reinterpret_cast<const uint2*>(rec + (size_t)s * 8);
-  const uint32_t sbw = *reinterpret_cast<const uint32_t*>(rec + lay.qi + (size_t)(s >> 1) * 4);
-  return fmaf(w, slice_term<BITS>(q, sbw, hs, hsm), acc);
+__device__ __forceinline__ void down_word(uint32_t w, const float2* hv, float2* acc) {
+  const uint32_t hi = w >> 16;
+  if constexpr (BITS == 4) {
+    acc[0] = __ffma2_rn(mk2(w, 0xFu, 0xF0u), hv[0], acc[0]);
+    acc[1] = __ffma2_rn(mk2(w, 0xF00u, 0xF000u), hv[1], acc[1]);
+    acc[2] = __ffma2_rn(mk2(hi, 0xFu, 0xF0u), hv[0], acc[2]);
+    acc[3] = __ffma2_rn(mk2(hi, 0xF00u, 0xF000u), hv[1], acc[3]);
+  } else {
+    acc[0] = __ffma2_rn(mk2(w, 0x3u, 0xCu), hv[0], acc[0]);
+    acc[1] = __ffma2_rn(mk2(w, 0x30u, 0xC0u), hv[1], acc[1]);
+    acc[2] = __ffma2_rn(mk2(w, 0x300u, 0xC00u), hv[2], acc[2]);
+    acc[3] = __ffma2_rn(mk2(w, 0x3000u, 0xC000u), hv[3], acc[3]);
+    acc[4] = __ffma2_rn(mk2(hi, 0x3u, 0xCu), hv[0], acc[4]);
+    acc[5] = __ffma2_rn(mk2(hi, 0x30u, 0xC0u), hv[1], acc[5]);
+    acc[6] = __ffma2_rn(mk2(hi, 0x300u, 0xC00u), hv[2], acc[6]);
+    acc[7] = __ffma2_rn(mk2(hi, 0x3000u, 0xC000u), hv[3], acc[7]);
+  }
 }
 
-template <int BITS>
-__global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constant__ FusedParams p) {
+// MW: code words of a down column per down thread, ceil(H / (32/BITS) / 256)
+// rounded up to 1, 2 or 4.
+template <int BITS, int MW>
+__global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int RW = 32 / BITS;                 // rows per code word of a down column
+  constexpr int NV = BITS == 4 ? 4 : 8;         // pre-scaled copies of h per column
   const FusedPlan& pl = p.plan;
   const BlobLayout& lay = p.lay;
   // control area
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem);          // ring stage filled (count 1 + bytes)
-  uint64_t* bar_empty = bar_full + kMaxStages;                      // ring stage released (one per consumer warp)
-  uint64_t* bar_dfull = bar_empty + kMaxStages;                     // slot's down records filled
-  uint64_t* bar_routed = bar_dfull + kMaxSlots;                     // slot's expert id known
-  uint64_t* bar_slot = bar_routed + kMaxSlots;                      // slot's partial sums written
-  uint64_t* bar_hready = bar_slot + kMaxSlots;                      // slot's full h staged
-  uint64_t* bar_xready = bar_hready + kMaxSlots;                    // layer input complete (consumers)
-  uint64_t* bar_ddone = bar_xready + 1;                             // slot's down records used (down warps)
-  uint64_t* bar_layer = bar_ddone + kMaxSlots;                      // layer done (every warp but the producer)
-  uint64_t* bar_tail = bar_layer + 1;                               // tail slots' down rows done (gate/up warps)
-  float* s_tail = reinterpret_cast<float*>(smem + 1536);            // [nd] tail slots' sum per down row
-  int* s_ids = reinterpret_cast<int*>(smem + 1024);                 // [kMaxSlots]
-  float* s_w = reinterpret_cast<float*>(smem + 1152);               // [kMaxSlots] routing weights, shared gate
-  float* s_red = reinterpret_cast<float*>(smem + 1280);             // [kConsumerWarps][2]
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 1408);
-  float* s_part = reinterpret_cast<float*>(smem + pl.part_off);    // [slot][row][part][2]
-  unsigned long long* s_stage = reinterpret_cast<unsigned long long*>(smem + pl.stage_off);  // one slot's h words
-  uint8_t* s_hs = smem + pl.hs_off;                                // [slot] h slices + slice sums
-  float4* s_x4 = reinterpret_cast<float4*>(smem + pl.xs_off);      // layer input, slice-major
-  uint8_t* darea = smem + pl.darea_off;                            // [slot] down records
-  uint8_t* ring = smem + pl.ring_off;                              // [stage] gate/up records
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem);   // ring stage filled (count 1 + bytes)
+  uint64_t* bar_empty = bar_full + kMaxStages;              // ring stage free (gate/up warps + finaliser)
+  uint64_t* bar_gudone = bar_empty + kMaxStages;            // stage's partial sums written (gate/up warps)
+  uint64_t* bar_x = bar_gudone + kMaxStages;                // layer input gathered (input warps)
+  uint64_t* bar_routed = bar_x + 1;                         // routing published (finaliser)
+  uint64_t* bar_zero = bar_routed + 1;                      // next accumulator slice cleared (finaliser)
+  uint64_t* bar_dfull = bar_zero + 1;                       // down area filled (count 1 + bytes)
+  uint64_t* bar_ddone = bar_dfull + 1;                      // down area free again (down warps)
+  uint64_t* bar_dsync = bar_ddone + 1;                      // [2] down warps among themselves
+  Piece* s_pc = reinterpret_cast<Piece*>(smem + 512);       // [kMaxPieces]
+  int* s_np = reinterpret_cast<int*>(smem + 640);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 644);
+  uint32_t* s_hdone = reinterpret_cast<uint32_t*>(smem + 648);   // stages whose h is written (cumulative)
+  int* s_ids = reinterpret_cast<int*>(smem + 704);          // [kMaxSlots]
+  float* s_w = reinterpret_cast<float*>(smem + 832);        // [kMaxSlots] routing weights, shared gate
+  float* s_red = reinterpret_cast<float*>(smem + 960);      // [kPollWarps][2]
+  float4* s_x4 = reinterpret_cast<float4*>(smem + pl.xs_off);   // layer input h (not normalised), slice-major
+  float* s_part = reinterpret_cast<float*>(smem + pl.part_off); // [stage][R][nparts][2]
+  float* s_hb = reinterpret_cast<float*>(smem + pl.hbuf_off);   // [len][hb]: NV pre-scaled h, then h
+  uint8_t* darea = smem + pl.darea_off;
+  uint8_t* ring = smem + pl.ring_off;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, n = gridDim.x;
   const int NS = p.K + p.S;
   const int H = p.H, I = p.I;
-
-  // Gate/up: this block owns rows [ra, ra+nr) of every slot.  The rows of
-  // all slots form one sequence of NS*nr "virtual rows" (slot-major) that
-  // the ring carries R at a time; a gate/up warp handles rows rs0 and rs1
-  // of each stage (its slice range `sl` of H).
   const int tl = H / kSlice;
-  const int R = pl.rows_per_stage;
-  const int nparts = pl.nparts;
-  const int gw = tl < 32 ? tl : 32;                                // reduction width
-  const int ra = (int)((long long)I * c / n);
-  const int nr = (int)((long long)I * (c + 1) / n) - ra;
-  const int V = NS * nr;
-  const int nstg = (V + R - 1) / R;
-  int rs0, sl, pi;
-  if (tl >= 32) {
-    rs0 = warp < (R / 2) * nparts ? warp / nparts : R;   // warps beyond a whole pass stay idle
-    pi = warp % nparts;
-    sl = pi * 32 + lane;
-  } else {
-    rs0 = warp * (32 / tl) + lane / tl;
-    pi = 0;
-    sl = lane % tl;
-  }
-  const int rs1 = rs0 + R / 2;
-  // Down: this block owns output rows [ja, ja+nd); a row has tld slices;
-  // lpr lanes per row, rpp rows per warp pass.  Staged h: float4 j of slice
-  // s at j*(tld+1) + s (the padding keeps the exchanger's stores free of
-  // bank conflicts), then the tld slice sums.
-  const int ja = (int)((long long)H * c / n);
+  const int R = pl.R, nparts = pl.nparts, hb = pl.hb;
+  const int gw = tl < 32 ? tl : 32;                          // reduction width of a gate/up row
+  const long long V = (long long)NS * I;
+  const int len = (int)(V * (c + 1) / n - V * c / n);       // columns of this block
+  const int nstg = (len + R - 1) / R;
+  const int ja = (int)((long long)H * c / n);               // accumulator slice this block clears
   const int nd = (int)((long long)H * (c + 1) / n) - ja;
-  const int tld = I / kSlice;
-  const int hstride = tld + 1;
-  const int lpr = tld < 32 ? tld : 32;
-  const int rpp = 32 / lpr;
-  const int spl = tld > 32 ? tld / 32 : 1;
-  const int ngroups = (nd + rpp - 1) / rpp;
-  const int dlag = pl.dlag;
-  // slots whose down rows the gate/up warps take over at the end of a layer
-  const int ntail = NS - 1 < kFusedTailSlots ? NS - 1 : kFusedTailSlots;
+  const unsigned long long tmo = p.timeout_ns;
 
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], kGuWarps);
+      mbar_init(&bar_empty[i], kGuWarps + 1);
+      mbar_init(&bar_gudone[i], kGuWarps);
     }
-    for (int i = 0; i < kMaxSlots; ++i) {
-      mbar_init(&bar_dfull[i], 1);
-      mbar_init(&bar_routed[i], 1);
-      mbar_init(&bar_slot[i], kGuWarps);
-      mbar_init(&bar_hready[i], 1);
-    }
-    mbar_init(bar_xready, 1);
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&bar_ddone[i], kDownWarps);
-    mbar_init(bar_layer, kFusedThreads / 32 - 1);
-    mbar_init(bar_tail, kGuWarps);
+    mbar_init(bar_x, kPollWarps);
+    mbar_init(bar_routed, 1);
+    mbar_init(bar_zero, 1);
+    mbar_init(bar_dfull, 1);
+    mbar_init(bar_ddone, kDnWarps);
+    mbar_init(&bar_dsync[0], kDnWarps);
+    mbar_init(&bar_dsync[1], kDnWarps);
+    int dbytes = 0;
+    *s_np = block_pieces(NS, I, c, n, lay, s_pc, kMaxPieces, dbytes);
     *s_abort = 0;
+    *s_hdone = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  cta_sync();
+  __syncthreads();
+  const int np = *s_np;
+  const uint32_t lb = *reinterpret_cast<volatile uint32_t*>(p.lbase);
 
-  uint32_t g_issue = 0;   // gate/up stages issued (producer warp)
-  uint32_t n_copies = 0;  // bulk copies issued (producer warp): picks the issuing lane
-  uint32_t g_cons = 0;    // gate/up stages consumed (consumer warps)
-  const unsigned long long tmo = p.timeout_ns;
-  // tags of this launch: layer l publishes with epoch * 64 + l + 1 (never 0,
-  // the value of a freshly zeroed workspace)
-  const uint32_t tag0 = *reinterpret_cast<volatile uint32_t*>(p.epoch) * (uint32_t)kMaxFusedLayers + 1u;
-
-  int nx_id = -1;       // routing exchange warp: top-K pick of its lane for the coming layer
+  uint32_t g_issue = 0;   // ring stages issued (producer)
+  uint32_t n_copies = 0;  // bulk copies issued (producer): picks the issuing lane
+  uint32_t g_cons = 0;    // ring stages consumed (gate/up warps, finaliser)
+  int nx_id = -1;         // finaliser: top-K pick of its lane for the coming layer
   float nx_l = 0.f;
+  auto slot_h = [&](int slot) -> int { return p.S ? (slot == 0 ? p.K : slot - 1) : slot; };
+
   for (int l = 0; l < p.L; ++l) {
     const FusedLayerPtrs lp = p.layer[l];
     const uint32_t lpar = (uint32_t)(l & 1);
-    const uint32_t tag = tag0 + (uint32_t)l;
-    // input: x (block), the stack input h (layer 0), or the previous layer's
-    // published output; residual likewise; output: out, or published words
-    const bool in_ll = p.norm && l > 0;
-    const bool out_ll = p.norm && l < p.L - 1;
-    const float* hin = p.norm ? p.out : p.x;
-    const unsigned long long* hin_ll = p.hbufll + (size_t)((l - 1) & 1) * H;
-    unsigned long long* out_llp = p.hbufll + (size_t)(l & 1) * H;
-    // slot ps: 0 is the shared expert when there is one; its h goes to index K
-    auto hidx = [&](int ps) -> int { return p.S ? (ps == 0 ? p.K : ps - 1) : ps; };
+    unsigned long long* acc_cur = p.acc + (size_t)((lb + l) % 3) * H;
+    const unsigned long long* acc_prev = p.acc + (size_t)((lb + l + 2) % 3) * H;
+    unsigned long long* acc_next = p.acc + (size_t)((lb + l + 1) % 3) * H;
 
-    if (warp == kProducerWarp) {
+    if (warp < kPollWarps) {
       // ------------------------------------------------------------------
-      // producer: the warp walks the layer's copies in consumption order;
-      // lane 0 declares each barrier's bytes, and successive copies are
-      // issued by successive lanes: the copies one thread issues are carried
-      // out one after another, those of different threads side by side
+      // layer input: x (block), h (first layer of a stack) or the previous
+      // layer's complete sum added to its input; staged slice-major, with
+      // the sums of squares and of products with the shared-gate vector
       // ------------------------------------------------------------------
-#if FMOE_FUSED_LATE_PREFETCH
-      // the previous layer's exchanges go first: its last slot's h staged
-      if (l > 0) mbar_wait(&bar_hready[NS - 1], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
-#endif
-      auto slot_blob = [&](int ps) -> const uint8_t* {
-        if (p.S && ps == 0) return lp.shared;
-        return lp.experts + (size_t)s_ids[ps] * p.blob;
-      };
-      // lane 0's view of the abort flag, the same in every lane
-      auto aborted = [&]() -> bool { return __shfl_sync(0xFFFFFFFFu, *s_abort, 0) != 0; };
-      bool routed = false;       // routed ids are published all at once
-      auto ensure_routed = [&](int ps) {
-        if (ps >= p.S && !routed) {
-          mbar_wait(&bar_routed[0], lpar, tmo, p.err, s_abort);
-          routed = true;
-        }
-      };
-      auto copy = [&](void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-        if (lane == (int)(n_copies % kFusedIssueLanes)) bulk_g2s(dst, src, bytes, bar);
-        ++n_copies;
-      };
-      auto issue_down = [&](int ps) {
-        // the previous layer's down work is done with this slot's area
-        if (l > 0) mbar_wait(&bar_ddone[ps], (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
-        if (nd == 0 || aborted()) {
-          if (lane == 0) mbar_arrive_expect_tx(&bar_dfull[ps], 0);
-          return;
-        }
-        ensure_routed(ps);
-        if (lane == 0) mbar_arrive_expect_tx(&bar_dfull[ps], (uint32_t)(nd * lay.d_row));
-        __syncwarp();
-        const int per = (nd + kFusedDownCopies - 1) / kFusedDownCopies;
-        for (int r0 = 0; r0 < nd; r0 += per)
-          copy(darea + (size_t)ps * pl.dslot_bytes + (size_t)r0 * lay.d_row,
-               slot_blob(ps) + lay.d_off + (size_t)(ja + r0) * lay.d_row, (uint32_t)(min(per, nd - r0) * lay.d_row),
-               &bar_dfull[ps]);
-      };
-      int dnext = 0;
-      for (int k = 0; k < nstg; ++k) {
-        const uint32_t st = g_issue % pl.nstage;
-        const uint32_t use = g_issue / pl.nstage;
-        ++g_issue;
-        if (use >= 1) mbar_wait(&bar_empty[st], (use - 1) & 1u, tmo, p.err, s_abort);
-        const int v0 = k * R, v1 = min(V, v0 + R);
-        if (aborted()) {
-          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], 0);
-        } else {
-          // the stage's bytes are expected up front; the shared expert's
-          // segment goes out at once, routed segments once ids are known
-          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((v1 - v0) * lay.gu_row));
-          __syncwarp();
-          uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
-          for (int v = v0; v < v1;) {           // copies of at most kFusedRowsPerCopy rows of one slot
-            const int ps = v / nr, r = v % nr;
-            const int cnt = min(min(v1 - v, nr - r), kFusedRowsPerCopy);
-            ensure_routed(ps);
-            if (!aborted())
-              copy(buf + (size_t)(v - v0) * lay.gu_row, slot_blob(ps) + (size_t)(ra + r) * lay.gu_row,
-                   (uint32_t)(cnt * lay.gu_row), &bar_full[st]);
-            v += cnt;
-          }
-        }
-        // down records of slots whose gate/up is dlag slots behind
-        const int slots_issued = v1 / nr;
-        while (dnext < slots_issued - dlag) issue_down(dnext++);
-      }
-      while (dnext < NS) issue_down(dnext++);
-      __syncwarp();
-    } else if (warp == kFinalWarp) {
-      // ------------------------------------------------------------------
-      // finaliser: h = silu(gate . x) * (up . x) for this block's rows, to L2
-      // ------------------------------------------------------------------
-      for (int ps = 0; ps < NS; ++ps) {
-        mbar_wait(&bar_slot[ps], lpar, tmo, p.err, s_abort);
-        float* hdst = p.hmid + (size_t)hidx(ps) * I + ra;
-        unsigned long long* hll = p.hll + (size_t)hidx(ps) * I + ra;
-        const float* part = s_part + (size_t)ps * pl.nrmax * nparts * 2;
-        for (int r = lane; r < nr; r += 32) {
-          float a = 0.f, u = 0.f;
-          for (int q = 0; q < nparts; ++q) {
-            a += part[(r * nparts + q) * 2];
-            u += part[(r * nparts + q) * 2 + 1];
-          }
-          const float hv = silu_f(a) * u;
-          ll_store(hll + r, hv, tag);
-          if (l == p.L - 1) hdst[r] = hv;
-        }
-      }
-    } else if (warp == kExchangeWarp || warp == kExchangeWarp2) {
-      // ------------------------------------------------------------------
-      // exchangers: each slot's full h from L2 into shared memory, the first
-      // exchanger taking even slots, the second odd; the second also routes
-      // ------------------------------------------------------------------
-      const int xw = warp - kExchangeWarp;
-      if (xw == kRouteXw) {
-        // the layer's top-K: computed at the end of the previous layer (the
-        // logits are inputs), or now for the first layer of the launch
-        if (l == 0) warp_topk(p.logits, p.E, p.K, nx_id, nx_l);
-        const int my_id = nx_id;
-        const float my_w = warp_topk_softmax(nx_l, p.K);
-        // publish once the consumers hold the whole layer input
-        mbar_wait(bar_xready, lpar, tmo, p.err, s_abort);
-        if (lane < p.K) {
-          s_ids[p.S + lane] = my_id;
-          s_w[p.S + lane] = my_w;
-          if (c == 0 && p.ids_out != nullptr) {
-            p.ids_out[(size_t)l * p.K + lane] = my_id;
-            p.w_out[(size_t)l * p.K + lane] = my_w;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_routed[0]);
-      }
-      unsigned long long* my_stage = s_stage + (size_t)xw * I;
-      for (int q = xw; q < NS; q += 2) {
-        const unsigned long long* hsrc = p.hll + (size_t)hidx(q) * I;
-        float* hsf = reinterpret_cast<float*>(s_hs + (size_t)q * pl.hs_slot_bytes);
-#if FMOE_XCHG_WAIT_OWN
-        // the other blocks finish a slot at about the time this one does:
-        // polling earlier only returns stale words one round trip later
-        mbar_wait(&bar_slot[q], lpar, tmo, p.err, s_abort);
-#endif
-        // fetch all I words of the slot, then re-fetch until every tag is current
-        uint64_t t0 = 0;
-        bool started = false;
-        while (true) {
-          for (int c2 = lane; c2 < I / 2; c2 += 32) cp_async16(my_stage + 2 * c2, hsrc + 2 * c2);
-          cp_async_wait_all();
-          __syncwarp();
-          bool ok = true;
-          for (int i = lane; i < I; i += 32) ok = ok && ll_is(my_stage[i], tag);
-          if (__all_sync(0xFFFFFFFFu, ok)) break;
-          if (*s_abort) break;
-          const uint64_t t = global_timer_ns();
-          if (!started) {
-            t0 = t;
-            started = true;
-          } else if (t - t0 > tmo) {
-            atomicOr(p.err, kErrWaitTimeout);
-            *s_abort = 1;
-            break;
-          }
-          __nanosleep(kExchangePollNs);
-        }
-        // pre-scale into the padded slice-major layout; lane = position in the
-        // slice, so that the reads are consecutive and the stores hit 32 banks
-        const float ps_l = pos_scale<BITS>(lane);
-        const int fo = ((lane >> 2) * hstride) * 4 + (lane & 3);
-#pragma unroll 8
-        for (int m = 0; m < tld; ++m) hsf[fo + m * 4] = ll_value(my_stage[(size_t)m * kSlice + lane]) * ps_l;
-        __threadfence_block();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_hready[q]);
-      }
-      // the next layer's top-K, off its critical path; its ids are published
-      // only once that layer's input is complete
-      if (xw == kRouteXw && l + 1 < p.L) warp_topk(p.logits + (size_t)(l + 1) * p.E, p.E, p.K, nx_id, nx_l);
-    } else {
-      // ------------------------------------------------------------------
-      // consumers: 12 gate/up warps and 4 down warps
-      // ------------------------------------------------------------------
-      float rinv;
-      {
-        // The layer input goes through shared memory, slice-major (float4 j of
-        // slice s at j*tl + s), so that each lane then reads its slice without
-        // bank conflicts.  Every consumer thread fetches 8 consecutive elements
-        // (plain, or published words of the previous layer) and adds up their
-        // squares and their products with the shared-expert gate vector.
-        float ss = 0.f, wg = 0.f;
-        for (int e = tid * 8; e < H; e += kConsumerWarps * 32 * 8) {
-          float4 v0, v1;
-          if (in_ll) {
-            ll_wait8(hin_ll + e, tag - 1u, v0, v1, tmo, p.err, s_abort);
-          } else {
-            const float4* src = reinterpret_cast<const float4*>(hin + e);
-            v0 = p.norm ? __ldcg(src) : __ldg(src);
-            v1 = p.norm ? __ldcg(src + 1) : __ldg(src + 1);
-          }
-          s_x4[((e & 31) >> 2) * tl + (e >> 5)] = v0;
-          s_x4[(((e + 4) & 31) >> 2) * tl + (e >> 5)] = v1;
-          ss += (v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w);
-          ss += (v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w);
-          if (p.S) {
-            const uint4 wb = __ldg(reinterpret_cast<const uint4*>(lp.wsg + e));
-            wg += (bf16lo(wb.x) * v0.x + bf16hi(wb.x) * v0.y) + (bf16lo(wb.y) * v0.z + bf16hi(wb.y) * v0.w);
-            wg += (bf16lo(wb.z) * v1.x + bf16hi(wb.z) * v1.y) + (bf16lo(wb.w) * v1.z + bf16hi(wb.w) * v1.w);
-          }
-        }
-        ss = warp_sum(ss);
-        wg = warp_sum(wg);
+      float ss = 0.f, wg = 0.f;
+      if (l > 0 && warp * 256 < H) {
+        // one lane waits for the warp's first words before every lane polls
+        // its own: the accumulators are not read over and over while the
+        // blocks' additions are still landing
         if (lane == 0) {
-          s_red[2 * warp] = ss;
-          s_red[2 * warp + 1] = wg;
+          float sm[8];
+          poll8(acc_prev + warp * 256, n, sm, tmo, p.err, s_abort);
         }
-        consumer_sync();
-        float tot = 0.f, wgt = 0.f;
-#pragma unroll
-        for (int q = 0; q < kConsumerWarps; ++q) {
-          tot += s_red[2 * q];
-          wgt += s_red[2 * q + 1];
+        __syncwarp();
+      }
+      for (int e = tid * 8; e < H; e += kPollWarps * 32 * 8) {
+        const int q0 = xs_pos4(e, tl), q1 = xs_pos4(e + 4, tl);
+        float4 v0, v1;
+        if (l == 0) {
+          const float4* src = reinterpret_cast<const float4*>((p.norm ? p.out : p.x) + e);
+          v0 = __ldcg(src);
+          v1 = __ldcg(src + 1);
+        } else {
+          float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          poll8(acc_prev + e, n, sm, tmo, p.err, s_abort);
+          v0 = s_x4[q0];
+          v1 = s_x4[q1];
+          v0.x += sm[0]; v0.y += sm[1]; v0.z += sm[2]; v0.w += sm[3];
+          v1.x += sm[4]; v1.y += sm[5]; v1.z += sm[6]; v1.w += sm[7];
         }
-        rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
-        if (warp == 0 && lane == 0) {
-          const float gate = p.S ? sigmoid_f(wgt * rinv) : 0.f;
-          if (p.S) s_w[0] = gate;
-          if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
-          mbar_arrive(bar_xready);
+        s_x4[q0] = v0;
+        s_x4[q1] = v1;
+        ss += (v0.x * v0.x + v0.y * v0.y) + (v0.z * v0.z + v0.w * v0.w);
+        ss += (v1.x * v1.x + v1.y * v1.y) + (v1.z * v1.z + v1.w * v1.w);
+        if (p.S) {
+          const uint4 wb = __ldg(reinterpret_cast<const uint4*>(lp.wsg + e));
+          wg += (bf16lo(wb.x) * v0.x + bf16hi(wb.x) * v0.y) + (bf16lo(wb.y) * v0.z + bf16hi(wb.y) * v0.w);
+          wg += (bf16lo(wb.z) * v1.x + bf16hi(wb.z) * v1.y) + (bf16lo(wb.w) * v1.z + bf16hi(wb.w) * v1.w);
         }
       }
+      // every block's contributions to the previous sum were observed:
+      // order them before this block's next clear and its next additions
+      if (l > 0) fence_acq_rel_gpu();
+      ss = warp_sum(ss);
+      wg = warp_sum(wg);
+      if (lane == 0) {
+        s_red[2 * warp] = ss;
+        s_red[2 * warp + 1] = wg;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_x);
 
       if (warp < kGuWarps) {
         // ---------------- gate/up: stream the ring, partial sums to smem ----
+        int rs0, sl, pi;
+        if (tl >= 32) {
+          rs0 = warp < (R / 2) * nparts ? warp / nparts : R;   // warps beyond a whole pass stay idle
+          pi = warp % nparts;
+          sl = pi * 32 + lane;
+        } else {
+          rs0 = warp * (32 / tl) + lane / tl;
+          pi = 0;
+          sl = lane % tl;
+        }
+        const int rs1 = rs0 + R / 2;
+        mbar_wait(bar_x, lpar, tmo, p.err, s_abort);
+        float tot = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < kPollWarps; ++q) tot += s_red[2 * q];
+        const float rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
         SliceX xs;
         float xsum = 0.f;
 #pragma unroll
@@ -513,21 +342,14 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           const float4 v = s_x4[j * tl + sl];
           xsum += put_x4<BITS>(xs, j, make_float4(v.x * rinv, v.y * rinv, v.z * rinv, v.w * rinv));
         }
-        int next_done = 0;
-        if (nr == 0) {               // no gate/up rows here: every slot is complete at once
-          __syncwarp();
-          if (lane == 0)
-            for (int ps = 0; ps < NS; ++ps) mbar_arrive(&bar_slot[ps]);
-          next_done = NS;
-        }
         for (int k = 0; k < nstg; ++k) {
           const uint32_t st = g_cons % pl.nstage;
           mbar_wait(&bar_full[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
           ++g_cons;
           const uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
-          const int v0 = k * R + rs0, v1 = k * R + rs1;
+          const int u0 = k * R + rs0, u1 = k * R + rs1;
           float ga0 = 0.f, ua0 = 0.f, ga1 = 0.f, ua1 = 0.f;
-          if (rs0 < R / 2 && v0 < V) {
+          if (rs0 < R / 2 && u0 < len) {
             const uint8_t* rec = buf + (size_t)rs0 * lay.gu_row;
             SliceCodes<BITS> qg, qu;
             if constexpr (BITS == 4) {
@@ -542,7 +364,7 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
             ga0 = slice_term<BITS>(qg, sg, xs, xsum);
             ua0 = slice_term<BITS>(qu, su, xs, xsum);
           }
-          if (rs0 < R / 2 && v1 < V) {
+          if (rs0 < R / 2 && u1 < len) {
             const uint8_t* rec = buf + (size_t)rs1 * lay.gu_row;
             SliceCodes<BITS> qg, qu;
             if constexpr (BITS == 4) {
@@ -559,159 +381,307 @@ __global__ void __maxnreg__(kFusedMaxRegs) fused_moe_kernel(const __grid_constan
           }
           const float v = quad_reduce(ga0, ua0, ga1, ua1, gw, lane);
           const int pos = lane & (gw - 1), qw = gw >> 2;
-          const int vv = pos < 2 * qw ? v0 : v1;
-          if (rs0 < R / 2 && vv < V && (pos & (qw - 1)) == 0) {
-            const int ps = vv / nr, r = vv % nr;
-            s_part[(((size_t)ps * pl.nrmax + r) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
-          }
+          const int rsel = pos < 2 * qw ? rs0 : rs1;
+          if (rs0 < R / 2 && k * R + rsel < len && (pos & (qw - 1)) == 0)
+            s_part[(((size_t)st * R + rsel) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_empty[st]);
-          // slots whose last row was in this stage are complete
-          const int last_v = min(V, (k + 1) * R);
-          bool fenced = false;
-          while (next_done < NS && (next_done + 1) * nr <= last_v) {
-            if (!fenced) {
-              __threadfence_block();
-              __syncwarp();
-              fenced = true;
-            }
-            if (lane == 0) mbar_arrive(&bar_slot[next_done]);
-            ++next_done;
+          if (lane == 0) {
+            mbar_arrive(&bar_gudone[st]);
+            mbar_arrive(&bar_empty[st]);
           }
         }
-        if (ntail > 0) {
-          // the last slots' down rows: by the time their h is gathered the
-          // gate/up warps are idle, and twelve warps finish a slot sooner
-          // than the four down warps, whose every instruction waits on the
-          // one before it
-          float tacc[kMaxTailGroups];
+      } else {
+        // ---------------- down: owned columns, in order, into per-row sums ----
+        const int dt = tid - kGuWarps * 32;
+        const int W = H / RW;                                  // code words per column
+        float outp[MW * RW];
 #pragma unroll
-          for (int gi = 0; gi < kMaxTailGroups; ++gi) tacc[gi] = 0.f;
-          for (int ps = NS - ntail; ps < NS; ++ps) {
-            mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
-            mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
-            const float wk = s_w[ps];
-            const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
-            const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
-            for (int k = 0; k < spl; ++k) {
-              const int s = (lane % lpr) + 32 * k;
-              SliceX hs;
-              const float hsm = staged_h_slice<BITS>(hs4, hstride, s, hs);
+        for (int r = 0; r < MW * RW; ++r) outp[r] = 0.f;
+        // this block's clear of the next accumulator, before this thread adds
+        mbar_wait(bar_zero, lpar, tmo, p.err, s_abort);
+        fence_acq_rel_gpu();
+        mbar_wait(bar_dfull, lpar, tmo, p.err, s_abort);
+        const uint32_t hd_base = (uint32_t)l * (uint32_t)nstg;
+        int seen = 0;                                          // stages of this layer known finalised
+        for (int pidx = 0; pidx < np; ++pidx) {
+          const Piece pc = s_pc[pidx];
+          const uint8_t* cbase = darea + pc.col_off;
+          for (int gi = 0; gi < pc.ng; ++gi) {
+            const int g = pc.g0 + gi;
+            const int ia = max(pc.i0, g * kGroup), ib = min(pc.i0 + pc.cnt, g * kGroup + kGroup);
+            float2 acc[MW][RW / 2];
 #pragma unroll
-              for (int gi = 0; gi < kMaxTailGroups; ++gi) {
-                const int grp = warp + kGuWarps * gi;
-                const int r = grp * rpp + lane / lpr;
-                if (grp < ngroups && r < nd)
-                  tacc[gi] = down_slice<BITS>(buf + (size_t)r * lay.d_row, lay, s, hs, hsm, wk, tacc[gi]);
+            for (int j = 0; j < MW; ++j)
+#pragma unroll
+              for (int t = 0; t < RW / 2; ++t) acc[j][t] = make_float2(0.f, 0.f);
+            float hs = 0.f;
+            for (int i = ia; i < ib; ++i) {
+              const int u = pc.loc + (i - pc.i0);
+              while (seen * R <= u) {
+                wait_count(s_hdone, hd_base + (uint32_t)seen + 1u, tmo, p.err, s_abort);
+                ++seen;
+              }
+              const float4* hp4 = reinterpret_cast<const float4*>(s_hb + (size_t)u * hb);
+              float2 hv[NV / 2];
+              {
+                const float4 a = hp4[0];
+                hv[0] = make_float2(a.x, a.y);
+                hv[1] = make_float2(a.z, a.w);
+                if constexpr (BITS == 2) {
+                  const float4 b = hp4[1];
+                  hv[2] = make_float2(b.x, b.y);
+                  hv[3] = make_float2(b.z, b.w);
+                }
+              }
+              hs += s_hb[(size_t)u * hb + NV];
+              const uint32_t* col = reinterpret_cast<const uint32_t*>(cbase + (size_t)(i - pc.i0) * lay.dcol);
+#pragma unroll
+              for (int j = 0; j < MW; ++j) {
+                const int m = dt + kDnThreads * j;
+                if (m < W) down_word<BITS>(col[m], hv, acc[j]);
+              }
+            }
+            // the group's scale and bias per row (RW consecutive words per code word)
+            const uint4* sbw =
+                reinterpret_cast<const uint4*>(darea + pc.sb_off + (size_t)gi * lay.dsb_group);
+#pragma unroll
+            for (int j = 0; j < MW; ++j) {
+              const int m = dt + kDnThreads * j;
+              if (m < W) {
+#pragma unroll
+                for (int t4 = 0; t4 < RW / 4; ++t4) {
+                  const uint4 s4 = sbw[m * (RW / 4) + t4];
+                  const float2 a01 = acc[j][2 * t4], a23 = acc[j][2 * t4 + 1];
+                  float* o = outp + j * RW + 4 * t4;
+                  o[0] += fmaf(bf16lo(s4.x) * 18446744073709551616.0f, a01.x, bf16hi(s4.x) * hs);
+                  o[1] += fmaf(bf16lo(s4.y) * 18446744073709551616.0f, a01.y, bf16hi(s4.y) * hs);
+                  o[2] += fmaf(bf16lo(s4.z) * 18446744073709551616.0f, a23.x, bf16hi(s4.z) * hs);
+                  o[3] += fmaf(bf16lo(s4.w) * 18446744073709551616.0f, a23.y, bf16hi(s4.w) * hs);
+                }
               }
             }
           }
+        }
+        // every down thread is done with the down area: reuse it to turn the
+        // per-thread rows into row order, then add them (coalesced) into
+        // this layer's accumulator
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_dsync[0]);
+        mbar_wait(&bar_dsync[0], lpar, tmo, p.err, s_abort);
+        float* tb = reinterpret_cast<float*>(darea);
 #pragma unroll
-          for (int gi = 0; gi < kMaxTailGroups; ++gi) {
-            const int grp = warp + kGuWarps * gi;
-            const float v = warp_sum(tacc[gi], lpr);
-            const int r = grp * rpp + lane / lpr;
-            if (grp < ngroups && r < nd && (lane % lpr) == 0) s_tail[r] = v;
+        for (int j = 0; j < MW; ++j) {
+          const int m = dt + kDnThreads * j;
+          if (m < W) {
+#pragma unroll
+            for (int t = 0; t < RW; t += 4)
+              *reinterpret_cast<float4*>(tb + m * RW + t) =
+                  make_float4(outp[j * RW + t], outp[j * RW + t + 1], outp[j * RW + t + 2], outp[j * RW + t + 3]);
           }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_dsync[1]);
+        mbar_wait(&bar_dsync[1], lpar, tmo, p.err, s_abort);
+        if (!*s_abort)
+          for (int r = dt; r < H; r += kDnThreads) red_add_u64(acc_cur + r, fix_word(tb[r], p.err));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ddone);
+      }
+    } else if (warp == kProducerWarp) {
+      // ------------------------------------------------------------------
+      // producer: the layer's copies in consumption order; lane 0 declares
+      // each barrier's bytes, successive copies are issued by successive
+      // lanes (the copies one thread issues are carried out one after
+      // another, those of different threads side by side)
+      // ------------------------------------------------------------------
+      auto aborted = [&]() -> bool { return __shfl_sync(0xFFFFFFFFu, *s_abort, 0) != 0; };
+      bool routed = false;       // routed ids are published all at once
+      auto ensure_routed = [&](int slot) {
+        if (slot >= p.S && !routed) {
+          mbar_wait(bar_routed, lpar, tmo, p.err, s_abort);
+          routed = true;
+        }
+      };
+      auto slot_blob = [&](int slot) -> const uint8_t* {
+        if (p.S && slot == 0) return lp.shared;
+        return lp.experts + (size_t)s_ids[slot] * p.blob;
+      };
+      auto copy = [&](uint8_t* dst, const uint8_t* src, uint32_t bytes, uint64_t* bar) {
+        for (uint32_t off = 0; off < bytes; off += kFusedCopyBytes) {
+          const uint32_t b = bytes - off < kFusedCopyBytes ? bytes - off : kFusedCopyBytes;
+          if (lane == (int)(n_copies % kFusedIssueLanes)) bulk_g2s(dst + off, src + off, b, bar);
+          ++n_copies;
+        }
+      };
+      auto issue_darea = [&]() {
+        // the previous layer's down work is done with the area
+        if (l > 0) mbar_wait(bar_ddone, (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
+        uint32_t total = 0;
+        for (int q = 0; q < np; ++q) total += (uint32_t)(s_pc[q].cnt * lay.dcol + s_pc[q].ng * lay.dsb_group);
+        if (aborted()) {
+          if (lane == 0) mbar_arrive_expect_tx(bar_dfull, 0);
+          return;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar_dfull, total);
+        __syncwarp();
+        for (int q = 0; q < np; ++q) {
+          const Piece pc = s_pc[q];
+          ensure_routed(pc.slot);
+          if (aborted()) continue;
+          const uint8_t* b = slot_blob(pc.slot);
+          copy(darea + pc.col_off, b + lay.dq_off + (size_t)pc.i0 * lay.dcol, (uint32_t)(pc.cnt * lay.dcol),
+               bar_dfull);
+          copy(darea + pc.sb_off, b + lay.dsb_off + (size_t)pc.g0 * lay.dsb_group,
+               (uint32_t)(pc.ng * lay.dsb_group), bar_dfull);
+        }
+      };
+      bool darea_issued = false;
+      for (int k = 0; k < nstg; ++k) {
+        const uint32_t st = g_issue % pl.nstage;
+        const uint32_t use = g_issue / pl.nstage;
+        ++g_issue;
+        if (use >= 1) mbar_wait(&bar_empty[st], (use - 1) & 1u, tmo, p.err, s_abort);
+        const int a0 = k * R, a1 = min(len, a0 + R);
+        if (aborted()) {
+          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], 0);
+        } else {
+          if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], (uint32_t)((a1 - a0) * lay.gu_row));
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tail);
-        }
-      } else {
-        // ---------------- down projection + combine + residual -------------
-        const int dw = warp - kGuWarps;
-        float acc[kMaxDownGroups];
-        float resv[kMaxDownGroups];
-#pragma unroll
-        for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-          const int grp = dw + kDownWarps * gi;
-          const int r = grp * rpp + lane / lpr;
-          acc[gi] = 0.f;
-          resv[gi] = 0.f;
-          if (grp < ngroups && r < nd && (lane % lpr) == 0) {
-            if (p.norm) {
-              const int e = ja + r;
-              resv[gi] = reinterpret_cast<const float*>(s_x4)[(((e & 31) >> 2) * tl + (e >> 5)) * 4 + (e & 3)];
-            } else {
-              resv[gi] = __ldg(p.residual + ja + r);
-            }
+          uint8_t* buf = ring + (size_t)st * pl.stage_bytes;
+          for (int q = 0; q < np; ++q) {
+            const Piece pc = s_pc[q];
+            const int b0 = max(a0, pc.loc), b1 = min(a1, pc.loc + pc.cnt);
+            if (b0 >= b1) continue;
+            ensure_routed(pc.slot);
+            if (aborted()) continue;
+            copy(buf + (size_t)(b0 - a0) * lay.gu_row, slot_blob(pc.slot) + (size_t)(pc.i0 + b0 - pc.loc) * lay.gu_row,
+                 (uint32_t)((b1 - b0) * lay.gu_row), &bar_full[st]);
           }
         }
-        for (int ps = 0; ps < NS - ntail; ++ps) {
-          mbar_wait(&bar_hready[ps], lpar, tmo, p.err, s_abort);
-          mbar_wait(&bar_dfull[ps], lpar, tmo, p.err, s_abort);
-          const float wk = s_w[ps];
-          const float4* hs4 = reinterpret_cast<const float4*>(s_hs + (size_t)ps * pl.hs_slot_bytes);
-          const uint8_t* buf = darea + (size_t)ps * pl.dslot_bytes;
-          for (int k = 0; k < spl; ++k) {
-            const int s = (lane % lpr) + 32 * k;
-            SliceX hs;
-            const float hsm = staged_h_slice<BITS>(hs4, hstride, s, hs);
-#pragma unroll
-            for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-              const int grp = dw + kDownWarps * gi;
-              const int r = grp * rpp + lane / lpr;
-              if (grp < ngroups && r < nd)
-                acc[gi] = down_slice<BITS>(buf + (size_t)r * lay.d_row, lay, s, hs, hsm, wk, acc[gi]);
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_ddone[ps]);
-        }
-        if (ntail > 0) {
-          // the tail slots' rows were done by the gate/up warps
-          mbar_wait(bar_tail, lpar, tmo, p.err, s_abort);
-          __syncwarp();
-          if (lane == 0)
-            for (int ps = NS - ntail; ps < NS; ++ps) mbar_arrive(&bar_ddone[ps]);
-        }
-        // combine + residual, written by each row's owner
-#pragma unroll
-        for (int gi = 0; gi < kMaxDownGroups; ++gi) {
-          const int grp = dw + kDownWarps * gi;
-          const float v = warp_sum(acc[gi], lpr);
-          const int r = grp * rpp + lane / lpr;
-          if (grp < ngroups && r < nd && (lane % lpr) == 0) {
-            const float o = resv[gi] + v + (ntail > 0 ? s_tail[r] : 0.f);
-            if (out_ll) ll_store(out_llp + ja + r, o, tag);
-            else p.out[ja + r] = o;
-          }
+        if (!darea_issued && (k + 1 >= kFusedDareaAfter || k + 1 >= pl.nstage)) {
+          issue_darea();
+          darea_issued = true;
         }
       }
-    }
-
-    // ---- end of layer: every role but the producer is done with this
-    // layer's shared memory.  The producer runs on into the next layer: the
-    // ring's stages come back to it through bar_empty and the down areas
-    // through bar_ddone, so it may request the next layer's shared expert
-    // while this layer's down projection finishes.
-    if (warp != kProducerWarp) {
+      if (!darea_issued) issue_darea();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_layer);
-      mbar_wait(bar_layer, lpar, tmo, p.err, s_abort);
+    } else {
+      // ------------------------------------------------------------------
+      // finaliser: routing, the accumulator clear, h of each stage
+      // ------------------------------------------------------------------
+      if (l == 0) warp_topk(p.logits, p.E, p.K, nx_id, nx_l);
+      const int my_id = nx_id;
+      const float my_w = warp_topk_softmax(nx_l, p.K);
+      mbar_wait(bar_x, lpar, tmo, p.err, s_abort);
+      float tot = 0.f, wgt = 0.f;
+#pragma unroll 4
+      for (int q = 0; q < kPollWarps; ++q) {
+        tot += s_red[2 * q];
+        wgt += s_red[2 * q + 1];
+      }
+      const float rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
+      const float gate = p.S ? sigmoid_f(wgt * rinv) : 0.f;
+      if (lane < p.K) {
+        s_ids[p.S + lane] = my_id;
+        s_w[p.S + lane] = my_w;
+        if (c == 0 && p.ids_out != nullptr) {
+          p.ids_out[(size_t)l * p.K + lane] = my_id;
+          p.w_out[(size_t)l * p.K + lane] = my_w;
+        }
+      }
+      if (lane == 0) {
+        if (p.S) s_w[0] = gate;
+        if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_routed);
+      // clear this block's slice of the next layer's accumulator (its last
+      // readers finished before this layer's input was complete)
+      for (int r = lane; r < nd; r += 32) acc_next[ja + r] = 0ull;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_zero);
+      const bool last = (l == p.L - 1) && p.hmid != nullptr;
+      for (int k = 0; k < nstg; ++k) {
+        const uint32_t st = g_cons % pl.nstage;
+        mbar_wait(&bar_gudone[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
+        ++g_cons;
+        const int nrec = min(R, len - k * R);
+        for (int r = lane; r < nrec; r += 32) {
+          const int u = k * R + r;
+          int q = 0;
+          while (q + 1 < np && u >= s_pc[q + 1].loc) ++q;
+          const int slot = s_pc[q].slot, i = s_pc[q].i0 + (u - s_pc[q].loc);
+          const float* part = s_part + ((size_t)st * R + r) * nparts * 2;
+          float a = 0.f, uu = 0.f;
+          for (int t = 0; t < nparts; ++t) {
+            a += part[2 * t];
+            uu += part[2 * t + 1];
+          }
+          const float hv = silu_f(a) * uu;
+          const float hw = s_w[slot] * hv;
+          float* dst = s_hb + (size_t)u * hb;
+#pragma unroll
+          for (int t = 0; t < NV; ++t) dst[t] = hw * pos_scale<BITS>(t);
+          dst[NV] = hw;
+          if (last) p.hmid[(size_t)slot_h(slot) * I + i] = hv;
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar_empty[st]);
+          st_release_shared(s_hdone, (uint32_t)l * (uint32_t)nstg + (uint32_t)k + 1u);
+        }
+      }
+      // the next layer's top-K, off its critical path; its ids are published
+      // only once that layer's input is complete
+      if (l + 1 < p.L) warp_topk(p.logits + (size_t)(l + 1) * p.E, p.E, p.K, nx_id, nx_l);
+    }
+  }
+
+  // ---- the last layer's output: this block's chunks of 8 outputs ----
+  if (warp < kPollWarps) {
+    const unsigned long long* acc_last = p.acc + (size_t)((lb + p.L - 1) % 3) * H;
+    for (int q = c + n * tid; q < H / 8; q += n * kPollWarps * 32) {
+      const int e = q * 8;
+      float sm[8];
+      if (!poll8(acc_last + e, n, sm, tmo, p.err, s_abort)) break;
+      float4 b0, b1;
+      if (p.norm) {
+        b0 = s_x4[xs_pos4(e, tl)];
+        b1 = s_x4[xs_pos4(e + 4, tl)];
+      } else {
+        b0 = __ldg(reinterpret_cast<const float4*>(p.residual + e));
+        b1 = __ldg(reinterpret_cast<const float4*>(p.residual + e) + 1);
+      }
+      float4* o = reinterpret_cast<float4*>(p.out + e);
+      o[0] = make_float4(b0.x + sm[0], b0.y + sm[1], b0.z + sm[2], b0.w + sm[3]);
+      o[1] = make_float4(b1.x + sm[4], b1.y + sm[5], b1.z + sm[6], b1.w + sm[7]);
     }
   }
 
   // No copy may still be writing this block's shared memory when it exits:
   // wait (bounded, whether or not the block gave up) for the last phase of
-  // every stage and down area that was used.
+  // every stage and of the down area.
   if (warp == kProducerWarp && lane == 0) {
     volatile int no_abort = 0;
     const uint32_t used = g_issue < (uint32_t)pl.nstage ? g_issue : (uint32_t)pl.nstage;
     for (uint32_t st = 0; st < used; ++st) {
-      const uint32_t last = g_issue - 1 - ((g_issue - 1 - st) % pl.nstage);   // last issue index of stage st
-      mbar_wait(&bar_full[st], (last / pl.nstage) & 1u, tmo, p.err, &no_abort);
+      const uint32_t lastu = g_issue - 1 - ((g_issue - 1 - st) % pl.nstage);   // last issue index of stage st
+      mbar_wait(&bar_full[st], (lastu / pl.nstage) & 1u, tmo, p.err, &no_abort);
     }
-    for (int ps = 0; ps < NS; ++ps) mbar_wait(&bar_dfull[ps], (uint32_t)((p.L - 1) & 1), tmo, p.err, &no_abort);
+    mbar_wait(bar_dfull, (uint32_t)((p.L - 1) & 1), tmo, p.err, &no_abort);
   }
 
-  // the last block out starts the next epoch of tags and resets the exit count
-  cta_sync();
+  // the last block out advances the layer count and resets the exit count
+  __syncwarp();
+  __syncthreads();
   if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(p.exit_ctr, 1u);
     if (old == (uint32_t)n - 1) {
       *p.exit_ctr = 0;
-      atomicAdd(p.epoch, 1u);
+      *p.lbase = (lb + (uint32_t)p.L) % 3u;
       __threadfence();
     }
   }
@@ -738,74 +708,79 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device) {
 FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem_max) {
   FusedPlan pl{};
   pl.ok = false;
-  const int tl = H / kSlice, tld = I / kSlice;
-  if (H % kSlice || I % kSlice || !pow2(tl) || !pow2(tld)) return pl;
-  if (tl < 4 || tl > 32 * kConsumerWarps || tld < 1) return pl;
-  if (K + S > kMaxSlots || K < 1 || sms < 1) return pl;
-  const int grid = sms;
+  if (bits != 4 && bits != 2) return pl;
+  const int tl = H / kSlice;
+  if (H % 64 || I % 64 || !pow2(tl) || tl < 4) return pl;
+  if (K < 1 || K + S > kMaxSlots || sms < 1 || sms > kFixMaxContrib) return pl;
   const int NS = K + S;
+  const int grid = sms;
   const BlobLayout lay = blob_layout(bits, H, I);
-  // gate/up stage: two rows per consumer warp and slice range
+  // a down thread holds at most 4 (4-bit) or 2 (2-bit) code words of a column
+  if (H / (32 / bits) > kDnThreads * (bits == 4 ? 4 : 2)) return pl;
   const int nparts = tl >= 32 ? tl / 32 : 1;
   if (nparts > kGuWarps) return pl;
   const int R = 2 * (tl >= 32 ? kGuWarps / nparts : kGuWarps * (32 / tl));
-  pl.rows_per_stage = R;
+  pl.R = R;
   pl.nparts = nparts;
   pl.stage_bytes = round_up_i((long long)R * lay.gu_row, 128);
-  // down records of one slot
-  const int ndmax = (H + grid - 1) / grid;
-  const int lpr = tld < 32 ? tld : 32, rpp = 32 / lpr;
-  if ((ndmax + rpp - 1) / rpp > kMaxDownGroups * kDownWarps) return pl;
-  if ((ndmax + rpp - 1) / rpp > kMaxTailGroups * kGuWarps || ndmax > kMaxTailRows) return pl;
-  pl.dslot_bytes = round_up_i((long long)ndmax * lay.d_row, 128);
-  pl.nrmax = (I + grid - 1) / grid;
-  pl.hs_slot_bytes = round_up_i((long long)8 * (tld + 1) * 16, 128);
-  pl.part_off = kCtrlBytes;
-  pl.stage_off = round_up_i(pl.part_off + (long long)NS * pl.nrmax * nparts * 2 * 4, 128);
-  pl.hs_off = round_up_i(pl.stage_off + (long long)2 * I * 8, 128);
-  // the layer input is staged where the slots' h will go: it is read by the
-  // consumers before their first gate/up stage, and the first h is written
-  // only after every block has finished a slot
-  pl.xs_off = pl.hs_off;
-  const long long hs_region = (long long)NS * pl.hs_slot_bytes > (long long)H * 4 ? (long long)NS * pl.hs_slot_bytes
-                                                                                  : (long long)H * 4;
-  pl.darea_off = round_up_i(pl.hs_off + hs_region, 128);
-  pl.ring_off = pl.darea_off + NS * pl.dslot_bytes;
-  const long long avail = (long long)smem_max - pl.ring_off;
-  const long long ns = avail / pl.stage_bytes;
-  if (ns < 2) return pl;
-  pl.nstage = (int)(ns > kFusedStageCap ? kFusedStageCap : ns);
-  pl.smem = (size_t)pl.ring_off + (size_t)pl.nstage * pl.stage_bytes;
-  pl.dlag = kFusedDownLag;
-  pl.grid = grid;
-  pl.ok = true;
+  const long long V = (long long)NS * I;
+  pl.len_max = (int)((V + grid - 1) / grid);
+  int darea = 0;
+  for (int c = 0; c < grid; ++c) {
+    Piece pc[kMaxPieces];
+    int b = 0;
+    if (block_pieces(NS, I, c, grid, lay, pc, kMaxPieces, b) > kMaxPieces) return pl;
+    darea = b > darea ? b : darea;
+  }
+  pl.darea_bytes = round_up_i(darea > H * 4 ? darea : H * 4, 128);
+  pl.hb = bits == 4 ? 8 : 12;
+  pl.xs_off = kCtrlBytes;
+  pl.part_off = round_up_i(pl.xs_off + (long long)H * 4, 128);
+  for (int ns = kFusedStageCap; ns >= 2; --ns) {
+    pl.hbuf_off = round_up_i(pl.part_off + (long long)ns * R * nparts * 2 * 4, 128);
+    pl.darea_off = round_up_i(pl.hbuf_off + (long long)(pl.len_max + 1) * pl.hb * 4, 128);
+    pl.ring_off = pl.darea_off + pl.darea_bytes;
+    const long long need = (long long)pl.ring_off + (long long)ns * pl.stage_bytes;
+    if (need <= smem_max) {
+      pl.nstage = ns;
+      pl.smem = (size_t)need;
+      pl.grid = grid;
+      pl.ok = true;
+      return pl;
+    }
+  }
   return pl;
 }
 
-template <int BITS>
+template <int BITS, int MW>
 static cudaError_t launch_fused_t(FusedParams& p, const FusedPlan& pl, cudaStream_t st) {
   // the shared-memory limit and the residency check, once per device and size
   // (function attributes belong to the device's context)
+  static std::mutex mu;
   static int configured_smem[64];
   static size_t checked_smem[64];
+  auto kern = fused_moe_kernel<BITS, MW>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured_smem[dev] < (int)pl.smem) {
-    e = cudaFuncSetAttribute(fused_moe_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = (int)pl.smem;
-  }
-  if (checked_smem[dev] != pl.smem) {
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_moe_kernel<BITS>, kFusedThreads, pl.smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    checked_smem[dev] = pl.smem;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured_smem[dev] < (int)pl.smem) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+      if (e != cudaSuccess) return e;
+      configured_smem[dev] = (int)pl.smem;
+    }
+    if (checked_smem[dev] != pl.smem) {
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, pl.smem);
+      if (e != cudaSuccess) return e;
+      if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+      checked_smem[dev] = pl.smem;
+    }
   }
   // cooperative: all blocks resident at once (every block waits for words
-  // that the other blocks publish)
+  // that the other blocks add)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kFusedThreads);
@@ -816,12 +791,20 @@ static cudaError_t launch_fused_t(FusedParams& p, const FusedPlan& pl, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fused_moe_kernel<BITS>, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_fused(FusedParams& p, const FusedPlan& pl, cudaStream_t st) {
   p.plan = pl;
-  return p.bits == 4 ? launch_fused_t<4>(p, pl, st) : launch_fused_t<2>(p, pl, st);
+  const int words = p.H / (32 / p.bits);                     // code words per down column
+  const int mw = (words + kDnThreads - 1) / kDnThreads;
+  if (p.bits == 4) {
+    if (mw <= 1) return launch_fused_t<4, 1>(p, pl, st);
+    if (mw <= 2) return launch_fused_t<4, 2>(p, pl, st);
+    return launch_fused_t<4, 4>(p, pl, st);
+  }
+  if (mw <= 1) return launch_fused_t<2, 1>(p, pl, st);
+  return launch_fused_t<2, 2>(p, pl, st);
 }
 
 // ---------------------------------------------------------------------------

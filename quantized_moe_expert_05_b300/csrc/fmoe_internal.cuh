@@ -35,16 +35,18 @@ constexpr int kXScaleExp = 64;        // products carry a factor 2^-64
 constexpr uint32_t kErrWaitTimeout = 1u;   // a wait on words of other blocks (or a counter) ran out
 constexpr uint32_t kErrCopyTimeout = 2u;   // bulk-copy barrier wait ran out
 constexpr uint32_t kErrBadExpert = 4u;     // expert id outside [0, E)
+constexpr uint32_t kErrRange = 8u;         // a partial sum outside the fixed-point range (|v| > 2^19)
 
 // ---------------------------------------------------------------------------
 // blob layout (the library's own statement of the packed format)
 // ---------------------------------------------------------------------------
 struct BlobLayout {
   size_t qh, sh;     // bytes of one gate/up row's codes and of its (scale,bias) words
-  size_t qi, si;     // the same for one down row
   size_t gu_row;     // stride of gate/up row records [gate_q | up_q | gate_sb | up_sb], 16-byte padded
-  size_t d_off;      // offset of down row 0 (256-byte aligned)
-  size_t d_row;      // stride of down row records [down_q | down_sb], 16-byte padded
+  size_t dq_off;     // offset of down column 0 (256-byte aligned)
+  size_t dcol;       // bytes of one down column: H codes packed over rows (H*bits/8)
+  size_t dsb_off;    // offset of the down (scale,bias) words of group 0 (256-byte aligned)
+  size_t dsb_group;  // bytes of one group's down (scale,bias) words: one word per row (H*4)
   size_t bytes;      // blob size, a multiple of 256
 };
 
@@ -54,12 +56,12 @@ __host__ __device__ inline BlobLayout blob_layout(int bits, int H, int I) {
   BlobLayout L;
   L.qh = (size_t)H * bits / 8;
   L.sh = (size_t)H / kGroup * 4;
-  L.qi = (size_t)I * bits / 8;
-  L.si = (size_t)I / kGroup * 4;
   L.gu_row = round_up(2 * L.qh + 2 * L.sh, 16);
-  L.d_row = round_up(L.qi + L.si, 16);
-  L.d_off = round_up((size_t)I * L.gu_row, kPlaneAlign);
-  L.bytes = round_up(L.d_off + (size_t)H * L.d_row, kPlaneAlign);
+  L.dq_off = round_up((size_t)I * L.gu_row, kPlaneAlign);
+  L.dcol = (size_t)H * bits / 8;
+  L.dsb_off = round_up(L.dq_off + (size_t)I * L.dcol, kPlaneAlign);
+  L.dsb_group = (size_t)H * 4;
+  L.bytes = round_up(L.dsb_off + (size_t)(I / kGroup) * L.dsb_group, kPlaneAlign);
   return L;
 }
 
@@ -69,15 +71,16 @@ __host__ __device__ inline BlobLayout blob_layout(int bits, int H, int I) {
 struct WsLayout {
   size_t err;        // uint32 error word; the 256-byte header also holds:
   size_t exit_ctr;   //   uint32: blocks of the current launch that have finished
-  size_t epoch;      //   uint32: launches completed on this workspace (tags the exchanges)
-  size_t header_clear;  // bytes of the header a fresh call may zero (everything before `epoch`)
+  size_t lbase;      //   uint32: layers run on this workspace, modulo 3 (picks the accumulator)
+  size_t header_clear;  // bytes of the header a fresh call may zero (error word and exit count)
+  size_t acc;        // u64 [3][H]: fixed-point (sum, count) accumulators of the persistent kernel
+  size_t state;      // bytes at the start that are state kept between calls (header + acc)
   size_t ids;        // int32 [T][K]
   size_t weights;    // fp32 [T][K]
   size_t gate;       // fp32 [T]
   size_t h;          // fp32 [T][K+S][I]
-  size_t hll;        // u64 [K+S][I]: (value, tag) exchange of h between blocks
-  size_t hbufll;     // u64 [2][H]: (value, tag) layer outputs of a stack
   size_t y;          // fp32 [T][K+S][H] unweighted expert outputs (batched path)
+  size_t xn;         // fp32 [H] normalised layer input (general path of a stack)
   size_t plan;       // int32 batch plan: 8-word header + 8 words per item
   size_t plan_words;
   size_t bytes;
@@ -89,16 +92,17 @@ inline WsLayout ws_layout(int H, int I, int S, int T, int K, int L) {
   size_t pos = 0;
   w.err = 0;
   w.exit_ctr = 96;
-  w.epoch = 128;
+  w.lbase = 128;
   w.header_clear = 128;
   pos = 256;
+  w.acc = pos; pos = round_up(pos + (size_t)3 * H * 8, 256);
+  w.state = pos;
   w.ids = pos; pos = round_up(pos + (size_t)T * K * 4, 256);
   w.weights = pos; pos = round_up(pos + (size_t)T * K * 4, 256);
   w.gate = pos; pos = round_up(pos + (size_t)T * 4, 256);
   w.h = pos; pos = round_up(pos + (size_t)T * (K + S) * I * 4, 256);
-  w.hll = pos; pos = round_up(pos + (size_t)(K + S) * I * 8, 256);
-  w.hbufll = pos; pos = round_up(pos + (size_t)2 * H * 8, 256);
   w.y = pos; pos = round_up(pos + (size_t)T * (K + S) * H * 4, 256);
+  w.xn = pos; pos = round_up(pos + (size_t)H * 4, 256);
   // plan: header, then at most T*K + S*T items of 8 words (one token per
   // item at worst)
   w.plan_words = 8 + 8 * ((size_t)T * K + (size_t)S * T);
@@ -106,6 +110,21 @@ inline WsLayout ws_layout(int H, int I, int S, int T, int K, int L) {
   w.bytes = pos;
   return w;
 }
+
+// ---------------------------------------------------------------------------
+// fixed-point partial sums
+//
+// Partial output sums of different blocks are added with 64-bit integer
+// atomics, so the total does not depend on the order in which they arrive:
+// a word holds (sum of round(v * 2^28)) << 8 plus, in its low 8 bits, the
+// number of contributions (at most 255 contributors, so the count never
+// carries into the sum).  |v| <= 2^19 per contribution keeps the sum of 255
+// contributions inside the 56-bit signed field.
+// ---------------------------------------------------------------------------
+constexpr int kFixFrac = 28;
+constexpr float kFixMax = 524288.0f;   // 2^19
+constexpr int kFixCountBits = 8;
+constexpr int kFixMaxContrib = (1 << kFixCountBits) - 1;
 
 // ---------------------------------------------------------------------------
 // small device helpers
@@ -333,6 +352,27 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t targe
     }
     __nanosleep(64);
   }
+}
+
+// One contribution to a fixed-point accumulator word (see above); a value
+// outside the range is clamped and reported.
+__device__ __forceinline__ unsigned long long fix_word(float v, uint32_t* err) {
+  if (!(fabsf(v) <= kFixMax)) {     // also catches NaN
+    atomicOr(err, kErrRange);
+    v = (v != v) ? 0.f : copysignf(kFixMax, v);
+  }
+  const long long q = __float2ll_rn(v * (float)(1 << kFixFrac));
+  return ((unsigned long long)q << kFixCountBits) + 1ull;
+}
+
+__device__ __forceinline__ int fix_count(unsigned long long w) { return (int)(w & ((1u << kFixCountBits) - 1)); }
+
+__device__ __forceinline__ float fix_value(unsigned long long w) {
+  return __ll2float_rn((long long)w >> kFixCountBits) * (1.0f / (float)(1 << kFixFrac));
+}
+
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void signal_counter(uint32_t* ctr) {

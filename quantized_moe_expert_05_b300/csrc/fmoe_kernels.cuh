@@ -11,9 +11,9 @@ struct BatchGeom {
   int gu_warps;             // consumer warps with gate/up rows (2 rows each per unit)
   int gu_rows;              // intermediate rows per gate/up work unit (2 * gu_warps)
   int gu_nstage, gu_stage_bytes;
-  int d_nstage, d_stage_bytes;    // down: 4 rows per consumer warp per unit
-  int gu_xs_bytes, d_xs_bytes;    // staged inputs
-  size_t gu_smem, d_smem;
+  int gu_xs_bytes;                // staged inputs
+  int bd_h_bytes;                 // down: staged h of an item's tokens
+  size_t gu_smem, bd_smem;
   int grid;
 };
 
@@ -48,7 +48,13 @@ constexpr int kBatchConsumerWarps = 8;
 constexpr int kBatchProducerWarp = kBatchConsumerWarps;
 constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 1);
 constexpr int kBatchMaxStages = 8;
-constexpr int kDownRowsPerWarp = 4;
+// down kernel: warps that each own a range of columns, columns per ring
+// stage of a warp, stages per warp (cp.async groups in flight)
+constexpr int kBdWarps = 8;
+constexpr int kBdThreads = 32 * kBdWarps;
+constexpr int kBdCols = 16;
+constexpr int kBdStages = 4;
+constexpr int kBdCtrlBytes = 256;
 constexpr int kBatchCtrlBytes = 256;   // mbarriers, work range, item header at the start of shared memory
 
 // Largest number of plan items for T tokens, top-K, S shared experts, G
@@ -65,81 +71,84 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids,
                          const uint16_t* wsg, const float* x, int H, float* gate, cudaStream_t st);
 // plan -> gate/up -> down into y (-> combine into a.out when non-null)
 cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st);
+// x = h / sqrt(mean(h^2) + eps)
+cudaError_t launch_rmsnorm(const float* h, float* x, int H, float eps, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // single-launch persistent kernel (fmoe_fused.cu)
 // ---------------------------------------------------------------------------
-#ifndef FMOE_FUSED_GU_WARPS
-#define FMOE_FUSED_GU_WARPS 12
-#endif
-constexpr int kGuWarps = FMOE_FUSED_GU_WARPS;          // dequantised gate/up GEMV warps
-constexpr int kDownWarps = 16 - kGuWarps;              // down projection + combine warps
-constexpr int kConsumerWarps = kGuWarps + kDownWarps;  // warps that hold the layer input
-constexpr int kProducerWarp = kConsumerWarps;          // issues the bulk copies
-constexpr int kFinalWarp = kConsumerWarps + 1;         // turns partial sums into h rows
-constexpr int kExchangeWarp = kConsumerWarps + 2;      // gathers the h of even slots
-constexpr int kExchangeWarp2 = kConsumerWarps + 3;     // routes; gathers the h of odd slots
-constexpr int kRouteXw = 1;                            // the exchange warp (0, 1) that routes
-constexpr int kFusedThreads = 32 * (kConsumerWarps + 4);
-// registers per thread: the most that every warp can hold when the warps are
-// spread over the SM's four schedulers, each with 16K registers (8 at a time)
-constexpr int kFusedWarpsPerScheduler = (kFusedThreads / 32 + 3) / 4;
-constexpr int kFusedMaxRegs = (16384 / (kFusedWarpsPerScheduler * 32)) / 8 * 8;
+constexpr int kGuWarps = 12;                           // dequantised gate/up GEMV warps
+constexpr int kDnWarps = 8;                            // down projection warps
+constexpr int kPollWarps = kGuWarps + kDnWarps;        // warps that gather each layer's input
+constexpr int kProducerWarp = kPollWarps;              // issues the bulk copies
+constexpr int kFinalWarp = kPollWarps + 1;             // routes, turns partial sums into h
+constexpr int kFusedWarps = kPollWarps + 2;
+constexpr int kFusedThreads = 32 * kFusedWarps;
+constexpr int kDnThreads = 32 * kDnWarps;
+// registers per thread: the SM's 64K registers shared by the block's threads
+constexpr int kFusedMaxRegs = (65536 / kFusedThreads) / 8 * 8;
 constexpr int kMaxFusedLayers = 64;    // layers per launch; longer stacks use several launches
 constexpr int kMaxSlots = FMOE_MAX_TOPK + 1;
 constexpr int kMaxStages = 16;
+constexpr int kMaxPieces = 4;          // slot ranges a block's columns may span
+constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, reductions
 // Tuning of the persistent kernel (compile-time; the defaults are the
-// measured best): ring stages at most, slots by which a slot's down records
-// trail its gate/up records, whether an exchange warp waits for its own
-// block's share of a slot before polling the other blocks' shares, whether
-// the producer waits for the previous layer's last exchange before it
-// requests the next layer's rows (its copies would otherwise queue ahead of
-// the exchange's loads), and how the block's rows are split into bulk copies.
+// measured best): ring stages at most, ring stages issued before a layer's
+// down columns, bytes per bulk copy, producer lanes that take turns issuing
+// copies, pause between two polls of the accumulators.
 #ifndef FMOE_FUSED_STAGE_CAP
-#define FMOE_FUSED_STAGE_CAP 16
+#define FMOE_FUSED_STAGE_CAP 8
 #endif
-#ifndef FMOE_FUSED_DOWN_LAG
-#define FMOE_FUSED_DOWN_LAG 3
+#ifndef FMOE_FUSED_DAREA_AFTER
+#define FMOE_FUSED_DAREA_AFTER 2
 #endif
-#ifndef FMOE_XCHG_WAIT_OWN
-#define FMOE_XCHG_WAIT_OWN 1
+#ifndef FMOE_FUSED_COPY_BYTES
+#define FMOE_FUSED_COPY_BYTES 16384
 #endif
-#ifndef FMOE_FUSED_LATE_PREFETCH
-#define FMOE_FUSED_LATE_PREFETCH 1
-#endif
-// Pause between two polls of published (value, tag) words: every block
-// polls the same few lines of L2, so polling too often slows down the
-// stores it is waiting for.
-#ifndef FMOE_INPUT_POLL_NS
-#define FMOE_INPUT_POLL_NS 32
-#endif
-#ifndef FMOE_EXCHANGE_POLL_NS
-#define FMOE_EXCHANGE_POLL_NS 32
-#endif
-constexpr unsigned kInputPollNs = FMOE_INPUT_POLL_NS;
-constexpr unsigned kExchangePollNs = FMOE_EXCHANGE_POLL_NS;
-#ifndef FMOE_FUSED_TAIL_SLOTS
-#define FMOE_FUSED_TAIL_SLOTS 2
-#endif
-constexpr int kFusedTailSlots = FMOE_FUSED_TAIL_SLOTS;   // last slots whose down rows the gate/up warps do
 #ifndef FMOE_FUSED_ISSUE_LANES
 #define FMOE_FUSED_ISSUE_LANES 4
 #endif
-constexpr int kFusedIssueLanes = FMOE_FUSED_ISSUE_LANES;   // producer lanes that take turns issuing copies
-#ifndef FMOE_FUSED_ROWS_PER_COPY
-#define FMOE_FUSED_ROWS_PER_COPY 64
+#ifndef FMOE_POLL_NS
+#define FMOE_POLL_NS 64
 #endif
-#ifndef FMOE_FUSED_DOWN_COPIES
-#define FMOE_FUSED_DOWN_COPIES 1
-#endif
-constexpr int kFusedRowsPerCopy = FMOE_FUSED_ROWS_PER_COPY;   // gate/up records per bulk copy
-constexpr int kFusedDownCopies = FMOE_FUSED_DOWN_COPIES;      // bulk copies per slot's down records
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
-constexpr int kFusedDownLag = FMOE_FUSED_DOWN_LAG;
-constexpr int kMaxDownGroups = 8;      // down row groups per down warp
-constexpr int kCtrlBytes = 2048;       // barriers, routing result, reductions, tail sums
-constexpr int kMaxTailRows = (kCtrlBytes - 1536) / 4;   // down rows per block the tail sums can hold
-constexpr int kMaxTailGroups = 4;      // down row groups per gate/up warp in the tail
+constexpr int kFusedDareaAfter = FMOE_FUSED_DAREA_AFTER;
+constexpr uint32_t kFusedCopyBytes = FMOE_FUSED_COPY_BYTES;
+constexpr int kFusedIssueLanes = FMOE_FUSED_ISSUE_LANES;
+constexpr unsigned kPollNs = FMOE_POLL_NS;
+
+// A block's intermediate columns within one slot: columns [i0, i0+cnt) of
+// slot `slot`, local indices [loc, loc+cnt); in the block's down area its
+// columns' codes at col_off and the (scale,bias) words of groups g0..g0+ng-1
+// at sb_off.
+struct Piece {
+  int slot, i0, cnt, loc, col_off, sb_off, g0, ng;
+};
+
+// Columns of block c of n: the virtual columns [V*c/n, V*(c+1)/n) of the
+// slot-major sequence (slot 0 = the shared expert when there is one), split
+// at slot boundaries.  Returns the number of pieces (at most max_pieces are
+// written) and the down-area bytes they need.
+__host__ __device__ inline int block_pieces(int NS, int I, int c, int n, const BlobLayout& lay, Piece* pc,
+                                            int max_pieces, int& darea_bytes) {
+  const long long V = (long long)NS * I;
+  long long v = V * c / n;
+  const long long v1 = V * (c + 1) / n;
+  int np = 0, off = 0, u = 0;
+  while (v < v1) {
+    const int slot = (int)(v / I), i0 = (int)(v % I);
+    const int cnt = (int)((v1 - v) < (long long)(I - i0) ? (v1 - v) : (long long)(I - i0));
+    const int g0 = i0 / kGroup, ng = (i0 + cnt - 1) / kGroup - g0 + 1;
+    const int cb = (int)round_up((size_t)cnt * lay.dcol, 128), sbb = (int)round_up((size_t)ng * lay.dsb_group, 128);
+    if (np < max_pieces) pc[np] = Piece{slot, i0, cnt, u, off, off + cb, g0, ng};
+    off += cb + sbb;
+    u += cnt;
+    v += cnt;
+    ++np;
+  }
+  darea_bytes = off;
+  return np;
+}
 
 struct FusedLayerPtrs {
   const uint8_t* experts;
@@ -152,32 +161,31 @@ struct FusedPlan {
   bool ok;
   int grid;
   size_t smem;
-  int rows_per_stage;       // gate/up rows per ring stage (two per consumer warp and slice range)
+  int R;                    // gate/up records per ring stage (two per gate/up warp and slice range)
+  int nparts;               // partial sums per gate/up row (slice ranges of H)
   int nstage, stage_bytes;  // ring
-  int dslot_bytes;          // one slot's down records
-  int nrmax, nparts;        // gate/up rows per block and partial sums per row
-  int part_off, xs_off, stage_off, hs_off, hs_slot_bytes, darea_off, ring_off;
-  int dlag;                 // a slot's down records are copied, and used, dlag slots after its gate/up
+  int len_max;              // most intermediate columns a block owns
+  int hb;                   // floats per column in the h buffer
+  int xs_off, part_off, hbuf_off, darea_off, darea_bytes, ring_off;
 };
 
 struct FusedParams {
   int bits, H, I, E, K, S, L;
-  int norm;                 // 1: input = RMSNorm(hin), residual = hin (stack); 0: given x / residual
+  int norm;                 // 1: input = RMSNorm(h), residual = h (stack); 0: given x / residual
   float eps;
   size_t blob;
   BlobLayout lay;
   const float* x;           // norm == 0: input [H]
   const float* residual;    // norm == 0: residual [H]
-  float* out;               // norm == 0: output [H];  norm == 1: h (in for layer 0, out for the last)
+  float* out;               // norm == 0: output [H];  norm == 1: h (in for layer 0, out after the last)
   const float* logits;      // [L][E]
-  float* hmid;              // [K+S][I] h of the last layer (plain fp32)
-  unsigned long long* hll;  // [K+S][I] (value, tag) exchange of h
-  unsigned long long* hbufll;  // [2][H] (value, tag) outputs of layers 0..L-2 (stacks)
+  float* hmid;              // [K+S][I] h of the last layer (plain fp32), or nullptr
+  unsigned long long* acc;  // [3][H] fixed-point accumulators (workspace state)
+  uint32_t* lbase;          // layers run on the workspace, modulo 3
   int32_t* ids_out;         // [L][K] or nullptr
   float* w_out;             // [L][K] or nullptr
   float* gate_out;          // [L] or nullptr
   uint32_t* exit_ctr;       // zero on entry and on exit
-  uint32_t* epoch;          // incremented by the last block out
   uint32_t* err;
   unsigned long long timeout_ns;
   FusedPlan plan;
@@ -191,6 +199,71 @@ FusedPlan fused_plan(int bits, int H, int I, int K, int S, int device);
 // per block (host arithmetic only).
 FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem_max);
 cudaError_t launch_fused(FusedParams& p, const FusedPlan& plan, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// host-side argument checks shared by the entry points
+// ---------------------------------------------------------------------------
+inline bool host_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bool host_vec_ok(const void* p) { return p != nullptr && host_aligned(p, 16); }
+
+inline bool host_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+// Shape and pointer checks common to every call that reads expert blobs.
+inline fmoe_status check_layer(const fmoe_layer* L, bool need_ptrs) {
+  if (L == nullptr) return FMOE_ERR_INVALID_ARG;
+  if (L->bits != 4 && L->bits != 2) return FMOE_ERR_UNSUPPORTED;
+  if (L->group != kGroup) return FMOE_ERR_UNSUPPORTED;
+  if (L->hidden <= 0 || L->inter <= 0 || L->hidden % kGroup || L->inter % kGroup) return FMOE_ERR_INVALID_ARG;
+  if (L->hidden > FMOE_MAX_HIDDEN || L->inter > FMOE_MAX_INTER) return FMOE_ERR_UNSUPPORTED;
+  if (L->n_experts <= 0 || L->n_experts > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
+  if (L->has_shared != 0 && L->has_shared != 1) return FMOE_ERR_INVALID_ARG;
+  if (need_ptrs) {
+    if (L->experts == nullptr || !host_aligned(L->experts, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
+    if (L->has_shared) {
+      if (L->shared == nullptr || !host_aligned(L->shared, kPlaneAlign)) return FMOE_ERR_INVALID_ARG;
+      if (L->shared_gate_w == nullptr || !host_aligned(L->shared_gate_w, 16)) return FMOE_ERR_INVALID_ARG;
+    }
+  }
+  return FMOE_OK;
+}
+
+// The activation arguments of fmoe_moe_block (T tokens): non-null, 16-byte
+// aligned; out may alias residual but must not overlap x or the logits.
+inline fmoe_status check_block_args(const fmoe_layer* L, const float* x, const float* logits,
+                                    const float* residual, const float* out, int T) {
+  if (!host_vec_ok(x) || !host_vec_ok(logits) || !host_vec_ok(residual) || !host_vec_ok(out))
+    return FMOE_ERR_INVALID_ARG;
+  const size_t hb = (size_t)T * L->hidden * 4;
+  if (host_overlap(out, hb, x, hb) || host_overlap(out, hb, logits, (size_t)T * L->n_experts * 4))
+    return FMOE_ERR_INVALID_ARG;
+  if (out != residual && host_overlap(out, hb, residual, hb)) return FMOE_ERR_INVALID_ARG;
+  return FMOE_OK;
+}
+
+// Fill the persistent kernel's per-call fields for layer descriptors
+// layers[0..n) (same shape), n <= kMaxFusedLayers.
+inline void fused_params_for(FusedParams& p, const fmoe_layer* layers, int n, int K) {
+  const fmoe_layer& L0 = layers[0];
+  p.bits = L0.bits;
+  p.H = L0.hidden;
+  p.I = L0.inter;
+  p.E = L0.n_experts;
+  p.K = K;
+  p.S = L0.has_shared;
+  p.L = n;
+  p.lay = blob_layout(L0.bits, L0.hidden, L0.inter);
+  p.blob = p.lay.bytes;
+  for (int i = 0; i < n; ++i) {
+    p.layer[i].experts = static_cast<const uint8_t*>(layers[i].experts);
+    p.layer[i].shared = static_cast<const uint8_t*>(layers[i].shared);
+    p.layer[i].wsg = layers[i].shared_gate_w;
+  }
+}
 
 cudaError_t launch_wait_test(uint32_t* counter, uint32_t* err, int n_blocks, int expected,
                              unsigned long long timeout_ns, cudaStream_t st);

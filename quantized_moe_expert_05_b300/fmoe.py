@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfmoe.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_RANGE = 0, 1, 2, 3, 4, 5
 MAX_TOKENS, MAX_TOPK, MAX_EXPERTS, MAX_LAYERS = 16, 16, 1024, 1024
 
 
@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "fmoe_last_device_error": (I, [P, P]),
         "fmoe_debug_wait_test": (I, [P, I, I, I, P]),
         "fmoe_moe_block_noalloc": (I, [LP, P, P, P, P, I, P, P]),
+        "fmoe_debug_launch_geometry": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
+        "fmoe_debug_block_pieces": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -233,7 +235,7 @@ def debug_wait_test(ws: torch.Tensor, n_blocks: int, expected: int, timeout_us: 
            "fmoe_debug_wait_test")
 
 
-NOALLOC_SCRATCH_BYTES = 256 * 1024
+NOALLOC_SCRATCH_BYTES = 128 * 1024
 
 
 def moe_block_noalloc(layer: Layer, x: torch.Tensor, logits: torch.Tensor, residual: torch.Tensor, K: int,

@@ -24,15 +24,17 @@ Blob format written here (one contiguous blob per expert):
         up_q   [H*bits/32] uint32   packed codes of up row r
         gate_sb [H/64]     uint32   low half = scale (bf16), high half = bias (bf16)
         up_sb   [H/64]     uint32
-    down rows, j = 0..H-1, starting on a 256-byte boundary, each padded to a
-    multiple of 16 bytes:
-        down_q [I*bits/32] uint32
-        down_sb [I/64]     uint32
+    the down projection by column, i = 0..I-1, starting on a 256-byte boundary:
+        down_q [H*bits/32] uint32   word w: codes of rows w*(32/bits).. of column i
+    its (scale, bias) words by group of 64 columns, g = 0..I/64-1, starting on
+    a 256-byte boundary:
+        down_sb [H]        uint32   word j: row j's scale and bias for group g
     the blob is padded to a multiple of 256 bytes.
 
-Element c of a packed row sits at bits (c % (32/bits))*bits of word
-c/(32/bits).  One row of each matrix is contiguous with its scales, so any
-range of rows is one contiguous byte range.
+Element c of a packed gate/up row sits at bits (c % (32/bits))*bits of word
+c/(32/bits); row j of a down column likewise at bits (j % (32/bits))*bits of
+word j/(32/bits).  A range of gate/up rows, a range of down columns and a
+range of down groups are each one contiguous byte range.
 
 The packed-code and affine-group form follows the flash-moe write-ups'
 description of the 4-bit / 2-bit expert weights ("nibble * scale + bias",
@@ -108,34 +110,35 @@ def _round_up(n: int, a: int) -> int:
 
 
 def plane_words(bits: int, hidden: int, inter: int) -> dict:
-    """(rows, words per row) of each of the six parts of a blob."""
+    """(rows, words per row) of each of the six parts of a blob; a "row" of
+    down_q is a column of the down projection, a row of down_sb a group."""
     per = 32 // bits
     return {
         "gate_q": (inter, hidden // per),
         "gate_sb": (inter, hidden // GROUP),
         "up_q": (inter, hidden // per),
         "up_sb": (inter, hidden // GROUP),
-        "down_q": (hidden, inter // per),
-        "down_sb": (hidden, inter // GROUP),
+        "down_q": (inter, hidden // per),
+        "down_sb": (inter // GROUP, hidden),
     }
 
 
 def row_layout(bits: int, hidden: int, inter: int) -> tuple:
     """(dict part -> (byte offset of row 0, byte stride between rows), blob bytes)."""
     qh, sh = hidden * bits // 8, hidden // GROUP * 4
-    qi, si = inter * bits // 8, inter // GROUP * 4
     gu_row = _round_up(2 * qh + 2 * sh, 16)
-    d_row = _round_up(qi + si, 16)
-    d_off = _round_up(inter * gu_row, PLANE_ALIGN)
+    dq_off = _round_up(inter * gu_row, PLANE_ALIGN)
+    dcol = hidden * bits // 8
+    dsb_off = _round_up(dq_off + inter * dcol, PLANE_ALIGN)
     parts = {
         "gate_q": (0, gu_row),
         "up_q": (qh, gu_row),
         "gate_sb": (2 * qh, gu_row),
         "up_sb": (2 * qh + sh, gu_row),
-        "down_q": (d_off, d_row),
-        "down_sb": (d_off + qi, d_row),
+        "down_q": (dq_off, dcol),
+        "down_sb": (dsb_off, hidden * 4),
     }
-    return parts, _round_up(d_off + hidden * d_row, PLANE_ALIGN)
+    return parts, _round_up(dsb_off + inter // GROUP * hidden * 4, PLANE_ALIGN)
 
 
 def blob_bytes(bits: int, hidden: int, inter: int) -> int:

@@ -55,7 +55,7 @@ def test_expert_bytes_rejects_bad_shapes(fm):
 
 
 def test_status_strings(fm):
-    for s in range(5):
+    for s in range(6):
         assert fm.status_string(s)
     assert fm.status_string(fm.ERR_TIMEOUT) == "device-side wait timed out"
 

@@ -53,16 +53,48 @@ def sb(scale, bias, rows, groups):
     return np.full((rows, groups), bf16(scale) | (bf16(bias) << 16), dtype=np.uint32)
 
 
+def _up(n, a):
+    return -(-n // a) * a
+
+
 def build_blob(bits, H, I, gate, up, down):
-    """Blob bytes from (codes, sb_words) per matrix, placed with the generator's layout."""
-    parts, nbytes = synth.row_layout(bits, H, I)
+    """Blob bytes from (codes, sb_words) per matrix, written field by field.
+
+    The test's own statement of the packed format: I gate/up records of
+    [gate codes | up codes | gate (scale,bias) words | up words], each padded
+    to 16 bytes; from the next 256-byte boundary the down projection by
+    column (column i: H codes packed over rows, lowest bits first); from the
+    next 256-byte boundary the down (scale,bias) words by group of 64 columns
+    (group g: one word per row); the blob padded to 256 bytes.  Codes are
+    [rows][cols] of the matrix as used (gate/up [I][H], down [H][I]).
+    """
+    per = 32 // bits
+    qh, sh = H // per * 4, H // 64 * 4
+    gu = _up(2 * qh + 2 * sh, 16)
+    dq = _up(I * gu, 256)
+    dcol = H // per * 4
+    dsb = _up(dq + I * dcol, 256)
+    nbytes = _up(dsb + I // 64 * H * 4, 256)
     words = np.zeros(nbytes // 4, dtype=np.uint32)
-    for name, (codes, sbw) in (("gate", gate), ("up", up), ("down", down)):
-        for part, rows in ((name + "_q", pack(codes, bits)), (name + "_sb", np.asarray(sbw, dtype=np.uint32))):
-            base, stride = parts[part]
-            for r in range(rows.shape[0]):
-                o = (base + r * stride) // 4
-                words[o:o + rows.shape[1]] = rows[r]
+
+    def put(byte_off, vals):
+        vals = np.asarray(vals, dtype=np.uint32)
+        words[byte_off // 4: byte_off // 4 + vals.size] = vals
+
+    gq, gsb = pack(gate[0], bits), np.asarray(gate[1], dtype=np.uint32)
+    uq, usb = pack(up[0], bits), np.asarray(up[1], dtype=np.uint32)
+    for r in range(gq.shape[0]):
+        put(r * gu, gq[r])
+        put(r * gu + qh, uq[r])
+        put(r * gu + 2 * qh, gsb[r])
+        put(r * gu + 2 * qh + sh, usb[r])
+    dcodes = np.asarray(down[0])                      # [H][I]
+    dcols = pack(dcodes.T, bits)                      # [I][H/per]: column i packed over rows
+    dsbw = np.asarray(down[1], dtype=np.uint32)       # [H][I/64]
+    for i in range(dcols.shape[0]):
+        put(dq + i * dcol, dcols[i])
+    for g in range(dsbw.shape[1]):
+        put(dsb + g * H * 4, dsbw[:, g])
     return words.view(np.uint8)
 
 
@@ -179,6 +211,36 @@ def pin_group_decomposition():
                 sl = slice(64 * g, 64 * g + 64)
                 tot += sv[r, g] * float(codes[r, sl] @ x[sl]) + bv[r, g] * float(x[sl].sum())
             assert got[r] == tot, (bits, r)
+
+
+def pin_random_blob_fields():
+    """Every code and (scale,bias) word of all three matrices lands where the
+    format puts it: random codes and per-(row, group) dyadic scales and
+    biases, written field by field, dequantise exactly to q*s+b (a row
+    permutation, a stride slip or a transposed plane changes some value)."""
+    rng = np.random.default_rng(13)
+    scales = [2.0 ** -6, 3 * 2.0 ** -7, 2.0 ** -5, 5 * 2.0 ** -8, 2.0 ** -4]
+    biases = [-(2.0 ** -4), -(3 * 2.0 ** -6), 0.0, -(2.0 ** -3), 2.0 ** -7]
+    for bits, H, I in ((4, 128, 128), (2, 128, 128), (4, 192, 64), (2, 64, 192)):
+        cmax = (1 << bits) - 1
+
+        def mat(rows, n):
+            codes = rng.integers(0, cmax + 1, size=(rows, n))
+            si = rng.integers(len(scales), size=(rows, n // 64))
+            bi = rng.integers(len(biases), size=(rows, n // 64))
+            sbw = np.vectorize(lambda a, b: bf16(scales[a]) | (bf16(biases[b]) << 16),
+                               otypes=[np.uint32])(si, bi)
+            g = np.arange(n) // 64
+            want = codes * np.array(scales)[si][:, g] + np.array(biases)[bi][:, g]
+            return (codes, sbw), want
+
+        gate, wg = mat(I, H)
+        up, wu = mat(I, H)
+        down, wd = mat(H, I)
+        blob = build_blob(bits, H, I, gate, up, down)
+        got = om.expert_weights(blob, bits, H, I)
+        for name, g_, w_ in zip(("gate", "up", "down"), got, (wg, wu, wd)):
+            assert g_.shape == w_.shape and np.array_equal(g_, w_), (bits, H, I, name)
 
 
 CONST = dict(cg=3, sg=2.0 ** -6, bg=-(2.0 ** -5),   # gate weight 1/64
@@ -347,7 +409,7 @@ def pin_stack_closed_form():
 
 
 PINS = [pin_unpack_golden, pin_dequant_golden, pin_two_groups, pin_fma_identity,
-        pin_group_decomposition, pin_constant_rows, pin_route_bruteforce,
+        pin_group_decomposition, pin_random_blob_fields, pin_constant_rows, pin_route_bruteforce,
         pin_route_weights, pin_special_values, pin_zero_weight, pin_page_sizes,
         pin_layout_matches_generator, pin_block_closed_form, pin_stack_closed_form]
 
@@ -408,6 +470,29 @@ def _layout_gate_up_swapped(bits, hidden, inter):
     return planes, nbytes
 
 
+def _layout_down_parts_swapped(bits, hidden, inter):
+    planes, nbytes = _ORIG["layout"](bits, hidden, inter)
+    planes = dict(planes)
+    (qo, qs, qr, qw), (so, ss, sr, sw) = planes["down_q"], planes["down_sb"]
+    planes["down_q"], planes["down_sb"] = (so, qs, qr, qw), (qo, ss, sr, sw)
+    return planes, nbytes
+
+
+def _layout_up_rows_shifted(bits, hidden, inter):
+    planes, nbytes = _ORIG["layout"](bits, hidden, inter)
+    planes = dict(planes)
+    off, stride, rows, wpr = planes["up_q"]
+    planes["up_q"] = (off + stride, stride, rows, wpr) if rows > 1 else (off, stride, rows, wpr)
+    return planes, nbytes
+
+
+def _weights_down_row_major(blob, bits, hidden, inter):
+    wg, wu, _ = _ORIG["expert_weights"](blob, bits, hidden, inter)
+    q = om.unpack_codes(om.part_rows(blob, bits, hidden, inter, "down_q"), bits)   # [I][H], not transposed
+    sbw = om.part_rows(blob, bits, hidden, inter, "down_sb").T
+    return wg, wu, om.dequantize_codes(q.reshape(hidden, inter), sbw)
+
+
 def _route_full_softmax(logits, k):
     l = np.asarray(logits, dtype=np.float64)
     ids = np.argsort(-l, kind="stable")[:k]
@@ -450,7 +535,8 @@ def _rms_sum(h, eps):
     return h / np.sqrt(np.sum(h * h) + eps)
 
 
-_ORIG = {n: getattr(om, n) for n in ("unpack_codes", "dequantize", "route", "combine", "layout")}
+_ORIG = {n: getattr(om, n) for n in ("unpack_codes", "dequantize", "route", "combine", "layout",
+                                      "expert_weights")}
 
 MUTANTS = [
     ("unpack_codes", _unpack_msb_first),
@@ -461,6 +547,9 @@ MUTANTS = [
     ("expert_ffn", _ffn_no_up),
     ("expert_ffn", _ffn_down_transposed),
     ("layout", _layout_gate_up_swapped),
+    ("layout", _layout_down_parts_swapped),
+    ("layout", _layout_up_rows_shifted),
+    ("expert_weights", _weights_down_row_major),
     ("route", _route_full_softmax),
     ("route", _route_ties_high),
     ("route", _route_ascending),

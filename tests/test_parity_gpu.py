@@ -163,13 +163,15 @@ def test_zero_weight_invariance_on_gpu(fm):
 @pytest.mark.parametrize("T", [1, 3])
 def test_poisoned_outputs_and_scratch_are_fully_written(fm, T):
     """Every output element and every scratch word a call reads is written by
-    the call: outputs and the whole workspace past its 256-byte header (error
-    word, exit count, launch count) start as NaN."""
+    the call: outputs and the whole workspace past its state (the 256-byte
+    header and the single-launch kernel's accumulators, 256 + 24*H bytes
+    rounded up to 256) start as NaN."""
     shape = synth.BlockShape("tiny_shared_h512_e8_top2_i128_q4", 512, 128, 8, 2, True, 4, 0.002, 0.02, -0.1,
                              0.0, seed=23)
     layer = make_layer(fm, shape)
     ws = fm.new_workspace(layer, 3, 2)
-    ws[256:].view(torch.float32).fill_(float("nan"))
+    state = (256 + 24 * shape.hidden + 255) // 256 * 256
+    ws[state:].view(torch.float32).fill_(float("nan"))
     inp = synth.block_inputs(shape, T, tag=90)
     out = torch.full((T, shape.hidden), float("nan"), device="cuda")
     fm.moe_block(layer, inp.x.cuda(), inp.logits.cuda(), inp.residual.cuda(), 2, ws, out=out)
@@ -181,7 +183,7 @@ def test_poisoned_outputs_and_scratch_are_fully_written(fm, T):
     for t in range(T):
         assert_close(got[t], ref["out"][t], what=f"poisoned run, token {t}")
 
-    ws[256:].view(torch.float32).fill_(float("nan"))
+    ws[state:].view(torch.float32).fill_(float("nan"))
     ids = torch.tensor([[1, 5], [5, 1], [0, 7]][:T], dtype=torch.int32, device="cuda")
     y = torch.full((T, 3, shape.hidden), float("nan"), device="cuda")
     fm.expert_ffn(layer, ids, inp.x.cuda(), ws, y=y)

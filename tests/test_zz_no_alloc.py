@@ -68,8 +68,8 @@ def test_noalloc_in_place_and_without_error_output(fm):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(fm):
-    # H 8192, I 4096, top-16 plus a shared expert needs about 280 KB of
-    # scratch, more than the library's fixed 256 KB array: refused up front.
+    # H 8192 needs 256 + 24 * 8192 = 196,864 bytes of scratch, more than the
+    # library's fixed 128 KiB array: refused up front.
     dummy = torch.zeros(1024, dtype=torch.int32, device="cuda")
     wsg = torch.zeros(8192, dtype=torch.int16, device="cuda")
     layer = fm.Layer(4, 8192, 4096, 64, dummy, dummy, wsg)
