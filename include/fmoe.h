@@ -236,7 +236,8 @@ fmoe_status fmoe_ws_batch_plan(void* ws, const fmoe_layer* layer /* host */, int
 enum {
   FMOE_GEO_FUSED_OK, FMOE_GEO_FUSED_GRID, FMOE_GEO_FUSED_SMEM, FMOE_GEO_FUSED_CTRL_BYTES,
   FMOE_GEO_FUSED_XS_OFF, FMOE_GEO_FUSED_PART_OFF, FMOE_GEO_FUSED_HBUF_OFF, FMOE_GEO_FUSED_HBUF_STRIDE,
-  FMOE_GEO_FUSED_DAREA_OFF, FMOE_GEO_FUSED_DAREA_BYTES, FMOE_GEO_FUSED_RING_OFF, FMOE_GEO_FUSED_NSTAGE,
+  FMOE_GEO_FUSED_DSCR_OFF, FMOE_GEO_FUSED_DAREA_OFF, FMOE_GEO_FUSED_DAREA_BYTES, FMOE_GEO_FUSED_RING_OFF,
+  FMOE_GEO_FUSED_NSTAGE,
   FMOE_GEO_FUSED_STAGE_BYTES, FMOE_GEO_FUSED_ROWS_PER_STAGE, FMOE_GEO_FUSED_NPARTS, FMOE_GEO_FUSED_LEN_MAX,
   FMOE_GEO_BATCH_GRID, FMOE_GEO_BATCH_G, FMOE_GEO_BATCH_GU_WARPS, FMOE_GEO_BATCH_GU_ROWS,
   FMOE_GEO_BATCH_GU_NSTAGE, FMOE_GEO_BATCH_GU_STAGE_BYTES, FMOE_GEO_BATCH_GU_XS_BYTES, FMOE_GEO_BATCH_GU_SMEM,

@@ -267,6 +267,7 @@ fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, i
   out[FMOE_GEO_FUSED_PART_OFF] = f.part_off;
   out[FMOE_GEO_FUSED_HBUF_OFF] = f.hbuf_off;
   out[FMOE_GEO_FUSED_HBUF_STRIDE] = f.hb;
+  out[FMOE_GEO_FUSED_DSCR_OFF] = f.dscr_off;
   out[FMOE_GEO_FUSED_DAREA_OFF] = f.darea_off;
   out[FMOE_GEO_FUSED_DAREA_BYTES] = f.darea_bytes;
   out[FMOE_GEO_FUSED_RING_OFF] = f.ring_off;

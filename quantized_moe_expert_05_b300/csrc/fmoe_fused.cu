@@ -83,9 +83,13 @@ __device__ __forceinline__ float quad_reduce(float a, float b, float c, float d,
   return y;
 }
 
-__device__ __forceinline__ void ld_relaxed_v2(const unsigned long long* p, unsigned long long& a,
+// Acquire loads of accumulator words: a reader that sees every block's
+// contribution also sees what those blocks wrote before adding (their clears
+// of other accumulators), without a fence that would wait for this thread's
+// unrelated copies in flight.
+__device__ __forceinline__ void ld_acquire_v2(const unsigned long long* p, unsigned long long& a,
                                               unsigned long long& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -110,7 +114,7 @@ __device__ __forceinline__ bool poll8(const unsigned long long* p, int need, flo
   while (true) {
     unsigned long long w[8];
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) ld_relaxed_v2(p + i, w[i], w[i + 1]);
+    for (int i = 0; i < 8; i += 2) ld_acquire_v2(p + i, w[i], w[i + 1]);
     bool ok = true;
 #pragma unroll
     for (int i = 0; i < 8; ++i) ok = ok && fix_count(w[i]) == need;
@@ -133,19 +137,21 @@ __device__ __forceinline__ bool poll8(const unsigned long long* p, int need, flo
   }
 }
 
-// Wait (bounded) until a release counter in shared memory reaches `target`.
+// Wait (bounded) until a release counter in shared memory reaches `target`,
+// spinning (the waiting warps resume as soon as the counter moves).
 __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, unsigned long long timeout_ns,
                                            uint32_t* err, volatile int* abort) {
   if (ld_acquire_shared(ctr) >= target) return true;
   const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(32);
+  for (uint32_t it = 1;; ++it) {
     if (ld_acquire_shared(ctr) >= target) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      atomicOr(err, kErrWaitTimeout);
-      *abort = 1;
-      return false;
+    if ((it & 255u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        atomicOr(err, kErrWaitTimeout);
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
@@ -190,25 +196,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
   const BlobLayout& lay = p.lay;
   // control area
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem);   // ring stage filled (count 1 + bytes)
-  uint64_t* bar_empty = bar_full + kMaxStages;              // ring stage free (gate/up warps + finaliser)
-  uint64_t* bar_gudone = bar_empty + kMaxStages;            // stage's partial sums written (gate/up warps)
-  uint64_t* bar_x = bar_gudone + kMaxStages;                // layer input gathered (input warps)
-  uint64_t* bar_routed = bar_x + 1;                         // routing published (finaliser)
+  uint64_t* bar_empty = bar_full + kMaxStages;              // ring stage free (gate/up warps)
+  uint64_t* bar_gudone = bar_empty + kMaxStages;            // [2*kMaxStages] stage's partial sums written
+  uint64_t* bar_pfree = bar_gudone + 2 * kMaxStages;        // [2*kMaxStages] partial sums read (finaliser)
+  uint64_t* bar_x = bar_pfree + 2 * kMaxStages;             // layer input gathered (input warps)
+  uint64_t* bar_routed = bar_x + 1;                         // layer's routing published (finaliser)
   uint64_t* bar_zero = bar_routed + 1;                      // next accumulator slice cleared (finaliser)
   uint64_t* bar_dfull = bar_zero + 1;                       // down area filled (count 1 + bytes)
   uint64_t* bar_ddone = bar_dfull + 1;                      // down area free again (down warps)
-  uint64_t* bar_dsync = bar_ddone + 1;                      // [2] down warps among themselves
-  Piece* s_pc = reinterpret_cast<Piece*>(smem + 512);       // [kMaxPieces]
-  int* s_np = reinterpret_cast<int*>(smem + 640);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 644);
-  uint32_t* s_hdone = reinterpret_cast<uint32_t*>(smem + 648);   // stages whose h is written (cumulative)
-  int* s_ids = reinterpret_cast<int*>(smem + 704);          // [kMaxSlots]
-  float* s_w = reinterpret_cast<float*>(smem + 832);        // [kMaxSlots] routing weights, shared gate
-  float* s_red = reinterpret_cast<float*>(smem + 960);      // [kPollWarps][2]
+  Piece* s_pc = reinterpret_cast<Piece*>(smem + 1024);      // [kMaxPieces]
+  int* s_np = reinterpret_cast<int*>(smem + 1152);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 1156);
+  uint32_t* s_hdone = reinterpret_cast<uint32_t*>(smem + 1160);  // stages whose h is written (cumulative)
+  int* s_ids = reinterpret_cast<int*>(smem + 1280);         // [2][kMaxSlots] by layer parity
+  float* s_w = reinterpret_cast<float*>(smem + 1536);       // [2][kMaxSlots] routing weights, shared gate
+  float* s_red = reinterpret_cast<float*>(smem + 1792);     // [kPollWarps][2]
   float4* s_x4 = reinterpret_cast<float4*>(smem + pl.xs_off);   // layer input h (not normalised), slice-major
-  float* s_part = reinterpret_cast<float*>(smem + pl.part_off); // [stage][R][nparts][2]
+  float* s_part = reinterpret_cast<float*>(smem + pl.part_off); // [2*nstage][R][nparts][2]
   float* s_hb = reinterpret_cast<float*>(smem + pl.hbuf_off);   // [len][hb]: NV pre-scaled h, then h
-  uint8_t* darea = smem + pl.darea_off;
+  float* s_dscr = reinterpret_cast<float*>(smem + pl.dscr_off);  // [kDnThreads][RW*MW] transpose scratch
+  uint8_t* darea = smem + pl.darea_off;                          // the block's down columns and scale/bias
   uint8_t* ring = smem + pl.ring_off;
 
   const int tid = threadIdx.x;
@@ -229,16 +236,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
   if (tid == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_empty[i], kGuWarps + 1);
+      mbar_init(&bar_empty[i], kGuWarps);
+    }
+    for (int i = 0; i < 2 * kMaxStages; ++i) {
       mbar_init(&bar_gudone[i], kGuWarps);
+      mbar_init(&bar_pfree[i], 1);
     }
     mbar_init(bar_x, kPollWarps);
     mbar_init(bar_routed, 1);
     mbar_init(bar_zero, 1);
     mbar_init(bar_dfull, 1);
     mbar_init(bar_ddone, kDnWarps);
-    mbar_init(&bar_dsync[0], kDnWarps);
-    mbar_init(&bar_dsync[1], kDnWarps);
     int dbytes = 0;
     *s_np = block_pieces(NS, I, c, n, lay, s_pc, kMaxPieces, dbytes);
     *s_abort = 0;
@@ -255,7 +263,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
   int nx_id = -1;         // finaliser: top-K pick of its lane for the coming layer
   float nx_l = 0.f;
   auto slot_h = [&](int slot) -> int { return p.S ? (slot == 0 ? p.K : slot - 1) : slot; };
-
   for (int l = 0; l < p.L; ++l) {
     const FusedLayerPtrs lp = p.layer[l];
     const uint32_t lpar = (uint32_t)(l & 1);
@@ -305,9 +312,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
           wg += (bf16lo(wb.z) * v1.x + bf16hi(wb.z) * v1.y) + (bf16lo(wb.w) * v1.z + bf16hi(wb.w) * v1.w);
         }
       }
-      // every block's contributions to the previous sum were observed:
-      // order them before this block's next clear and its next additions
-      if (l > 0) fence_acq_rel_gpu();
       ss = warp_sum(ss);
       wg = warp_sum(wg);
       if (lane == 0) {
@@ -379,25 +383,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
             ga1 = slice_term<BITS>(qg, sg, xs, xsum);
             ua1 = slice_term<BITS>(qu, su, xs, xsum);
           }
+          // the ring stage is free once every gate/up warp has read it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_empty[st]);
           const float v = quad_reduce(ga0, ua0, ga1, ua1, gw, lane);
           const int pos = lane & (gw - 1), qw = gw >> 2;
           const int rsel = pos < 2 * qw ? rs0 : rs1;
+          // partial sums: 2*nstage slots, each reused once the finaliser has read it
+          const uint32_t g = g_cons - 1, ps = g % (2u * pl.nstage);
+          if (g >= 2u * pl.nstage) mbar_wait(&bar_pfree[ps], ((g / (2u * pl.nstage)) - 1u) & 1u, tmo, p.err, s_abort);
           if (rs0 < R / 2 && k * R + rsel < len && (pos & (qw - 1)) == 0)
-            s_part[(((size_t)st * R + rsel) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
+            s_part[(((size_t)ps * R + rsel) * nparts + pi) * 2 + ((pos / qw) & 1)] = v;
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bar_gudone[st]);
-            mbar_arrive(&bar_empty[st]);
-          }
+          if (lane == 0) mbar_arrive(&bar_gudone[ps]);
         }
       } else {
         // ---------------- down: owned columns, in order, into per-row sums ----
+        // Thread dt owns code words [MW*dt, MW*dt + MW) of every column, i.e.
+        // RW*MW consecutive output rows; the block's columns and their groups'
+        // scale/bias words sit in the down area (bulk copies by the producer).
         const int dt = tid - kGuWarps * 32;
         const int W = H / RW;                                  // code words per column
+        const int wb = MW * dt;                                // this thread's first code word
+        const bool dact = wb < W;
         float outp[MW * RW];
 #pragma unroll
         for (int r = 0; r < MW * RW; ++r) outp[r] = 0.f;
-        // this block's clear of the next accumulator, before this thread adds
+        // this block's clear of the next accumulator is ordered before this
+        // thread's additions (the fence waits here, off the critical path)
         mbar_wait(bar_zero, lpar, tmo, p.err, s_abort);
         fence_acq_rel_gpu();
         mbar_wait(bar_dfull, lpar, tmo, p.err, s_abort);
@@ -434,23 +447,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
                 }
               }
               hs += s_hb[(size_t)u * hb + NV];
-              const uint32_t* col = reinterpret_cast<const uint32_t*>(cbase + (size_t)(i - pc.i0) * lay.dcol);
+              if (dact) {
+                const uint32_t* col = reinterpret_cast<const uint32_t*>(cbase + (size_t)(i - pc.i0) * lay.dcol) + wb;
+                uint32_t w[MW];
+                if constexpr (MW == 4) {
+                  const uint4 v = *reinterpret_cast<const uint4*>(col);
+                  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                } else if constexpr (MW == 2) {
+                  const uint2 v = *reinterpret_cast<const uint2*>(col);
+                  w[0] = v.x; w[1] = v.y;
+                } else {
+                  w[0] = col[0];
+                }
 #pragma unroll
-              for (int j = 0; j < MW; ++j) {
-                const int m = dt + kDnThreads * j;
-                if (m < W) down_word<BITS>(col[m], hv, acc[j]);
+                for (int j = 0; j < MW; ++j) down_word<BITS>(w[j], hv, acc[j]);
               }
             }
-            // the group's scale and bias per row (RW consecutive words per code word)
-            const uint4* sbw =
-                reinterpret_cast<const uint4*>(darea + pc.sb_off + (size_t)gi * lay.dsb_group);
+            // the group's scale and bias per row: out += s * 2^64 * acc + b * sum(h)
+            if (dact) {
+              const uint4* sbw = reinterpret_cast<const uint4*>(darea + pc.sb_off + (size_t)gi * lay.dsb_group +
+                                                                (size_t)wb * RW * 4);
 #pragma unroll
-            for (int j = 0; j < MW; ++j) {
-              const int m = dt + kDnThreads * j;
-              if (m < W) {
+              for (int j = 0; j < MW; ++j) {
 #pragma unroll
                 for (int t4 = 0; t4 < RW / 4; ++t4) {
-                  const uint4 s4 = sbw[m * (RW / 4) + t4];
+                  const uint4 s4 = sbw[j * (RW / 4) + t4];
                   const float2 a01 = acc[j][2 * t4], a23 = acc[j][2 * t4 + 1];
                   float* o = outp + j * RW + 4 * t4;
                   o[0] += fmaf(bf16lo(s4.x) * 18446744073709551616.0f, a01.x, bf16hi(s4.x) * hs);
@@ -462,30 +483,29 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
             }
           }
         }
-        // every down thread is done with the down area: reuse it to turn the
-        // per-thread rows into row order, then add them (coalesced) into
-        // this layer's accumulator
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_dsync[0]);
-        mbar_wait(&bar_dsync[0], lpar, tmo, p.err, s_abort);
-        float* tb = reinterpret_cast<float*>(darea);
-#pragma unroll
-        for (int j = 0; j < MW; ++j) {
-          const int m = dt + kDnThreads * j;
-          if (m < W) {
-#pragma unroll
-            for (int t = 0; t < RW; t += 4)
-              *reinterpret_cast<float4*>(tb + m * RW + t) =
-                  make_float4(outp[j * RW + t], outp[j * RW + t + 1], outp[j * RW + t + 2], outp[j * RW + t + 3]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_dsync[1]);
-        mbar_wait(&bar_dsync[1], lpar, tmo, p.err, s_abort);
-        if (!*s_abort)
-          for (int r = dt; r < H; r += kDnThreads) red_add_u64(acc_cur + r, fix_word(tb[r], p.err));
+        // the down area may be refilled for the next layer
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_ddone);
+        // Each warp owns 32*RW*MW consecutive rows; a transpose through the
+        // warp's own scratch lets every red instruction of the warp add 32
+        // consecutive rows (coalesced), with no wait on the other down warps.
+        {
+          float* scr = s_dscr + (size_t)(warp - kGuWarps) * 32 * RW * MW;
+          const int r0 = (warp - kGuWarps) * 32 * RW * MW;    // the warp's first row
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < RW * MW; t += 4)
+            *reinterpret_cast<float4*>(scr + lane * RW * MW + t) =
+                make_float4(outp[t], outp[t + 1], outp[t + 2], outp[t + 3]);
+          __syncwarp();
+          if (!*s_abort && r0 < H) {
+#pragma unroll 4
+            for (int t = 0; t < RW * MW; ++t)
+              if (r0 + 32 * t + lane < H)
+                red_add_u64(acc_cur + r0 + 32 * t + lane, fix_word(scr[32 * t + lane], p.err));
+          }
+          __syncwarp();
+        }
       }
     } else if (warp == kProducerWarp) {
       // ------------------------------------------------------------------
@@ -498,13 +518,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
       bool routed = false;       // routed ids are published all at once
       auto ensure_routed = [&](int slot) {
         if (slot >= p.S && !routed) {
+          // the ids are known early; the copies wait for the layer's input
           mbar_wait(bar_routed, lpar, tmo, p.err, s_abort);
+          mbar_wait(bar_x, lpar, tmo, p.err, s_abort);
           routed = true;
         }
       };
+      const int* ids_l = s_ids + (size_t)(l & 1) * kMaxSlots;
       auto slot_blob = [&](int slot) -> const uint8_t* {
         if (p.S && slot == 0) return lp.shared;
-        return lp.experts + (size_t)s_ids[slot] * p.blob;
+        return lp.experts + (size_t)ids_l[slot] * p.blob;
       };
       auto copy = [&](uint8_t* dst, const uint8_t* src, uint32_t bytes, uint64_t* bar) {
         for (uint32_t off = 0; off < bytes; off += kFusedCopyBytes) {
@@ -569,9 +592,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
       // ------------------------------------------------------------------
       // finaliser: routing, the accumulator clear, h of each stage
       // ------------------------------------------------------------------
-      if (l == 0) warp_topk(p.logits, p.E, p.K, nx_id, nx_l);
-      const int my_id = nx_id;
-      const float my_w = warp_topk_softmax(nx_l, p.K);
+      // the routing of a layer is published as soon as it is known (at the
+      // end of the previous layer): the producer still waits for the
+      // layer's input before it requests a routed expert
+      auto publish = [&](int ll) {
+        warp_topk(p.logits + (size_t)ll * p.E, p.E, p.K, nx_id, nx_l);
+        const float my_w = warp_topk_softmax(nx_l, p.K);
+        if (lane < p.K) {
+          s_ids[(ll & 1) * kMaxSlots + p.S + lane] = nx_id;
+          s_w[(ll & 1) * kMaxSlots + p.S + lane] = my_w;
+          if (c == 0 && p.ids_out != nullptr) {
+            p.ids_out[(size_t)ll * p.K + lane] = nx_id;
+            p.w_out[(size_t)ll * p.K + lane] = my_w;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_routed);
+      };
+      if (l == 0) publish(0);
+      float* w_l = s_w + (size_t)(l & 1) * kMaxSlots;
       mbar_wait(bar_x, lpar, tmo, p.err, s_abort);
       float tot = 0.f, wgt = 0.f;
 #pragma unroll 4
@@ -581,20 +620,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
       }
       const float rinv = p.norm ? 1.0f / sqrtf(tot / (float)H + p.eps) : 1.0f;
       const float gate = p.S ? sigmoid_f(wgt * rinv) : 0.f;
-      if (lane < p.K) {
-        s_ids[p.S + lane] = my_id;
-        s_w[p.S + lane] = my_w;
-        if (c == 0 && p.ids_out != nullptr) {
-          p.ids_out[(size_t)l * p.K + lane] = my_id;
-          p.w_out[(size_t)l * p.K + lane] = my_w;
-        }
-      }
       if (lane == 0) {
-        if (p.S) s_w[0] = gate;
+        if (p.S) w_l[0] = gate;
         if (c == 0 && p.gate_out != nullptr) p.gate_out[l] = gate;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_routed);
       // clear this block's slice of the next layer's accumulator (its last
       // readers finished before this layer's input was complete)
       for (int r = lane; r < nd; r += 32) acc_next[ja + r] = 0ull;
@@ -603,8 +633,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
       if (lane == 0) mbar_arrive(bar_zero);
       const bool last = (l == p.L - 1) && p.hmid != nullptr;
       for (int k = 0; k < nstg; ++k) {
-        const uint32_t st = g_cons % pl.nstage;
-        mbar_wait(&bar_gudone[st], (g_cons / pl.nstage) & 1u, tmo, p.err, s_abort);
+        const uint32_t ps = g_cons % (2u * pl.nstage);
+        mbar_wait_spin(&bar_gudone[ps], (g_cons / (2u * pl.nstage)) & 1u, tmo, p.err, s_abort);
         ++g_cons;
         const int nrec = min(R, len - k * R);
         for (int r = lane; r < nrec; r += 32) {
@@ -612,14 +642,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
           int q = 0;
           while (q + 1 < np && u >= s_pc[q + 1].loc) ++q;
           const int slot = s_pc[q].slot, i = s_pc[q].i0 + (u - s_pc[q].loc);
-          const float* part = s_part + ((size_t)st * R + r) * nparts * 2;
+          const float* part = s_part + ((size_t)ps * R + r) * nparts * 2;
           float a = 0.f, uu = 0.f;
           for (int t = 0; t < nparts; ++t) {
             a += part[2 * t];
             uu += part[2 * t + 1];
           }
           const float hv = silu_f(a) * uu;
-          const float hw = s_w[slot] * hv;
+          const float hw = w_l[slot] * hv;
           float* dst = s_hb + (size_t)u * hb;
 #pragma unroll
           for (int t = 0; t < NV; ++t) dst[t] = hw * pos_scale<BITS>(t);
@@ -629,13 +659,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
         __threadfence_block();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bar_empty[st]);
+          mbar_arrive(&bar_pfree[ps]);
           st_release_shared(s_hdone, (uint32_t)l * (uint32_t)nstg + (uint32_t)k + 1u);
         }
       }
-      // the next layer's top-K, off its critical path; its ids are published
-      // only once that layer's input is complete
-      if (l + 1 < p.L) warp_topk(p.logits + (size_t)(l + 1) * p.E, p.E, p.K, nx_id, nx_l);
+      // the next layer's routing, off its critical path
+      if (l + 1 < p.L) publish(l + 1);
     }
   }
 
@@ -732,13 +761,16 @@ FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem
     if (block_pieces(NS, I, c, grid, lay, pc, kMaxPieces, b) > kMaxPieces) return pl;
     darea = b > darea ? b : darea;
   }
-  pl.darea_bytes = round_up_i(darea > H * 4 ? darea : H * 4, 128);
+  pl.darea_bytes = round_up_i(darea > 128 ? darea : 128, 128);
+  const int mw = (H / (32 / bits) + kDnThreads - 1) / kDnThreads;
+  const int mwp = mw <= 1 ? 1 : mw <= 2 ? 2 : 4;               // code words per down thread
   pl.hb = bits == 4 ? 8 : 12;
   pl.xs_off = kCtrlBytes;
   pl.part_off = round_up_i(pl.xs_off + (long long)H * 4, 128);
   for (int ns = kFusedStageCap; ns >= 2; --ns) {
-    pl.hbuf_off = round_up_i(pl.part_off + (long long)ns * R * nparts * 2 * 4, 128);
-    pl.darea_off = round_up_i(pl.hbuf_off + (long long)(pl.len_max + 1) * pl.hb * 4, 128);
+    pl.hbuf_off = round_up_i(pl.part_off + (long long)2 * ns * R * nparts * 2 * 4, 128);
+    pl.dscr_off = round_up_i(pl.hbuf_off + (long long)(pl.len_max + 1) * pl.hb * 4, 128);
+    pl.darea_off = round_up_i(pl.dscr_off + (long long)kDnThreads * (32 / bits) * mwp * 4, 128);
     pl.ring_off = pl.darea_off + pl.darea_bytes;
     const long long need = (long long)pl.ring_off + (long long)ns * pl.stage_bytes;
     if (need <= smem_max) {

@@ -94,8 +94,11 @@ constexpr int kMaxPieces = 4;          // slot ranges a block's columns may span
 constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, reductions
 // Tuning of the persistent kernel (compile-time; the defaults are the
 // measured best): ring stages at most, ring stages issued before a layer's
-// down columns, bytes per bulk copy, producer lanes that take turns issuing
-// copies, pause between two polls of the accumulators.
+// down columns, most bytes per bulk copy (the TMA unit spends about half a
+// microsecond per copy whatever its size, so a block streams fastest with
+// few large copies: 16 KB copies cap an SM near 33 GB/s, 32 KB and larger
+// near 47 GB/s), producer lanes that take turns issuing copies, pause
+// between two polls of the accumulators.
 #ifndef FMOE_FUSED_STAGE_CAP
 #define FMOE_FUSED_STAGE_CAP 8
 #endif
@@ -103,7 +106,7 @@ constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, redu
 #define FMOE_FUSED_DAREA_AFTER 2
 #endif
 #ifndef FMOE_FUSED_COPY_BYTES
-#define FMOE_FUSED_COPY_BYTES 16384
+#define FMOE_FUSED_COPY_BYTES (1u << 19)
 #endif
 #ifndef FMOE_FUSED_ISSUE_LANES
 #define FMOE_FUSED_ISSUE_LANES 4
@@ -111,6 +114,7 @@ constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, redu
 #ifndef FMOE_POLL_NS
 #define FMOE_POLL_NS 64
 #endif
+
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
 constexpr int kFusedDareaAfter = FMOE_FUSED_DAREA_AFTER;
 constexpr uint32_t kFusedCopyBytes = FMOE_FUSED_COPY_BYTES;
@@ -166,7 +170,7 @@ struct FusedPlan {
   int nstage, stage_bytes;  // ring
   int len_max;              // most intermediate columns a block owns
   int hb;                   // floats per column in the h buffer
-  int xs_off, part_off, hbuf_off, darea_off, darea_bytes, ring_off;
+  int xs_off, part_off, hbuf_off, dscr_off, darea_off, darea_bytes, ring_off;
 };
 
 struct FusedParams {

@@ -14,7 +14,7 @@ SMS, SMEM_MAX = 148, 232448          # B300: SMs, opt-in shared memory per block
 
 # index names of the geometry vector (include/fmoe.h, FMOE_GEO_*)
 NAMES = ["fused_ok", "fused_grid", "fused_smem", "fused_ctrl", "xs_off", "part_off", "hbuf_off", "hb",
-         "darea_off", "darea_bytes", "ring_off", "nstage", "stage_bytes", "R", "nparts", "len_max",
+         "dscr_off", "darea_off", "darea_bytes", "ring_off", "nstage", "stage_bytes", "R", "nparts", "len_max",
          "batch_grid", "G", "gu_warps", "gu_rows", "gu_nstage", "gu_stage", "gu_xs", "gu_smem",
          "d_rows", "d_h", "d_smem", "batch_ctrl"]
 
@@ -74,15 +74,17 @@ def test_geometry(fm, bits, H, I, K, S):
     assert g["fused_grid"] == SMS
     assert g["xs_off"] >= g["fused_ctrl"]
     assert g["part_off"] >= g["xs_off"] + H * 4
-    assert g["hbuf_off"] >= g["part_off"] + g["nstage"] * g["R"] * g["nparts"] * 2 * 4
+    assert g["hbuf_off"] >= g["part_off"] + 2 * g["nstage"] * g["R"] * g["nparts"] * 2 * 4
     assert g["hb"] >= (5 if bits == 4 else 9)
     assert g["len_max"] == -(-NS * I // SMS)
-    assert g["darea_off"] >= g["hbuf_off"] + g["len_max"] * g["hb"] * 4
-    assert g["darea_bytes"] >= H * 4                      # the down warps' row-order buffer
+    assert g["dscr_off"] >= g["hbuf_off"] + g["len_max"] * g["hb"] * 4
+    words = H // (32 // bits)                              # code words per down column
+    mw = 1 if words <= 256 else 2 if words <= 512 else 4   # per down thread
+    assert g["darea_off"] >= g["dscr_off"] + 256 * (32 // bits) * mw * 4   # the down warps' transpose scratch
     assert g["ring_off"] >= g["darea_off"] + g["darea_bytes"]
     assert g["nstage"] >= 2 and g["stage_bytes"] >= g["R"] * gu_row
     assert g["fused_smem"] == g["ring_off"] + g["nstage"] * g["stage_bytes"] <= SMEM_MAX
-    for k in ("xs_off", "part_off", "hbuf_off", "darea_off", "darea_bytes", "ring_off", "stage_bytes"):
+    for k in ("xs_off", "part_off", "hbuf_off", "dscr_off", "darea_off", "darea_bytes", "ring_off", "stage_bytes"):
         assert g[k] % 128 == 0, k            # bulk-copy destinations: 16-byte aligned at least
     # every block's columns fit its down area, each copy 16-byte aligned
     covered = 0
