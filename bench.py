@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--chain", type=int, default=CHAIN,
                     help="blocks per step for the single-block workloads (1..64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations measured with the default workload")
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="run only this many steps (for an ncu launch list); prints no JSON")
     return ap.parse_args()
@@ -236,36 +238,78 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (bounded sample)
 # ---------------------------------------------------------------------------
+def _one_thread_worker():
+    import torch
+    torch.set_num_threads(1)
+
+
+def _oracle_expert_ffn(path, bits, hidden, inter, x):
+    """One active expert of a block by the oracle: its blob (written beforehand,
+    read through the page cache), dequantised, fp64 gate/up/down matvecs +
+    SwiGLU.  Top level for a spawned worker."""
+    import numpy as np
+    import oracle
+    blob = np.load(path, mmap_mode="r")
+    return oracle.expert_ffn(oracle.expert_weights(np.asarray(blob), bits, hidden, inter), x)
+
+
 def oracle_sample(shape, n_blocks, seed_tag=0):
-    """Time the fp64 oracle on `n_blocks` blocks of the workload (inputs made first).
-    Returns (seconds per block, threads used, description)."""
+    """Time the fp64 oracle on blocks of the workload: every active expert of a
+    block (dequantise + fp64 matvecs) as one task, the block's routing and
+    combine in this process.  The experts' blobs are generated and written to
+    a temporary directory first (input preparation, not timed).  Run on every
+    core this process may use (len(os.sched_getaffinity(0)) spawned worker
+    processes, one thread each) over n_blocks blocks, and on one core over a
+    quarter of them.  Returns ({"all": s/block, "one": s/block}, cores, text)."""
+    import concurrent.futures
+    import multiprocessing
+    import tempfile
     import numpy as np
     import oracle
     import synth
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:  # noqa: BLE001
-        threads = 1
     K = shape.top_k
     inp = synth.block_inputs(shape, n_blocks, tag=1000 + seed_tag)
-    blobs = []
+    ncores = len(os.sched_getaffinity(0))
+    tmp = tempfile.TemporaryDirectory(prefix="oracle_blobs_")
+    tasks = []
     for b in range(n_blocks):
         ids, _ = oracle.route(inp.logits[b].numpy(), K)
-        ex = {int(e): synth.expert_blob(shape, 0, int(e)).numpy().view(np.uint8) for e in ids}
-        sh = synth.expert_blob(shape, 0, shape.n_experts + b).numpy().view(np.uint8) if shape.has_shared else None
-        blobs.append((ex, sh))
+        experts = [int(e) for e in ids] + ([shape.n_experts + b] if shape.has_shared else [])
+        for e in experts:
+            path = os.path.join(tmp.name, f"b{b}_e{e}.npy")
+            np.save(path, synth.expert_blob(shape, 0, e).numpy().view(np.uint8))
+            tasks.append((path, shape.bits, shape.hidden, shape.inter, inp.x[b].numpy().astype(np.float64)))
+    per = K + (1 if shape.has_shared else 0)
     wsg = synth.shared_gate_vector(shape).numpy().view(np.uint16) if shape.has_shared else None
-    t0 = time.perf_counter()
-    for b in range(n_blocks):
-        ex, sh = blobs[b]
-        get = lambda e, ex=ex: oracle.expert_weights(ex[e], shape.bits, shape.hidden, shape.inter)
-        shw = oracle.expert_weights(sh, shape.bits, shape.hidden, shape.inter) if sh is not None else None
-        oracle.moe_block(get, inp.x[b].numpy(), inp.logits[b].numpy(), inp.residual[b].numpy(), K, shw, wsg)
-    dt = (time.perf_counter() - t0) / n_blocks
-    desc = (f"{n_blocks} block(s) of {shape.name}: dequantise the {K + (1 if shape.has_shared else 0)} "
-            f"active experts + fp64 matvecs + combine (numpy/OpenBLAS), inputs prepared beforehand")
-    return dt, threads, desc
+    saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    out = {}
+    try:
+        ctx = multiprocessing.get_context("spawn")
+        for label, workers, nb in (("all", ncores, n_blocks), ("one", 1, max(1, n_blocks // 4))):
+            with concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx,
+                                                        initializer=_one_thread_worker) as pool:
+                list(pool.map(int, range(workers)))                 # start the workers
+                t0 = time.perf_counter()
+                ys = list(pool.map(_oracle_expert_ffn, *zip(*tasks[:nb * per])))
+                for b in range(nb):
+                    ids, w = oracle.route(inp.logits[b].numpy(), K)
+                    yb = ys[b * per:(b + 1) * per]
+                    g = oracle.shared_gate(wsg, inp.x[b].numpy()) if shape.has_shared else None
+                    oracle.combine(inp.residual[b].numpy(), yb[:K], w, yb[K] if shape.has_shared else None, g)
+                out[label] = (time.perf_counter() - t0) / nb
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        tmp.cleanup()
+    desc = (f"{n_blocks} block(s) of {shape.name} on {ncores} cores ({n_blocks // 4 or 1} on one core): each active "
+            f"expert ({per} per block) dequantised and run through fp64 matvecs + SwiGLU in a spawned worker "
+            f"process with one thread, then routing and combine (numpy); blobs generated beforehand")
+    return out, ncores, desc
 
 
 def run_reference(args):
@@ -278,11 +322,10 @@ def run_reference(args):
     import numpy as np
     import oracle
     import synth
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:  # noqa: BLE001
-        threads = 1
+    # the oracle as it stands, on one host core: numpy's BLAS held to one thread
+    from threadpoolctl import threadpool_limits
+    threadpool_limits(1)
+    threads = 1
     shape, n_layers = workload_desc(args.workload, args.chain)
     inp = synth.block_inputs(shape, 1, tag=500)
     ids, _ = oracle.route(inp.logits[0].numpy(), shape.top_k)
@@ -320,7 +363,7 @@ def run_reference(args):
     el = time.perf_counter() - t0
     dt = el / max(args.steps, 1)
     gbs = nbytes / el / 1e9
-    desc = (f"per step the first {frac:.3f} of the intermediate columns of one active expert of a {shape.name} block "
+    desc = (f"one host core; per step the first {frac:.3f} of the intermediate columns of one active expert of a {shape.name} block "
             f"(dequantise + fp64 gate/up/down matvecs + SwiGLU, numpy/OpenBLAS), cycling over the "
             f"block's {len(blobs)} experts; value = packed bytes processed per second")
     line = {
@@ -340,27 +383,21 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # batched block with Zipf routing: unique-expert bytes per second
 # ---------------------------------------------------------------------------
-def run_batch(args):
+def measure_batch(T, steps, warmup, dev):
     """T tokens through one Qwen-shaped 4-bit block (fmoe_moe_block, batched
-    path) with Zipf(1.1) routing; value = distinct experts' bytes (routed +
-    shared) per second.  Each step is one graph replay of the block's launches
-    over one of NSETS input sets.  L2 is flushed before every timed step,
-    outside its events, by a read of 256 MiB: that leaves L2 holding clean
-    lines only (a write would leave dirty lines whose write-back would land in
-    the timed region)."""
+    path; the persistent kernel at T = 1) with Zipf(1.1) routing.  Each step is
+    one graph replay of the block's launches over one of NSETS input sets; L2 is
+    flushed before every timed step, outside its events, by a read of 256 MiB
+    (a read leaves L2 holding clean lines only: a write would leave dirty lines
+    whose write-back would land in the timed region).  Returns a dict."""
     import torch
-    from quantized_moe_expert_05_b300 import build
-    build.build()
     from quantized_moe_expert_05_b300 import fmoe as fm
     import synth
 
-    T = args.tokens
     if not 1 <= T <= 16:
         raise ValueError("--tokens must be in 1..16")
     shape = synth.QWEN_Q4_BATCH
     K = shape.top_k
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
     nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
     pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
     synth.fill_pool(pool, shape, 0, 0, shape.n_experts)
@@ -393,13 +430,13 @@ def run_batch(args):
         graphs.append(g)
     flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    for i in range(args.warmup):
+    for i in range(warmup):
         graphs[i % NSETS].replay()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     nbytes = 0
-    with ClockSampler(0) as clocks:
-        for i in range(args.steps):
+    with ClockSampler(dev.index or 0) as clocks:
+        for i in range(steps):
             flush.sum()
             evs[i][0].record(stream)
             graphs[i % NSETS].replay()
@@ -410,20 +447,41 @@ def run_batch(args):
     if fm.last_device_error(ws) != fm.OK:
         raise RuntimeError("device error in the timed region")
     value = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = load_peaks()
+    del pool, shared, graphs, flush
+    torch.cuda.empty_cache()
+    return {"T": T, "gbs": value, "frac": value / peak, "ms_per_step": ms / steps,
+            "tokens_per_s": T * steps / (ms * 1e-3), "distinct_experts_per_step": uniq,
+            "launches_per_step": 1 if T == 1 else 4, "clocks": clocks.summary()}
+
+
+def run_batch(args):
+    """--workload qwen_q4_zipf: the batched block at --tokens T; value =
+    distinct experts' bytes (routed + shared) per second."""
+    import torch
+    from quantized_moe_expert_05_b300 import build
+    build.build()
+    import synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    r = measure_batch(args.tokens, args.steps, args.warmup, dev)
     peak, peak_kind = load_peaks()
+    shape = synth.QWEN_Q4_BATCH
     line = {
-        "metric": "unique-expert GB/s (batched block, Zipf routing)", "value": value, "unit": "GB/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "metric": "unique-expert GB/s (batched block, Zipf routing)", "value": r["gbs"], "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{shape.name}: T={T} tokens through one block, Zipf(1.1) routing",
-                   "distinct_experts_per_step": uniq, "l2": "flushed (256 MiB read) before every step"},
-        "tokens_per_s": T * args.steps / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+        "config": {"workload": f"{shape.name}: T={args.tokens} tokens through one block, Zipf(1.1) routing",
+                   "distinct_experts_per_step": r["distinct_experts_per_step"],
+                   "l2": "flushed (256 MiB read) before every step"},
+        "tokens_per_s": r["tokens_per_s"],
+        "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": peak, "unit": "GB/s", "frac": r["frac"],
                      "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)", "traffic": None,
-                     "kernel": "plan + gate/up + down + combine (4 launches, one graph)"},
-        "gpu_launches": 4 * args.steps,
-        "clocks": clocks.summary(),
+                     "kernel": "plan + gate/up + down + combine (4 launches, one graph)" if args.tokens > 1
+                     else "fused_moe_kernel (one launch)"},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": r["clocks"],
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -432,6 +490,167 @@ def run_batch(args):
 # ---------------------------------------------------------------------------
 # CUDA path
 # ---------------------------------------------------------------------------
+def build_chain(shape, n_layers, dev, rank):
+    """Pools, layers, workspace and NSETS input sets of a decode chain/stack.
+    A stack has its own routed pool per layer; a chain shares one routed pool
+    and gives every block its own shared expert and gate vector."""
+    import dataclasses
+    import torch
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+    K = shape.top_k
+    S = 1 if shape.has_shared else 0
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+    layers, keep = [], []
+    if shape.n_layers > 1:
+        for l in range(n_layers):
+            pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
+            synth.fill_pool(pool, shape, l, 0, shape.n_experts)
+            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool))
+    else:
+        pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
+        synth.fill_pool(pool, shape, 0, 0, shape.n_experts)
+        shared = None
+        if S:
+            shared = torch.empty(n_layers * nw, dtype=torch.int32, device=dev)
+            synth.fill_pool(shared, shape, 0, shape.n_experts, n_layers)
+        for l in range(n_layers):
+            sh = shared[l * nw:(l + 1) * nw] if S else None
+            wsg = synth.shared_gate_vector(shape, l).to(dev) if S else None
+            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool, sh, wsg))
+    ws = fm.new_workspace(layers[0], 1, K, n_layers)
+    NSETS = 8
+    h0, logits = synth.stack_inputs(
+        dataclasses.replace(shape, seed=shape.seed + 1000 * rank, n_layers=n_layers), NSETS)
+    return layers, ws, h0, logits
+
+
+def measure_chain(shape, n_layers, steps, warmup, dev, local, world, rank, e2e=True, repeats=5):
+    """Decode steps (one token through n_layers blocks, one persistent launch)
+    timed with CUDA events on the launching stream.  The step graph (input copy
+    + launch) and the launch alone are timed interleaved over `repeats`
+    rounds; the medians are reported, so the launch time never exceeds the step
+    time because of drift between two separate loops.  Optionally end to end
+    through the C ABI with pinned host inputs and the result copied back."""
+    import torch
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    K = shape.top_k
+    layers, ws, h0, logits = build_chain(shape, n_layers, dev, rank)
+    NSETS = h0.shape[0]
+    h0_d, lg_d = h0.to(dev), logits.to(dev)
+    h = torch.empty(shape.hidden, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        h.copy_(h0_d[i % NSETS])
+        fm.stack_decode(layers, lg_d[i % NSETS], h, K, shape.eps, ws)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    graphs, kgraphs = [], []
+    for i in range(NSETS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(i)
+        graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fm.stack_decode(layers, lg_d[i % NSETS], h, K, shape.eps, ws)
+        kgraphs.append(g)
+    for i in range(warmup):
+        graphs[i % NSETS].replay()
+    torch.cuda.synchronize()
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    per = max(1, steps // repeats)
+    step_ms, kern_ms = [], []
+    total_ms = 0.0
+    barrier()
+    with ClockSampler(local) as clocks:
+        done = 0
+        for r in range(repeats):
+            n = per if r < repeats - 1 else steps - per * (repeats - 1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            for i in range(n):
+                graphs[(done + i) % NSETS].replay()
+            ev[1].record(stream)
+            ev[2].record(stream)
+            for i in range(n):
+                kgraphs[(done + i) % NSETS].replay()
+            ev[3].record(stream)
+            ev[3].synchronize()
+            t = ev[0].elapsed_time(ev[1])
+            total_ms += t
+            step_ms.append(t / n)
+            kern_ms.append(ev[2].elapsed_time(ev[3]) / n)
+            done += n
+    barrier()
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    res = {"ms_per_step": statistics.median(step_ms), "launch_ms": statistics.median(kern_ms),
+           "total_ms": total_ms, "step_ms_repeats": step_ms, "launch_ms_repeats": kern_ms,
+           "clocks": clocks.summary()}
+    if e2e:
+        h0_host = h0.pin_memory()
+        lg_host = logits.pin_memory()
+        out_host = torch.empty((steps, shape.hidden), dtype=torch.float32).pin_memory()
+        lg_step = torch.empty_like(lg_d[0])
+        for i in range(3):
+            h.copy_(h0_host[i % NSETS], non_blocking=True)
+            lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
+            fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
+            out_host[i].copy_(h, non_blocking=True)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            h.copy_(h0_host[i % NSETS], non_blocking=True)
+            lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
+            fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
+            out_host[i].copy_(h, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        barrier()
+        res["e2e_ms"] = e0.elapsed_time(e1)
+        res["h2d"] = h0_host[0].numel() * 4 + lg_host[0].numel() * 4
+        res["d2h"] = shape.hidden * 4
+        if fm.last_device_error(ws) != fm.OK:
+            raise RuntimeError("device-side wait timed out in the end-to-end steps")
+    del layers, ws, graphs, kgraphs
+    torch.cuda.empty_cache()
+    return res
+
+
+def fused_mw(shape):
+    """Code words of a down column per down thread (the kernel's template argument)."""
+    words = shape.hidden // (32 // shape.bits)
+    mw = -(-words // 256)
+    return 1 if mw <= 1 else 2 if mw <= 2 else 4
+
+
+def chain_summary(shape, n_layers, r):
+    """Derived figures of one measured chain or stack."""
+    per_step = bytes_per_token(shape, n_layers)
+    peak, _ = load_peaks()
+    gbs = per_step / (r["ms_per_step"] * 1e-3) / 1e9
+    achieved = per_step / (r["launch_ms"] * 1e-3) / 1e9
+    return {"workload": workload_name(shape, n_layers), "gbs": gbs, "frac": gbs / peak,
+            "launch_ms": r["launch_ms"], "ms_per_step": r["ms_per_step"],
+            "kernel_gbs": achieved, "kernel_frac": achieved / peak,
+            "us_per_block": r["ms_per_step"] * 1e3 / n_layers,
+            "tokens_per_s_stack": 1e3 / r["ms_per_step"],
+            "tokens_per_s_per_block": n_layers * 1e3 / r["ms_per_step"]}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -456,147 +675,33 @@ def main():
 
     shape, n_layers = workload_desc(args.workload, args.chain)
     K = shape.top_k
-    S = 1 if shape.has_shared else 0
-    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
-
-    # expert pools: a stack has its own routed pool per layer; a chain shares
-    # one routed pool and gives every block its own shared expert
-    layers = []
-    if shape.n_layers > 1:
-        for l in range(n_layers):
-            pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
-            synth.fill_pool(pool, shape, l, 0, shape.n_experts)
-            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool))
-    else:
-        pool = torch.empty(shape.n_experts * nw, dtype=torch.int32, device=dev)
-        synth.fill_pool(pool, shape, 0, 0, shape.n_experts)
-        shared = None
-        if S:
-            shared = torch.empty(n_layers * nw, dtype=torch.int32, device=dev)
-            synth.fill_pool(shared, shape, 0, shape.n_experts, n_layers)
-        for l in range(n_layers):
-            sh = shared[l * nw:(l + 1) * nw] if S else None
-            wsg = synth.shared_gate_vector(shape, l).to(dev) if S else None
-            layers.append(fm.Layer(shape.bits, shape.hidden, shape.inter, shape.n_experts, pool, sh, wsg))
-    ws = fm.new_workspace(layers[0], 1, K, n_layers)
-
-    # per-step inputs: NSETS distinct (h0, logits) sets, cycled
-    NSETS = 8
-    import dataclasses
-    h0, logits = synth.stack_inputs(
-        dataclasses.replace(shape, seed=shape.seed + 1000 * rank, n_layers=n_layers), NSETS)
-    h0_d, lg_d = h0.to(dev), logits.to(dev)
-    h = torch.empty(shape.hidden, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(i):
-        h.copy_(h0_d[i % NSETS])
-        fm.stack_decode(layers, lg_d[i % NSETS], h, K, shape.eps, ws)
 
     if args.profile_launches:
         # the steps sit in an NVTX range so that an ncu launch list can skip
         # the pool generation (ncu --nvtx --nvtx-include "steps/")
+        layers, ws, h0, logits = build_chain(shape, n_layers, dev, rank)
+        h = torch.empty(shape.hidden, dtype=torch.float32, device=dev)
+        h0_d, lg_d = h0.to(dev), logits.to(dev)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("steps")
         for i in range(args.profile_launches):
-            step(i)
+            h.copy_(h0_d[i % h0.shape[0]])
+            fm.stack_decode(layers, lg_d[i % h0.shape[0]], h, K, shape.eps, ws)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         assert fm.last_device_error(ws) == fm.OK
         return 0
 
-    # graph of NSETS steps (one persistent launch + one 16 KB copy each)
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    graphs = []
-    for i in range(NSETS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step(i)
-        graphs.append(g)
-    # the fused kernel alone (no input copy), for the roofline's launch time
-    kgraphs = []
-    for i in range(NSETS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fm.stack_decode(layers, lg_d[i % NSETS], h, K, shape.eps, ws)
-        kgraphs.append(g)
-
-    for i in range(args.warmup):
-        graphs[i % NSETS].replay()
-    torch.cuda.synchronize()
-    if fm.last_device_error(ws) != fm.OK:
-        raise RuntimeError("device-side wait timed out during warm-up")
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    # kernel-only timing: events around K graph replays on the launching stream
-    barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % NSETS].replay()
-        ev1.record(stream)
-        ev1.synchronize()
-    barrier()
-    ms = ev0.elapsed_time(ev1)
-    if fm.last_device_error(ws) != fm.OK:
-        raise RuntimeError("device-side wait timed out in the timed region")
-
-    # average duration of one fused launch: the same replays without the copy
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for i in range(args.steps):
-        kgraphs[i % NSETS].replay()
-    k1.record(stream)
-    k1.synchronize()
-    kernel_ms = k0.elapsed_time(k1) / args.steps
-    if fm.last_device_error(ws) != fm.OK:
-        raise RuntimeError("device-side wait timed out in the kernel-only replays")
-
-    # end-to-end through the C ABI: pinned host inputs in, result out, every step
-    h0_host = h0.pin_memory()
-    lg_host = logits.pin_memory()
-    out_host = torch.empty((args.steps, shape.hidden), dtype=torch.float32).pin_memory()
-    lg_step = torch.empty_like(lg_d[0])
-    for i in range(3):
-        h.copy_(h0_host[i % NSETS], non_blocking=True)
-        lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
-        fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
-        out_host[i].copy_(h, non_blocking=True)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        h.copy_(h0_host[i % NSETS], non_blocking=True)
-        lg_step.copy_(lg_host[i % NSETS], non_blocking=True)
-        fm.stack_decode(layers, lg_step, h, K, shape.eps, ws)
-        out_host[i].copy_(h, non_blocking=True)
-    e1.record(stream)
-    e1.synchronize()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    h2d = h0_host[0].numel() * 4 + lg_host[0].numel() * 4
-    d2h = shape.hidden * 4
-
-    # max over ranks
-    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev, world)
-
+    r = measure_chain(shape, n_layers, args.steps, args.warmup, dev, local, world, rank, e2e=True)
+    # max over ranks (the slowest rank's time)
+    ms_total, e2e_ms = max_over_ranks([r["total_ms"], r["e2e_ms"]], dev, world)
     per_step = bytes_per_token(shape, n_layers)
-    value = job_gbs(per_step, args.steps, world, ms)
+    value = job_gbs(per_step, args.steps, world, ms_total)
     e2e_value = job_gbs(per_step, args.steps, world, e2e_ms)
-    ms_step = ms / args.steps
-    # algorithmic bytes of one fused launch over its average launch time
-    achieved = per_step / (kernel_ms * 1e-3) / 1e9
+    ms_step = r["ms_per_step"]
+    achieved = per_step / (r["launch_ms"] * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
     traffic = committed_traffic(args.workload)
-    clk = clocks.summary()
 
     if rank != 0:
         return 0
@@ -611,22 +716,42 @@ def main():
             "l2": "inputs larger than L2: each step streams "
                   f"{per_step / 1e9:.2f} GB of expert weights (L2 126 MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "timing": "step graph and launch-only graph timed interleaved over 5 rounds; medians",
         },
-        "tokens_per_s_per_block": n_layers * args.steps * world / (ms * 1e-3),
-        "tokens_per_s_stack": args.steps * world / (ms * 1e-3),
+        "tokens_per_s_per_block": n_layers * 1e3 / ms_step,
+        "tokens_per_s_stack": 1e3 / ms_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)",
-                     "traffic": traffic, "kernel": f"fused_moe_kernel<{shape.bits}>",
-                     "algorithmic_bytes_per_launch": per_step, "launch_ms": kernel_ms},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                     "traffic": traffic,
+                     "kernel": f"fused_moe_kernel<{shape.bits}, {fused_mw(shape)}>",
+                     "algorithmic_bytes_per_launch": per_step, "launch_ms": r["launch_ms"],
+                     "frac_of_nominal_8tbs": achieved / 8000.0},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": args.steps,
-        "clocks": clk,
+        "clocks": r["clocks"],
     }
+    if world == 1 and not args.no_configs and args.workload == "qwen_q4":
+        # the other configurations of the workload family, measured in the same run
+        cfgs = {}
+        q2 = measure_chain(synth.QWEN_Q2, CHAIN, 100, 5, dev, local, 1, 0, e2e=False)
+        cfgs["qwen_q2_chain64"] = chain_summary(synth.QWEN_Q2, CHAIN, q2)
+        st = measure_chain(synth.STACK48, synth.STACK48.n_layers, 64, 4, dev, local, 1, 0, e2e=False)
+        cfgs["stack48"] = chain_summary(synth.STACK48, synth.STACK48.n_layers, st)
+        cfgs["stack48"]["tokens_per_s_per_full_stack"] = cfgs["stack48"]["tokens_per_s_stack"]
+        cfgs["qwen_q4_zipf"] = {}
+        for T in (1, 2, 4, 8, 16):
+            b = measure_batch(T, 50, 3, dev)
+            cfgs["qwen_q4_zipf"][f"T{T}"] = {k: b[k] for k in ("gbs", "frac", "ms_per_step", "tokens_per_s",
+                                                                "launches_per_step")}
+        line["configs"] = cfgs
     if world == 1 and not args.no_cpu_baseline:
-        n = 2 if shape.hidden >= 4096 else 4
-        dt, threads, desc = oracle_sample(shape, n)
-        line["cpu_baseline"] = {"value": bytes_per_token(shape, 1) / dt / 1e9, "unit": "GB/s", "cores": threads,
-                                "kind": "oracle", "sample": desc}
+        n = 16 if shape.hidden >= 4096 else 32
+        dts, ncores, desc = oracle_sample(shape, n)
+        bpb = bytes_per_token(shape, 1)
+        line["cpu_baseline"] = {"value": bpb / dts["all"] / 1e9, "unit": "GB/s", "cores": ncores,
+                                "kind": "oracle", "sample": desc, "s_per_block": dts["all"],
+                                "one_core": {"value": bpb / dts["one"] / 1e9, "unit": "GB/s", "cores": 1,
+                                             "s_per_block": dts["one"]}}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

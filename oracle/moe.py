@@ -112,7 +112,8 @@ def part_rows(blob: np.ndarray, bits: int, hidden: int, inter: int, name: str, n
         raise ValueError("blob too small")
     off, stride, rows, wpr = parts[name]
     n = rows if n is None else n
-    return np.stack([words[(off + r * stride) // 4: (off + r * stride) // 4 + wpr] for r in range(n)])
+    index = (off + np.arange(n)[:, None] * stride) // 4 + np.arange(wpr)[None, :]
+    return words[index]
 
 
 def expert_weights(blob: np.ndarray, bits: int, hidden: int, inter: int) -> tuple:

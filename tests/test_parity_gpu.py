@@ -15,7 +15,8 @@ import torch
 
 import oracle
 import synth
-from fmoe_testlib import TOL, assert_close, gpu_pool, make_layer, oracle_block, oracle_expert, rel_errors
+from fmoe_testlib import (STACK_FLOOR, TOL, assert_close, gpu_pool, make_layer, oracle_block, oracle_expert,
+                          oracle_pool, oracle_stack_token, rel_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -389,16 +390,45 @@ def stack48_layers(fm):
 
 
 def test_stack48_tokens(fm, stack48_layers):
+    """The first 8 tokens of the 48-layer stack (H 2048, 512 experts per layer,
+    top-10, I 512) through all 48 layers: ids of every layer exact, h within
+    the tolerance.  The oracle runs in a spawned process pool."""
     shape = synth.STACK48
+    T = 8
     ws = fm.new_workspace(stack48_layers[0], 1, shape.top_k, shape.n_layers)
-    h0, logits = synth.stack_inputs(shape, 1)
-    for t in range(1):
+    h0, logits = synth.stack_inputs(shape, T)
+    with oracle_pool() as pool:
+        futs = [pool.submit(oracle_stack_token, shape, h0[t].numpy(), logits[t].numpy(), shape.top_k)
+                for t in range(T)]
+        for t in range(T):
+            h = h0[t].clone().cuda()
+            fm.stack_decode(stack48_layers, logits[t].cuda(), h, shape.top_k, shape.eps, ws)
+            torch.cuda.synchronize()
+            assert fm.last_device_error(ws) == fm.OK
+            got_ids = fm.ws_routing(ws, stack48_layers[0], shape.n_layers, shape.top_k)["ids"].cpu().numpy()
+            ref, ids = futs[t].result()
+            assert np.array_equal(got_ids, np.asarray(ids)), f"token {t}: routing differs"
+            assert_close(h.cpu().numpy(), ref, what=f"stack48 token {t}", floor=STACK_FLOOR)
+
+
+def test_ragged_stack_general_path(fm):
+    """A stack whose shape the single-launch kernel does not take (H/32 = 6
+    slices) runs per layer on the general path (RMSNorm launch + batched
+    block), against the oracle."""
+    shape = synth.BlockShape("ragged_stack_h192_e6_top3_i320_q4", 192, 320, 6, 3, True, 4, 0.002, 0.02, -0.1,
+                             0.0, seed=41, n_layers=3)
+    layers = [make_layer(fm, shape, layer=l) for l in range(shape.n_layers)]
+    ws = fm.new_workspace(layers[0], 1, shape.top_k, shape.n_layers)
+    h0, logits = synth.stack_inputs(shape, 2)
+    for t in range(2):
         h = h0[t].clone().cuda()
-        fm.stack_decode(stack48_layers, logits[t].cuda(), h, shape.top_k, shape.eps, ws)
+        fm.stack_decode(layers, logits[t].cuda(), h, shape.top_k, shape.eps, ws)
         torch.cuda.synchronize()
         assert fm.last_device_error(ws) == fm.OK
-        ref, ids = _oracle_stack(shape, h0[t].numpy(), logits[t].numpy(), shape.top_k)
-        assert_close(h.cpu().numpy(), ref, what=f"stack48 token {t}")
+        ref, ids = oracle_stack_token(shape, h0[t].numpy(), logits[t].numpy(), shape.top_k, shared=True)
+        got_ids = fm.ws_routing(ws, layers[0], shape.n_layers, shape.top_k)["ids"].cpu().numpy()
+        assert np.array_equal(got_ids, np.asarray(ids))
+        assert_close(h.cpu().numpy(), ref, what=f"ragged stack token {t}")
 
 
 # ---------------------------------------------------------------------------
@@ -421,12 +451,13 @@ def _oracle_chain(shape, h0, logits):
                                lambda l: synth.shared_gate_vector(shape, l).numpy().view(np.uint16))
 
 
-def test_qwen_chain_as_benched(fm, qwen_pools):
-    """Four chained Qwen 4-bit blocks against the oracle; then the 64-block
-    launch the bench times equals sixteen 4-block launches bit for bit (every
-    block runs the same code on the same input whichever launch it is in)."""
+@pytest.mark.parametrize("shape", [synth.QWEN_Q4, synth.QWEN_Q2], ids=lambda s: s.name)
+def test_qwen_chain_as_benched(fm, qwen_pools, shape):
+    """Four chained Qwen blocks (4-bit and 2-bit) against the oracle; then the
+    64-block launch the bench times equals sixteen 4-block launches bit for
+    bit (every block runs the same code on the same input whichever launch it
+    is in, and the blocks' partial sums are added in exact integer arithmetic)."""
     import dataclasses
-    shape = synth.QWEN_Q4
     n = 64
     layers = _qwen_chain_layers(fm, shape, n, qwen_pools[shape.name])
     h0, logits = synth.stack_inputs(dataclasses.replace(shape, n_layers=n), 1)
@@ -436,7 +467,7 @@ def test_qwen_chain_as_benched(fm, qwen_pools):
     torch.cuda.synchronize()
     assert fm.last_device_error(ws) == fm.OK
     ref, ids = _oracle_chain(dataclasses.replace(shape, n_layers=4), h0[0].numpy(), logits[0, :4].numpy())
-    assert_close(h4.cpu().numpy(), ref, what="4-block Qwen chain")
+    assert_close(h4.cpu().numpy(), ref, what=f"4-block chain {shape.name}")
     got_ids = fm.ws_routing(ws, layers[0], 4, shape.top_k)["ids"].cpu().numpy()
     assert np.array_equal(got_ids, np.asarray(ids)), (got_ids, ids)
 

@@ -5,17 +5,21 @@ example code that runs inside an allocator or memory-pool callback, a plugin
 whose host framework owns every device allocation, or a real-time loop that
 must not block in cudaMalloc.  It keeps its scratch in a fixed array inside
 the library instead of a workspace.  These tests call it through the C ABI
-and check that two calls in a row give what fmoe_moe_block (with a workspace)
-gives for the same inputs.
+and check two calls in a row against fmoe_moe_block (with a workspace) and
+against the fp64 oracle, at the tiny, a small, the Qwen-shaped 4-bit and the
+48-layer stack's block shapes, and with shapes of different K and
+intermediate size alternating from call to call (the array keeps the last
+call's contents).
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
 """
+import numpy as np
 import pytest
 import torch
 
 import synth
-from fmoe_testlib import TOL, assert_close, make_layer
+from fmoe_testlib import TOL, assert_close, make_layer, oracle_block
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +56,40 @@ def test_noalloc_matches_workspace_call_twice(fm, shape):
         assert fm.last_device_error(ws) == fm.OK
         assert int(err.item()) == 0, "device-side error word of the scratch-free call"
         assert_close(got.cpu().numpy()[0], want.cpu().numpy()[0], tol=TOL, what=f"{shape.name} call {tag}")
+
+
+def _check_against_oracle(fm, layer, shape, tag, err):
+    inp = synth.block_inputs(shape, 1, tag=tag)
+    got = fm.moe_block_noalloc(layer, inp.x.cuda(), inp.logits.cuda(), inp.residual.cuda(), shape.top_k,
+                               device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device-side error word of the scratch-free call"
+    ref = oracle_block(shape, 0, inp.x.numpy(), inp.logits.numpy(), inp.residual.numpy(), shape.top_k)
+    assert_close(got.cpu().numpy()[0], ref["out"][0], what=f"{shape.name} tag {tag} against the oracle")
+
+
+STACK_BLOCK = synth.BlockShape("stack_block_h2048_e512_top10_i512_q4", 2048, 512, 512, 10, False, 4,
+                               0.002, 0.02, -0.1, 0.0, seed=4)
+
+
+@pytest.mark.parametrize("shape", [synth.QWEN_Q4, STACK_BLOCK], ids=lambda s: s.name)
+def test_noalloc_matches_oracle_at_full_size(fm, shape):
+    layer = make_layer(fm, shape)
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for tag in (200, 201):                               # two calls in a row
+        _check_against_oracle(fm, layer, shape, tag, err)
+
+
+def test_noalloc_alternating_shapes(fm):
+    """Calls with different K and intermediate size in a row: nothing a call
+    leaves in the shared array changes the next call's result."""
+    shapes = [synth.TINY, synth.QWEN_Q4, SHARED_SMALL, synth.TINY, synth.QWEN_Q4]
+    layers = {}
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for i, shape in enumerate(shapes):
+        if shape.name not in layers:
+            layers[shape.name] = make_layer(fm, shape)
+        _check_against_oracle(fm, layers[shape.name], shape, 300 + i, err)
 
 
 def test_noalloc_in_place_and_without_error_output(fm):
