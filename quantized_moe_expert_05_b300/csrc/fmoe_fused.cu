@@ -486,23 +486,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
         // the down area may be refilled for the next layer
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_ddone);
-        // Each warp owns 32*RW*MW consecutive rows; a transpose through the
-        // warp's own scratch lets every red instruction of the warp add 32
+        // Each warp owns 32*E consecutive rows (E = RW*MW per thread); a
+        // transpose through the warp's own 128-float scratch, four rows per
+        // lane at a time, lets every red instruction of the warp add 32
         // consecutive rows (coalesced), with no wait on the other down warps.
         {
-          float* scr = s_dscr + (size_t)(warp - kGuWarps) * 32 * RW * MW;
-          const int r0 = (warp - kGuWarps) * 32 * RW * MW;    // the warp's first row
-          __syncwarp();
+          constexpr int E = RW * MW;
+          float* scr = s_dscr + (size_t)(warp - kGuWarps) * 128;
+          const int r0 = (warp - kGuWarps) * 32 * E;          // the warp's first row
 #pragma unroll
-          for (int t = 0; t < RW * MW; t += 4)
-            *reinterpret_cast<float4*>(scr + lane * RW * MW + t) =
-                make_float4(outp[t], outp[t + 1], outp[t + 2], outp[t + 3]);
-          __syncwarp();
-          if (!*s_abort && r0 < H) {
-#pragma unroll 4
-            for (int t = 0; t < RW * MW; ++t)
-              if (r0 + 32 * t + lane < H)
-                red_add_u64(acc_cur + r0 + 32 * t + lane, fix_word(scr[32 * t + lane], p.err));
+          for (int t0 = 0; t0 < E; t0 += 4) {
+            // rows r0 + 32*t0 .. r0 + 32*(t0+4) - 1 are held by lanes
+            // 32*t0/E .. 32*(t0+4)/E - 1
+            const int l0 = 32 * t0 / E, l1 = 32 * (t0 + 4) / E;
+            __syncwarp();
+            if (lane >= l0 && lane < l1) {
+#pragma unroll
+              for (int e = 0; e < E; e += 4)
+                *reinterpret_cast<float4*>(scr + (lane - l0) * E + e) =
+                    make_float4(outp[e], outp[e + 1], outp[e + 2], outp[e + 3]);
+            }
+            __syncwarp();
+            if (!*s_abort && r0 < H) {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int row = r0 + 32 * (t0 + t) + lane;
+                if (row < H) red_add_u64(acc_cur + row, fix_word(scr[32 * t + lane], p.err));
+              }
+            }
           }
           __syncwarp();
         }
@@ -762,15 +773,13 @@ FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem
     darea = b > darea ? b : darea;
   }
   pl.darea_bytes = round_up_i(darea > 128 ? darea : 128, 128);
-  const int mw = (H / (32 / bits) + kDnThreads - 1) / kDnThreads;
-  const int mwp = mw <= 1 ? 1 : mw <= 2 ? 2 : 4;               // code words per down thread
   pl.hb = bits == 4 ? 8 : 12;
   pl.xs_off = kCtrlBytes;
   pl.part_off = round_up_i(pl.xs_off + (long long)H * 4, 128);
   for (int ns = kFusedStageCap; ns >= 2; --ns) {
     pl.hbuf_off = round_up_i(pl.part_off + (long long)2 * ns * R * nparts * 2 * 4, 128);
     pl.dscr_off = round_up_i(pl.hbuf_off + (long long)(pl.len_max + 1) * pl.hb * 4, 128);
-    pl.darea_off = round_up_i(pl.dscr_off + (long long)kDnThreads * (32 / bits) * mwp * 4, 128);
+    pl.darea_off = round_up_i(pl.dscr_off + (long long)kDnWarps * 128 * 4, 128);
     pl.ring_off = pl.darea_off + pl.darea_bytes;
     const long long need = (long long)pl.ring_off + (long long)ns * pl.stage_bytes;
     if (need <= smem_max) {

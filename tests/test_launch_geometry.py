@@ -78,9 +78,7 @@ def test_geometry(fm, bits, H, I, K, S):
     assert g["hb"] >= (5 if bits == 4 else 9)
     assert g["len_max"] == -(-NS * I // SMS)
     assert g["dscr_off"] >= g["hbuf_off"] + g["len_max"] * g["hb"] * 4
-    words = H // (32 // bits)                              # code words per down column
-    mw = 1 if words <= 256 else 2 if words <= 512 else 4   # per down thread
-    assert g["darea_off"] >= g["dscr_off"] + 256 * (32 // bits) * mw * 4   # the down warps' transpose scratch
+    assert g["darea_off"] >= g["dscr_off"] + 8 * 128 * 4    # the down warps' transpose scratch
     assert g["ring_off"] >= g["darea_off"] + g["darea_bytes"]
     assert g["nstage"] >= 2 and g["stage_bytes"] >= g["R"] * gu_row
     assert g["fused_smem"] == g["ring_off"] + g["nstage"] * g["stage_bytes"] <= SMEM_MAX
