@@ -17,19 +17,22 @@
 //                        token group) item, 2 intermediate rows per warp
 //   batch_down_kernel    y[t][k] = Wd h[t][k]; a unit is 256 (4-bit) or 512
 //                        (2-bit) output rows, the down projection being
-//                        stored by column
+//                        stored by column (tensor-map tiles of column slices)
 //   batch_combine_kernel out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
 // The two expert kernels run one block per SM over a contiguous share of
 // (item, row block) work units.  In the gate/up kernel a producer warp
 // streams each unit's packed rows (one contiguous range of the blob) into a
 // shared-memory ring with bulk asynchronous copies (TMA engine, mbarrier
-// completion) and eight consumer warps compute from the ring; in the down
-// kernel each of eight warps streams its own columns' slices with cp.async.
+// completion) and eight consumer warps compute from the ring; the down
+// kernel's producer streams tiles of column slices with tensor copies.
 //
 // Sources: flash-moe write-up (discuss.pytorch.kr): "per-layer pipeline"
 // (softmax + top-K routing, expert forward, combine), "hand-written Metal
 // compute shaders" (dequant matvec, fused SwiGLU, MoE combine + residual +
 // sigmoid gate), "FMA-optimised dequant kernel" (code * scale + bias).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -298,23 +301,68 @@ __device__ __forceinline__ SliceCodes<BITS> smem_codes(const uint8_t* row, int s
 // acc[r] += code[r] * h for the rows of one 32-bit code word of a down column
 // (codes masked in place, h pre-scaled per position; hv: 2 pairs at 4-bit,
 // 4 at 2-bit).
+// The masked code pairs of one 32-bit word of a down column (RW/2 pairs of
+// rows, each value carrying the position's power-of-two factor that the
+// pre-scaled h of that position cancels).
 template <int BITS>
-__device__ __forceinline__ void down_word_bd(uint32_t w, const float2* hv, float2* acc) {
+__device__ __forceinline__ void code_pairs(uint32_t w, float2* q) {
   const uint32_t hi = w >> 16;
   if constexpr (BITS == 4) {
-    acc[0] = __ffma2_rn(mk2(w, 0xFu, 0xF0u), hv[0], acc[0]);
-    acc[1] = __ffma2_rn(mk2(w, 0xF00u, 0xF000u), hv[1], acc[1]);
-    acc[2] = __ffma2_rn(mk2(hi, 0xFu, 0xF0u), hv[0], acc[2]);
-    acc[3] = __ffma2_rn(mk2(hi, 0xF00u, 0xF000u), hv[1], acc[3]);
+    q[0] = mk2(w, 0xFu, 0xF0u);
+    q[1] = mk2(w, 0xF00u, 0xF000u);
+    q[2] = mk2(hi, 0xFu, 0xF0u);
+    q[3] = mk2(hi, 0xF00u, 0xF000u);
   } else {
-    acc[0] = __ffma2_rn(mk2(w, 0x3u, 0xCu), hv[0], acc[0]);
-    acc[1] = __ffma2_rn(mk2(w, 0x30u, 0xC0u), hv[1], acc[1]);
-    acc[2] = __ffma2_rn(mk2(w, 0x300u, 0xC00u), hv[2], acc[2]);
-    acc[3] = __ffma2_rn(mk2(w, 0x3000u, 0xC000u), hv[3], acc[3]);
-    acc[4] = __ffma2_rn(mk2(hi, 0x3u, 0xCu), hv[0], acc[4]);
-    acc[5] = __ffma2_rn(mk2(hi, 0x30u, 0xC0u), hv[1], acc[5]);
-    acc[6] = __ffma2_rn(mk2(hi, 0x300u, 0xC00u), hv[2], acc[6]);
-    acc[7] = __ffma2_rn(mk2(hi, 0x3000u, 0xC000u), hv[3], acc[7]);
+    q[0] = mk2(w, 0x3u, 0xCu);
+    q[1] = mk2(w, 0x30u, 0xC0u);
+    q[2] = mk2(w, 0x300u, 0xC00u);
+    q[3] = mk2(w, 0x3000u, 0xC000u);
+    q[4] = mk2(hi, 0x3u, 0xCu);
+    q[5] = mk2(hi, 0x30u, 0xC0u);
+    q[6] = mk2(hi, 0x300u, 0xC00u);
+    q[7] = mk2(hi, 0x3000u, 0xC000u);
+  }
+}
+
+// Down step of `ncol` columns of a tile ([column][bx bytes], the lane's code
+// word at word `lane` of each column) for NT tokens: acc[t] += codes * h, the
+// codes masked once per column and met by every token from registers.  hq
+// holds, per token and column, h times the position factors of positions
+// 0..3 (positions 4..7 of a 2-bit word are those times 2^-8); hs[t] sums the
+// position-0 values (h times a power of two).
+template <int BITS, int NT>
+__device__ __forceinline__ void bd_columns(const uint8_t* tile, int bx, int ncol, bool row_ok, const float4* hq, int I,
+                                           float2 (&acc)[kMaxTokGroup][16 / BITS], float (&hs)[kMaxTokGroup]) {
+  constexpr int P = 16 / BITS;
+  const int lane = threadIdx.x & 31;
+#pragma unroll 2
+  for (int j = 0; j < ncol; ++j) {
+    const uint32_t w = row_ok ? reinterpret_cast<const uint32_t*>(tile + (size_t)j * bx)[lane] : 0u;
+    float2 q[P];
+    code_pairs<BITS>(w, q);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float4 a = hq[(size_t)t * I + j];
+      hs[t] += a.x;
+      const float2 h01 = make_float2(a.x, a.y), h23 = make_float2(a.z, a.w);
+      if constexpr (BITS == 4) {
+        acc[t][0] = __ffma2_rn(q[0], h01, acc[t][0]);
+        acc[t][1] = __ffma2_rn(q[1], h23, acc[t][1]);
+        acc[t][2] = __ffma2_rn(q[2], h01, acc[t][2]);
+        acc[t][3] = __ffma2_rn(q[3], h23, acc[t][3]);
+      } else {
+        const float2 k8 = make_float2(0.00390625f, 0.00390625f);
+        const float2 h45 = __fmul2_rn(h01, k8), h67 = __fmul2_rn(h23, k8);
+        acc[t][0] = __ffma2_rn(q[0], h01, acc[t][0]);
+        acc[t][1] = __ffma2_rn(q[1], h23, acc[t][1]);
+        acc[t][2] = __ffma2_rn(q[2], h45, acc[t][2]);
+        acc[t][3] = __ffma2_rn(q[3], h67, acc[t][3]);
+        acc[t][4] = __ffma2_rn(q[4], h01, acc[t][4]);
+        acc[t][5] = __ffma2_rn(q[5], h23, acc[t][5]);
+        acc[t][6] = __ffma2_rn(q[6], h45, acc[t][6]);
+        acc[t][7] = __ffma2_rn(q[7], h67, acc[t][7]);
+      }
+    }
   }
 }
 
@@ -659,56 +707,108 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_gateup_kernel(BatchArg
 }
 
 // ---------------------------------------------------------------------------
-// down: unit = (item, kBdRows output rows).  The down projection is stored by
-// column, so a unit's codes are a 128-byte slice of every column (32 lanes x
-// one code word).  Warp w owns the columns [I*w/8, I*(w+1)/8) and streams
-// their slices through its own ring with 16-byte cp.async copies (a warp's
-// copies of one stage are one commit group); lane l accumulates rows
-// r0 + l*RW .. r0 + l*RW + RW-1 for each of the item's tokens, applies each
-// 64-column group's scale and bias, and the eight warps' partial sums are
-// added in a fixed order at the end of the unit.
+// down: unit = (item, RB = 32*RW output rows).  The down projection is stored
+// by column, so a unit needs a bx-byte slice (bx = 128, or the whole column
+// when it is shorter) of each of the expert's I columns.  A 3-D tensor map
+// over the pool (slice bytes x columns x experts) lets one tiled bulk copy
+// fetch the slices of up to 256 consecutive columns into shared memory as a
+// [column][bx] tile; the producer warp streams a unit's copies through a ring
+// and consumer warp w takes columns [32w, 32w+32) of each tile: lane l the
+// l-th code word of each column, i.e. rows r0 + l*RW .. r0 + l*RW + RW-1, for
+// each of the item's tokens.  A warp's 32 columns lie in one 64-column group,
+// whose scale and bias it applies at the end of the chunk; the eight warps'
+// partial sums are added in a fixed order at the end of the unit.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16_bd(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_bd() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_bd() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 struct BdCtrl {
-  uint64_t cbar;            // the down warps among themselves
+  uint64_t full[kBdMaxStages];
+  uint64_t empty[kBdMaxStages];
+  uint64_t cbar;            // the consumer warps among themselves
   long long range[2];
   int item[kItemWords];
   int abort;
 };
 static_assert(sizeof(BdCtrl) <= kBdCtrlBytes, "control area");
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int BITS>
-__global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, float* __restrict__ y) {
+__global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, float* __restrict__ y,
+                                                                    const __grid_constant__ CUtensorMap tm_pool,
+                                                                    const __grid_constant__ CUtensorMap tm_shared) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int RW = 32 / BITS;                    // rows per code word
   constexpr int RB = 32 * RW;                      // rows per unit
-  constexpr int NV = BITS == 4 ? 4 : 8;            // pre-scaled copies of h per column
-  constexpr int SLICE = 128;                       // bytes of a column's slice of a unit
   constexpr int G = kMaxTokGroup;
+  const BatchGeom& geo = a.geo;
   BdCtrl* ctl = reinterpret_cast<BdCtrl*>(smem);
   const int I = a.I, H = a.H, NS = a.K + a.S;
-  float* hsm = reinterpret_cast<float*>(smem + kBdCtrlBytes);                 // [G][I] h of the item's tokens
-  uint8_t* ring = smem + kBdCtrlBytes + a.geo.bd_h_bytes;                     // [warp][stage][col][SLICE]
-  float* xbuf = reinterpret_cast<float*>(ring + (size_t)kBdWarps * kBdStages * kBdCols * SLICE);   // [warp][RB][G]
+  const int bx = geo.bd_bx, box = geo.bd_box_cols;                            // tile: [box columns][bx bytes]
+  float4* hsm = reinterpret_cast<float4*>(smem + kBdCtrlBytes);               // [G][I] h of the item's tokens, pre-scaled
+  uint8_t* ring = smem + geo.bd_ring_off;                                     // [stage][box][bx]
+  float* xbuf = reinterpret_cast<float*>(ring + (size_t)geo.bd_nstage * geo.bd_stage_bytes);   // [warp][RB][G]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_rb = (H + RB - 1) / RB;
+  const int nc = (I + box - 1) / box;              // tiles per unit
+  const int nst = geo.bd_nstage;                   // ring stages
   long long u0, u1;
   block_share(a, n_rb, ctl->range, u0, u1);
   if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], kBdWarps);
+    }
     mbar_init(&ctl->cbar, kBdWarps);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   volatile int* abort = &ctl->abort;
+  const uint32_t tile_bytes = (uint32_t)(box * bx);
+
+  if (warp == kBdWarps) {
+    // ---- producer: lane 0 issues every tile of the block's units, in order
+    long long k = 0;
+    if (lane == 0) {
+      int cur = -1, expert = 0;
+      for (long long u = u0; u < u1 && !*abort; ++u) {
+        const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
+        if (item != cur) {
+          expert = __ldcg(a.plan + kPlanHeader + item * kItemWords);
+          cur = item;
+        }
+        const CUtensorMap* map = expert >= 0 ? &tm_pool : &tm_shared;
+        const int z = expert >= 0 ? expert : 0;
+        const int x = rb * RB * BITS / 8;          // a multiple of 128 bytes
+        for (int c = 0; c < nc; ++c, ++k) {
+          const int st = (int)(k % nst);
+          const uint32_t use = (uint32_t)(k / nst);
+          if (use >= 1 && !mbar_wait(&ctl->empty[st], (use - 1) & 1u, a.timeout_ns, a.err, abort)) break;
+          mbar_arrive_expect_tx(&ctl->full[st], tile_bytes);
+          tma_load_3d(ring + (size_t)st * geo.bd_stage_bytes, map, x, c * box, z, &ctl->full[st]);
+        }
+      }
+      // drain: every stage's last copy has landed before the block may exit
+      for (int st = 0; st < nst && st < k; ++st) {
+        const long long last = st + ((k - 1 - st) / nst) * nst;
+        if (!mbar_wait_drain(&ctl->full[st], (uint32_t)(last / nst) & 1u, a.timeout_ns)) {
+          atomicOr(a.err, kErrCopyTimeout);
+          ctl->abort = 1;
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---- consumers
   uint32_t nsync = 0;
-  // all eight warps at one point (bounded)
+  // the eight consumer warps at one point (bounded)
   auto cons_sync = [&]() -> bool {
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->cbar);
@@ -716,9 +816,7 @@ __global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, 
     ++nsync;
     return ok;
   };
-  const int ca = (int)((long long)I * warp / kBdWarps), cb = (int)((long long)I * (warp + 1) / kBdWarps);
-  const int nch = (cb - ca + kBdCols - 1) / kBdCols;
-  uint8_t* wring = ring + (size_t)warp * kBdStages * kBdCols * SLICE;
+  long long k = 0;
   int cur = -1;
   for (long long u = u0; u < u1; ++u) {
     const int item = (int)(u / n_rb), rb = (int)(u % n_rb);
@@ -728,100 +826,74 @@ __global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, 
       if (tid < kItemWords) ctl->item[tid] = __ldcg(a.plan + kPlanHeader + item * kItemWords + tid);
       if (!cons_sync()) break;
       const int n = ctl->item[1];
-      for (int idx = tid; idx < n * I; idx += kBdThreads) {
+      for (int idx = tid; idx < n * I; idx += kBdWarps * 32) {
         const int t = idx / I, i = idx - t * I;
         const int pr = ctl->item[2 + t];
-        hsm[t * I + i] = __ldcg(a.h + ((size_t)(pr >> 8) * NS + (pr & 255)) * I + i);
+        const float hv = __ldcg(a.h + ((size_t)(pr >> 8) * NS + (pr & 255)) * I + i);
+        hsm[t * I + i] = make_float4(hv * pos_scale<BITS>(0), hv * pos_scale<BITS>(1), hv * pos_scale<BITS>(2),
+                                     hv * pos_scale<BITS>(3));
       }
       if (!cons_sync()) break;
       cur = item;
     }
     const int n = ctl->item[1];
     const uint8_t* blob = item_blob(a, ctl->item[0]);
-    const uint8_t* dq = blob + a.lay.dq_off + (size_t)r0 * BITS / 8;
-    const int vb = min(SLICE, (H - r0) * BITS / 8);   // valid bytes of a column's slice (a multiple of 16)
+    const int vb = min(bx, (H - r0) * BITS / 8);      // valid bytes of a column's slice (a multiple of 16)
     const bool row_ok = lane * 4 < vb;
-    auto issue = [&](int ch) {
-      uint8_t* stg = wring + (size_t)(ch % kBdStages) * kBdCols * SLICE;
-      if (ch < nch) {
-        for (int k = lane; k < kBdCols * (SLICE / 16); k += 32) {
-          const int col = k / (SLICE / 16), part = k % (SLICE / 16);
-          const int i = ca + ch * kBdCols + col;
-          if (i < cb && part * 16 < vb) cp_async16_bd(stg + col * SLICE + part * 16, dq + (size_t)i * a.lay.dcol + part * 16);
-        }
-      }
-      cp_async_commit_bd();
-    };
-#pragma unroll
-    for (int ch = 0; ch < kBdStages - 1; ++ch) issue(ch);
 
-    float2 acc[G][RW / 2];
     float outp[RW][G];
-    float hs[G];
 #pragma unroll
-    for (int t = 0; t < G; ++t) {
-      hs[t] = 0.f;
+    for (int r = 0; r < RW; ++r)
 #pragma unroll
-      for (int r = 0; r < RW / 2; ++r) acc[t][r] = make_float2(0.f, 0.f);
+      for (int t = 0; t < G; ++t) outp[r][t] = 0.f;
+    for (int c = 0; c < nc; ++c, ++k) {
+      const int st = (int)(k % nst);
+      const bool ok = mbar_wait(&ctl->full[st], (uint32_t)(k / nst) & 1u, a.timeout_ns, a.err, abort);
+      const int col0 = c * box + 32 * warp;            // this warp's first column of the tile
+      if (ok && 32 * warp < box && col0 < I) {
+        // the group's (scale, bias) words of the lane's rows
+        uint32_t sbv[RW];
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(blob + a.lay.dsb_off + (size_t)(col0 / kGroup) * a.lay.dsb_group +
+                                                            (size_t)(r0 + RW * lane) * 4);
 #pragma unroll
-      for (int r = 0; r < RW; ++r) outp[r][t] = 0.f;
-    }
-    // (scale, bias) words of the lane's rows for group g
-    uint32_t sbv[RW];
-    auto load_sb = [&](int g) {
-      const uint4* src = reinterpret_cast<const uint4*>(blob + a.lay.dsb_off + (size_t)g * a.lay.dsb_group +
-                                                        (size_t)(r0 + RW * lane) * 4);
-#pragma unroll
-      for (int q = 0; q < RW / 4; ++q) {
-        const uint4 v = row_ok ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
-        sbv[4 * q] = v.x; sbv[4 * q + 1] = v.y; sbv[4 * q + 2] = v.z; sbv[4 * q + 3] = v.w;
-      }
-    };
-    auto fold = [&]() {
-#pragma unroll
-      for (int t = 0; t < G; ++t) {
-#pragma unroll
-        for (int r = 0; r < RW / 2; ++r) {
-          outp[2 * r][t] += fmaf(bf16lo(sbv[2 * r]) * 18446744073709551616.0f, acc[t][r].x, bf16hi(sbv[2 * r]) * hs[t]);
-          outp[2 * r + 1][t] +=
-              fmaf(bf16lo(sbv[2 * r + 1]) * 18446744073709551616.0f, acc[t][r].y, bf16hi(sbv[2 * r + 1]) * hs[t]);
-          acc[t][r] = make_float2(0.f, 0.f);
+          for (int q = 0; q < RW / 4; ++q) {
+            const uint4 v = row_ok ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+            sbv[4 * q] = v.x; sbv[4 * q + 1] = v.y; sbv[4 * q + 2] = v.z; sbv[4 * q + 3] = v.w;
+          }
         }
-        hs[t] = 0.f;
-      }
-    };
-    int g_cur = ca / kGroup;
-    if (ca < cb) load_sb(g_cur);
-    for (int ch = 0; ch < nch; ++ch) {
-      issue(ch + kBdStages - 1);
-      cp_async_wait_bd<kBdStages - 1>();
-      __syncwarp();
-      const uint8_t* stg = wring + (size_t)(ch % kBdStages) * kBdCols * SLICE;
-      const int ncol = min(kBdCols, cb - ca - ch * kBdCols);
-      for (int col = 0; col < ncol; ++col) {
-        const int i = ca + ch * kBdCols + col;
-        if ((i >> 6) != g_cur) {
-          fold();
-          g_cur = i >> 6;
-          load_sb(g_cur);
-        }
-        const uint32_t w = row_ok ? reinterpret_cast<const uint32_t*>(stg + col * SLICE)[lane] : 0u;
+        float2 acc[G][RW / 2];
+        float hs[G];
 #pragma unroll
         for (int t = 0; t < G; ++t) {
-          if (t < n) {
-            const float hh = hsm[t * I + i];
-            hs[t] += hh;
-            float2 hv[NV / 2];
+          hs[t] = 0.f;
 #pragma unroll
-            for (int q = 0; q < NV / 2; ++q) hv[q] = make_float2(hh * pos_scale<BITS>(2 * q), hh * pos_scale<BITS>(2 * q + 1));
-            down_word_bd<BITS>(w, hv, acc[t]);
+          for (int r = 0; r < RW / 2; ++r) acc[t][r] = make_float2(0.f, 0.f);
+        }
+        const uint8_t* tile = ring + (size_t)st * geo.bd_stage_bytes + (size_t)(32 * warp) * bx;
+        const int ncol = min(32, I - col0);
+        const float4* hq = hsm + col0;
+        if (n == 1) bd_columns<BITS, 1>(tile, bx, ncol, row_ok, hq, I, acc, hs);
+        else if (n == 2) bd_columns<BITS, 2>(tile, bx, ncol, row_ok, hq, I, acc, hs);
+        else if (n == 3) bd_columns<BITS, 3>(tile, bx, ncol, row_ok, hq, I, acc, hs);
+        else bd_columns<BITS, 4>(tile, bx, ncol, row_ok, hq, I, acc, hs);
+#pragma unroll
+        for (int t = 0; t < G; ++t) hs[t] *= inv_pos_scale<BITS>(0);   // exact: a power of two
+        // out += s * 2^64 * acc + b * sum(h) over the chunk's columns
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+#pragma unroll
+          for (int r = 0; r < RW / 2; ++r) {
+            outp[2 * r][t] += fmaf(bf16lo(sbv[2 * r]) * 18446744073709551616.0f, acc[t][r].x, bf16hi(sbv[2 * r]) * hs[t]);
+            outp[2 * r + 1][t] +=
+                fmaf(bf16lo(sbv[2 * r + 1]) * 18446744073709551616.0f, acc[t][r].y, bf16hi(sbv[2 * r + 1]) * hs[t]);
           }
         }
       }
+      // the tile may be refilled
       __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->empty[st]);
     }
-    cp_async_wait_bd<0>();
-    if (ca < cb) fold();
     // the eight warps' partial sums, added in warp order
     float* xb = xbuf + (size_t)warp * RB * G;
 #pragma unroll
@@ -829,7 +901,7 @@ __global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, 
 #pragma unroll
       for (int t = 0; t < G; ++t) xb[(RW * lane + r) * G + t] = outp[r][t];
     if (!cons_sync()) break;
-    for (int idx = tid; idx < RB * n; idx += kBdThreads) {
+    for (int idx = tid; idx < RB * n; idx += kBdWarps * 32) {
       const int row = idx / n, t = idx - row * n;
       if (r0 + row < H) {
         float v = 0.f;
@@ -841,7 +913,6 @@ __global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, 
     }
     if (!cons_sync()) break;
   }
-  cp_async_wait_bd<0>();
 }
 
 // out[t] = residual[t] + sum_k w[t][k] y[t][k] + g[t] y[t][K]
@@ -925,16 +996,25 @@ BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max) {
   if (sms < 1 || smem_max <= kBatchCtrlBytes) return g;
   const BlobLayout lay = blob_layout(bits, H, I);
   const size_t avail = (size_t)smem_max - kBatchCtrlBytes;
-  const size_t bd_ring = (size_t)kBdWarps * kBdStages * kBdCols * 128;
   const int rb = 32 * (32 / bits);                  // output rows per down unit
+  // a down tile: up to 256 columns' 128-byte slices (the whole column when
+  // it is shorter); stages 1 KB aligned
+  const int bx = (int)std::min<size_t>(128, lay.dcol);
+  const int box = std::min(kBdMaxBoxCols, I);
+  const size_t bd_stage = (size_t)box * bx;
   // the most tokens per item, then the most gate/up warps, for which two
   // gate/up ring stages fit next to the staged inputs, and the down kernel's
   // staged h, ring and partial sums fit
   for (int G = kMaxTokGroup; G >= 1; G /= 2) {
     const size_t gx = round_up128(staged_bytes(H, G));
-    const size_t bdh = round_up128((size_t)G * I * 4);
-    const size_t bd_smem = kBdCtrlBytes + bdh + bd_ring + (size_t)kBdWarps * rb * kMaxTokGroup * 4;
-    if (bd_smem > (size_t)smem_max) continue;
+    // h staged pre-scaled (a float4 per token and column); as many ring
+    // stages as fit, at least two
+    const size_t bdh = round_up128((size_t)G * I * 16);
+    const size_t ring_off = (kBdCtrlBytes + bdh + 1023) / 1024 * 1024;
+    const size_t xb = (size_t)kBdWarps * rb * kMaxTokGroup * 4;
+    if (ring_off + 2 * bd_stage + xb > (size_t)smem_max) continue;
+    const int bd_nst = (int)std::min<size_t>(kBdMaxStages, ((size_t)smem_max - ring_off - xb) / bd_stage);
+    const size_t bd_smem = ring_off + (size_t)bd_nst * bd_stage + xb;
     for (int w = kBatchConsumerWarps; w >= 1; w /= 2) {
       const size_t gu_stage = round_up128((size_t)2 * w * lay.gu_row);
       if (I % (2 * w) || gx + 2 * gu_stage > avail) continue;
@@ -946,6 +1026,11 @@ BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max) {
       g.gu_xs_bytes = (int)gx;
       g.gu_smem = kBatchCtrlBytes + gx + (size_t)g.gu_nstage * gu_stage;
       g.bd_h_bytes = (int)bdh;
+      g.bd_bx = bx;
+      g.bd_box_cols = box;
+      g.bd_stage_bytes = (int)bd_stage;
+      g.bd_ring_off = (int)ring_off;
+      g.bd_nstage = bd_nst;
       g.bd_smem = bd_smem;
       g.grid = sms;
       return g;
@@ -967,6 +1052,37 @@ static cudaError_t allow_smem(Kern k, size_t bytes, size_t& done) {
 // belong to the device's context)
 static size_t g_smem_set[64][4];
 static std::mutex g_smem_mu;
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map over the down codes of `n` blobs `blob` bytes apart from
+// `base`: dimensions (slice bytes, columns, blobs), tile [box columns][bx].
+static bool down_tensor_map(CUtensorMap* m, const uint8_t* base, int n, const BatchArgs& a) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)a.lay.dcol, (cuuint64_t)a.I, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.lay.dcol, (cuuint64_t)a.blob};
+  const cuuint32_t box[3] = {(cuuint32_t)a.geo.bd_bx, (cuuint32_t)a.geo.bd_box_cols, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base + a.lay.dq_off), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
   int dev = 0;
@@ -991,12 +1107,16 @@ cudaError_t launch_batch(BatchArgs& a, float* y, cudaStream_t st) {
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+  CUtensorMap tm_pool, tm_shared;
+  if (!down_tensor_map(&tm_pool, a.experts, a.E, a) ||
+      !down_tensor_map(&tm_shared, a.S ? a.shared : a.experts, 1, a))
+    return cudaErrorInvalidValue;
   if (a.bits == 4) {
     if ((e = allow_smem(batch_down_kernel<4>, g.bd_smem, set[2])) != cudaSuccess) return e;
-    batch_down_kernel<4><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y);
+    batch_down_kernel<4><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y, tm_pool, tm_shared);
   } else {
     if ((e = allow_smem(batch_down_kernel<2>, g.bd_smem, set[3])) != cudaSuccess) return e;
-    batch_down_kernel<2><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y);
+    batch_down_kernel<2><<<g.grid, kBdThreads, g.bd_smem, st>>>(a, y, tm_pool, tm_shared);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -13,6 +13,8 @@ struct BatchGeom {
   int gu_nstage, gu_stage_bytes;
   int gu_xs_bytes;                // staged inputs
   int bd_h_bytes;                 // down: staged h of an item's tokens
+  int bd_bx, bd_box_cols;         // down: tile of a tensor copy, [bd_box_cols columns][bd_bx bytes]
+  int bd_stage_bytes, bd_ring_off, bd_nstage;
   size_t gu_smem, bd_smem;
   int grid;
 };
@@ -48,12 +50,12 @@ constexpr int kBatchConsumerWarps = 8;
 constexpr int kBatchProducerWarp = kBatchConsumerWarps;
 constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 1);
 constexpr int kBatchMaxStages = 8;
-// down kernel: warps that each own a range of columns, columns per ring
-// stage of a warp, stages per warp (cp.async groups in flight)
+// down kernel: consumer warps (32 columns of each tile each), one producer
+// warp, ring stages of one tensor tile, most columns per tile
 constexpr int kBdWarps = 8;
-constexpr int kBdThreads = 32 * kBdWarps;
-constexpr int kBdCols = 16;
-constexpr int kBdStages = 4;
+constexpr int kBdThreads = 32 * (kBdWarps + 1);
+constexpr int kBdMaxStages = 4;
+constexpr int kBdMaxBoxCols = 32 * kBdWarps;
 constexpr int kBdCtrlBytes = 256;
 constexpr int kBatchCtrlBytes = 256;   // mbarriers, work range, item header at the start of shared memory
 
