@@ -22,6 +22,8 @@ What is computed (all in fp64; fp32 and bf16 inputs are widened exactly):
 * route       top-K of the router logits by value (ties: lower expert id
               first), weights = softmax over the K selected logits
               (same write-up, section "per-layer pipeline": CPU softmax + top-K)
+* router      logits = W_r x, W_r bf16 [E][H] (same write-up, section
+              "per-layer pipeline": the routing logits come from the GPU)
 * shared gate g = sigmoid(w_sg . x) scaling the always-on shared expert
               (same write-up: model section "K=4 of 512 experts plus one
               shared expert", shader list "MoE combine + residual + sigmoid gate")
@@ -46,6 +48,7 @@ from .moe import (  # noqa: F401
     sigmoid,
     expert_ffn,
     route,
+    router_logits,
     shared_gate,
     combine,
     moe_block,

@@ -198,6 +198,20 @@ def shared_gate(wsg_bf16: np.ndarray, x: np.ndarray) -> float:
     return float(sigmoid(w @ np.asarray(x, dtype=np.float64)))
 
 
+def router_logits(w_router_bf16: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """Router logits l = W_r x of one token (x [H] -> [E]) or of T tokens
+    (x [T][H] -> [T][E]), W_r [E][H] given as bf16 bit patterns.
+
+    [FM] "per-layer pipeline": the second command buffer computes the routing
+    logits on the GPU (with o_proj, the norm and the shared expert) before the
+    CPU's softmax + top-K.  The pages give no storage type for W_r; bf16 is
+    this project's reading, as for w_sg.  Pinned by hand-worked values, exact
+    integer products checked against Python integers, and one-hot rows.
+    """
+    w = bf16_to_f64(w_router_bf16)
+    return np.asarray(x, dtype=np.float64) @ w.T
+
+
 def combine(residual, routed_y, weights, shared_y=None, g=None):
     """out = residual + sum_k w_k y_k (+ g * y_shared)."""
     out = np.asarray(residual, dtype=np.float64).copy()

@@ -273,6 +273,14 @@ def shared_gate_vector(shape: BlockShape, layer: int = 0, seed: Optional[int] = 
     return w.to(torch.bfloat16).view(torch.int16)
 
 
+def router_matrix(shape: BlockShape, layer: int = 0, seed: Optional[int] = None) -> torch.Tensor:
+    """bf16 bit patterns (int16 tensor [E][H]) of W_r ~ N(0, 1/H): with x ~ N(0, 1)
+    the logits are about N(0, 1), as the workloads' router logits."""
+    seed = shape.seed if seed is None else seed
+    w = normal(seed, 300 + layer, (shape.n_experts, shape.hidden), std=1.0 / math.sqrt(shape.hidden))
+    return w.to(torch.bfloat16).view(torch.int16)
+
+
 def zipf_logits(seed: int, tag: int, n_tokens: int, n_experts: int, s: float) -> torch.Tensor:
     """Router logits whose top-K is a Plackett-Luce draw from Zipf(s) popularity.
 

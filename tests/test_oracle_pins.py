@@ -408,10 +408,38 @@ def pin_stack_closed_form():
     assert np.allclose(h, hv, rtol=1e-12), (h[0], hv)
 
 
+def pin_router_logits():
+    # hand-worked: rows (1, -2, 0.5, 3), (0, 0, 0, 0.25), (-1, -1, -1, -1) against x = (1, 2, 3, 4)
+    W = np.array([[bf16(v) for v in row] for row in ((1, -2, 0.5, 3), (0, 0, 0, 0.25), (-1, -1, -1, -1))],
+                 dtype=np.uint16)
+    assert list(om.router_logits(W, np.array([1.0, 2.0, 3.0, 4.0]))) == [10.5, 1.0, -10.0]
+    rng = np.random.default_rng(11)
+    # one-hot rows pick x[perm[e]]: a row shift or a transposed operand fails
+    E, H = 7, 96
+    perm = rng.permutation(H)[:E]
+    onehot = np.zeros((E, H), dtype=np.uint16)
+    onehot[np.arange(E), perm] = bf16(1.0)
+    x = rng.standard_normal(H)
+    assert np.array_equal(om.router_logits(onehot, x), x[perm])
+    # small integers are exact in bf16 and fp64: compare with Python integers
+    Wi = rng.integers(-8, 9, size=(E, H))
+    xi = rng.integers(-50, 51, size=H)
+    Wb = np.vectorize(bf16)(Wi.astype(float)).astype(np.uint16)
+    want = [sum(int(Wi[e, j]) * int(xi[j]) for j in range(H)) for e in range(E)]
+    assert list(om.router_logits(Wb, xi.astype(float))) == [float(v) for v in want]
+    # T tokens at once equal T single calls; the shared gate is sigma of a one-row projection
+    X = rng.standard_normal((3, H))
+    Wr = synth.router_matrix(synth.TINY)[:E, :H].numpy().view(np.uint16)
+    # (equal up to fp64 summation order: one matrix product against T matrix-vector products)
+    assert np.allclose(om.router_logits(Wr, X), np.stack([om.router_logits(Wr, X[t]) for t in range(3)]),
+                       rtol=1e-13, atol=1e-15)
+    assert abs(om.shared_gate(Wr[0], X[0]) - float(om.sigmoid(om.router_logits(Wr[:1], X[0])[0]))) < 1e-15
+
+
 PINS = [pin_unpack_golden, pin_dequant_golden, pin_two_groups, pin_fma_identity,
         pin_group_decomposition, pin_random_blob_fields, pin_constant_rows, pin_route_bruteforce,
         pin_route_weights, pin_special_values, pin_zero_weight, pin_page_sizes,
-        pin_layout_matches_generator, pin_block_closed_form, pin_stack_closed_form]
+        pin_layout_matches_generator, pin_block_closed_form, pin_stack_closed_form, pin_router_logits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -516,6 +544,19 @@ def _gate_sign(wsg, x):
     return float(om.sigmoid(-(om.bf16_to_f64(wsg) @ np.asarray(x, dtype=np.float64))))
 
 
+def _router_low_half(w, x):
+    w = (np.asarray(w, dtype=np.uint32) & 0xFFFF).view(np.float32).astype(np.float64)
+    return np.asarray(x, dtype=np.float64) @ w.T
+
+
+def _router_rows_shifted(w, x):
+    return np.roll(_ORIG["router_logits"](w, x), 1, axis=-1)
+
+
+def _router_transposed(w, x):
+    return np.asarray(x, dtype=np.float64) @ om.bf16_to_f64(w)
+
+
 def _combine_no_residual(residual, routed_y, weights, shared_y=None, g=None):
     return _ORIG["combine"](np.zeros_like(np.asarray(residual, dtype=np.float64)),
                             routed_y, weights, shared_y, g)
@@ -536,7 +577,7 @@ def _rms_sum(h, eps):
 
 
 _ORIG = {n: getattr(om, n) for n in ("unpack_codes", "dequantize", "route", "combine", "layout",
-                                      "expert_weights")}
+                                      "expert_weights", "router_logits")}
 
 MUTANTS = [
     ("unpack_codes", _unpack_msb_first),
@@ -554,6 +595,9 @@ MUTANTS = [
     ("route", _route_ties_high),
     ("route", _route_ascending),
     ("shared_gate", _gate_sign),
+    ("router_logits", _router_low_half),
+    ("router_logits", _router_rows_shifted),
+    ("router_logits", _router_transposed),
     ("combine", _combine_no_residual),
     ("combine", _combine_unweighted_shared),
     ("rms_norm", _rms_eps_outside),
