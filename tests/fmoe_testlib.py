@@ -30,12 +30,13 @@ def rel_errors(got, ref, floor=1e-3):
 
 
 # Elementwise floor for a deep stack: after 48 fp32 layers every output
-# element carries about the same absolute rounding error, so an element a
-# thousand times below the largest is held to an absolute bound the
-# arithmetic does not give; for the 48-layer stack the elementwise form
-# divides by at least a hundredth of the largest element instead (the
-# max-normalised form keeps 2e-3).
-STACK_FLOOR = 1e-2
+# element carries about the same absolute rounding error (up to ~4e-5 of the
+# largest element, measured), so an element far below the largest is held to
+# an absolute bound the arithmetic does not give.  For the 48-layer stack the
+# elementwise form divides by at least 5e-2 of the largest element: an
+# element twenty times below the largest may be off by 1e-4 of the largest.
+# The max-normalised form keeps 2e-3.
+STACK_FLOOR = 5e-2
 
 
 def assert_close(got, ref, tol=TOL, what="", floor=1e-3):
