@@ -455,6 +455,135 @@ def measure_batch(T, steps, warmup, dev):
             "launches_per_step": 1 if T == 1 else 4, "clocks": clocks.summary()}
 
 
+def measure_router(shape, T, steps, warmup, dev, n_mat=8):
+    """The router projection logits = W_r x (bf16 W_r [E][H]) for T tokens: one
+    graph holds n_mat launches over n_mat different router matrices (each read
+    from HBM once per step: L2 is flushed before every step by a 256 MiB read,
+    outside the events).  Returns GB/s of router-matrix bytes and us per call."""
+    import torch
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    ws = [synth.router_matrix(shape, layer=i).to(dev) for i in range(n_mat)]
+    x = synth.normal(shape.seed, 900 + T, (T, shape.hidden)).to(dev)
+    out = torch.empty((n_mat, T, shape.n_experts), dtype=torch.float32, device=dev)
+    for i in range(n_mat):
+        fm.router_logits(ws[i], x, out[i])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_mat):
+            fm.router_logits(ws[i], x, out[i])
+    flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.sum()
+        evs[i][0].record(stream)
+        g.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)[steps // 2]        # median step
+    nbytes = n_mat * shape.n_experts * shape.hidden * 2
+    value = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = load_peaks()
+    del ws, flush, g
+    torch.cuda.empty_cache()
+    return {"T": T, "E": shape.n_experts, "H": shape.hidden, "gbs": value, "frac": value / peak,
+            "us_per_call": ms * 1e3 / n_mat, "bytes_per_call": nbytes // n_mat}
+
+
+def measure_pool(n_tokens, warmup, dev, n_slots=128):
+    """Decode tokens through one Qwen-shaped 4-bit block whose experts live in
+    pinned host memory, with n_slots of the 512 resident in HBM (the slot pool;
+    Zipf(1.1) routing).  Per token: route on the GPU, ids to the host, plan the
+    slots (LRU, the previous token's slots kept), whole-blob copies of the
+    misses on a copy stream, then the block on the compute stream against the
+    slots; token i+1's routing and copies overlap token i's block.  Timed on
+    the host clock end to end (host planning included).  Returns tokens/s,
+    hit rate and the copies' GB/s."""
+    import time
+    import numpy as np
+    import torch
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    shape = synth.QWEN_Q4_BATCH
+    K, E = shape.top_k, shape.n_experts
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+    blob = nw * 4
+    host = torch.empty(E * nw, dtype=torch.int32, pin_memory=True)
+    chunk = 64
+    for e0 in range(0, E, chunk):
+        tmp = torch.empty(chunk * nw, dtype=torch.int32, device=dev)
+        synth.fill_pool(tmp, shape, 0, e0, chunk)
+        host[e0 * nw:(e0 + chunk) * nw].copy_(tmp.cpu())
+        del tmp
+    slots = torch.zeros(n_slots * nw, dtype=torch.int32, device=dev)
+    shared = torch.empty(nw, dtype=torch.int32, device=dev)
+    synth.fill_pool(shared, shape, 0, E, 1)
+    layer = fm.Layer(shape.bits, shape.hidden, shape.inter, n_slots, slots, shared,
+                     synth.shared_gate_vector(shape).to(dev))
+    pool = fm.SlotPool(n_slots, E, blob, slots.data_ptr(), host.data_ptr())
+    total = warmup + n_tokens
+    logits = synth.zipf_logits(shape.seed, 4000, total, E, 1.1)
+    logits_dev = logits.to(dev)
+    xs = synth.normal(shape.seed, 4001, (total, shape.hidden)).to(dev)
+    res = synth.normal(shape.seed, 4002, (total, shape.hidden)).to(dev)
+    ws = fm.new_workspace(layer, 1, K)
+    out = torch.empty((1, shape.hidden), dtype=torch.float32, device=dev)
+    route_s, copy_s, comp_s = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.current_stream()
+    ids_host = torch.empty((1, K), dtype=torch.int32, pin_memory=True)
+    sl_host = [torch.empty((1, n_slots), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    done = [None, None]
+    loads_n = 0
+    t0 = None
+    for i in range(total):
+        if i == warmup:
+            torch.cuda.synchronize()
+            st0 = pool.stats()
+            loads_n = 0
+            t0 = time.perf_counter()
+        with torch.cuda.stream(route_s):
+            ids_dev, _ = fm.route(logits_dev[i:i + 1], K, stream=route_s)
+            ids_host.copy_(ids_dev, non_blocking=True)
+        route_s.synchronize()
+        ids = ids_host.numpy().copy()
+        sl_of, loads = pool.plan(ids.flatten().tolist(), keep=1)
+        loads_n += len(loads)
+        # a slot the token before the previous one used may be overwritten only after its block
+        if done[i % 2] is not None:
+            copy_s.wait_event(done[i % 2])
+        pool.load(loads, stream=copy_s)
+        landed = torch.cuda.Event()
+        landed.record(copy_s)
+        buf = sl_host[i % 2]
+        if done[i % 2] is not None:
+            done[i % 2].synchronize()          # the pinned slot-logit buffer of token i-2 is free again
+        buf.numpy()[:] = pool.slot_logits(logits[i:i + 1].numpy(), ids, np.array(sl_of, dtype=np.int32).reshape(1, K))
+        comp_s.wait_event(landed)
+        sl_dev = buf.to(dev, non_blocking=True)
+        fm.moe_block(layer, xs[i:i + 1], sl_dev, res[i:i + 1], K, ws, out=out)
+        ev = torch.cuda.Event()
+        ev.record(comp_s)
+        done[i % 2] = ev
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if fm.last_device_error(ws) != fm.OK:
+        raise RuntimeError("device error in the pool run")
+    st = pool.stats()
+    hits, misses = st["hits"] - st0["hits"], st["misses"] - st0["misses"]
+    del host, slots, shared, logits_dev, xs, res
+    torch.cuda.empty_cache()
+    return {"tokens": n_tokens, "slots": n_slots, "experts": E, "tokens_per_s": n_tokens / dt,
+            "us_per_token": dt * 1e6 / n_tokens, "hit_rate": hits / max(1, hits + misses),
+            "loads_per_token": loads_n / n_tokens, "h2d_gbs": loads_n * blob / dt / 1e9,
+            "routing": "Zipf(1.1) over 512 experts, top-4 + shared (shared expert resident)"}
+
+
 def run_batch(args):
     """--workload qwen_q4_zipf: the batched block at --tokens T; value =
     distinct experts' bytes (routed + shared) per second."""
@@ -743,6 +872,11 @@ def main():
             b = measure_batch(T, 50, 3, dev)
             cfgs["qwen_q4_zipf"][f"T{T}"] = {k: b[k] for k in ("gbs", "frac", "ms_per_step", "tokens_per_s",
                                                                 "launches_per_step")}
+        cfgs["slot_pool_25pct"] = measure_pool(300, 60, dev)
+        cfgs["router_projection"] = {}
+        for nm, sh in (("qwen", synth.QWEN_Q4), ("stack48", synth.STACK48)):
+            for T in (1, 16):
+                cfgs["router_projection"][f"{nm}_T{T}"] = measure_router(sh, T, 50, 3, dev)
         line["configs"] = cfgs
     if world == 1 and not args.no_cpu_baseline:
         n = 16 if shape.hidden >= 4096 else 32

@@ -142,6 +142,32 @@ fmoe_status fmoe_route(const float* logits, int T, int E, int K,
                        int32_t* ids, float* weights, void* stream);
 
 /*
+ * Router projection (flash-moe "per-layer pipeline": the second command
+ * buffer computes the routing logits on the GPU):
+ *   logits[t][e] = sum_j W_r[e][j] * x[t][j]
+ *   w_router  bf16 [E][H]   router matrix (bf16 bit patterns), 16-byte aligned
+ *   x         fp32 [T][H]   16-byte aligned
+ *   logits    fp32 [T][E]   out; must not overlap x or w_router
+ * 1 <= T <= FMOE_MAX_TOKENS, H a multiple of 64 up to FMOE_MAX_HIDDEN,
+ * 1 <= E <= FMOE_MAX_EXPERTS.  The sums are taken in fp32 in a fixed order
+ * (deterministic).  FMOE_ERR_INVALID_ARG for bad sizes or pointers.
+ */
+fmoe_status fmoe_router_logits(const uint16_t* w_router, const float* x, int T, int hidden, int E,
+                               float* logits, void* stream);
+
+/*
+ * Routing from the layer input: fmoe_router_logits, then fmoe_route on the
+ * logits and, when shared_gate_w is not null, gate[t] = sigmoid(w_sg . x[t])
+ * (two launches on `stream`).
+ *   logits  fp32 [T][E]   out (kept: the routing decisions are taken on them)
+ *   ids, weights          out, as fmoe_route
+ *   shared_gate_w bf16 [H] or NULL; gate fp32 [T] out (NULL when shared_gate_w is)
+ */
+fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, int hidden, int E, int K,
+                              const uint16_t* shared_gate_w, float* logits, int32_t* ids, float* weights,
+                              float* gate, void* stream);
+
+/*
  * Expert forward for given ids (flash-moe CMD3 "expert forward", without the
  * combine): for token t and slot k < K, y[t][k] = Wd (silu(Wg x_t) * (Wu x_t))
  * of routed expert ids[t][k]; if layer->has_shared, slot K holds the shared
@@ -259,6 +285,57 @@ fmoe_status fmoe_debug_launch_geometry(int bits, int hidden, int inter, int K, i
  */
 fmoe_status fmoe_debug_block_pieces(int bits, int hidden, int inter, int K, int has_shared, int sms,
                                     int block, int64_t* out, int n);
+
+/*
+ * Expert slot pool: n_slots HBM slots of one expert blob each, filled from a
+ * copy of all n_experts blobs in pinned host memory (host memory stands in
+ * for the SSD of the flash-moe write-up, section "SSD expert streaming and
+ * 'Trust the OS'"; fixed slots with eviction as in the slotstream write-up,
+ * "10 of 512 experts per layer"; whole-expert copies, "the disk was not the
+ * slow part").  All calls but fmoe_pool_load are host code that touch no
+ * device.  A routing step goes:
+ *   1. ids of the step's T*K picks on the host (e.g. fmoe_route, then a copy);
+ *   2. fmoe_pool_plan(ids) -> the slot of each pick and the loads (misses);
+ *   3. fmoe_pool_load(loads, copy_stream): one cudaMemcpyAsync per miss;
+ *   4. fmoe_pool_slot_logits -> logits over slots (the picks keep their
+ *      logits, every other slot gets -FLT_MAX);
+ *   5. fmoe_moe_block with layer.experts = the slots, layer.n_experts =
+ *      n_slots and the slot logits, on a stream ordered after step 3.
+ * Top-K and softmax over the slot logits select exactly the planned slots
+ * with the same weights.
+ *
+ * fmoe_pool_state_bytes: host bytes of the pool's bookkeeping (0 for bad
+ *   sizes).  The caller owns that memory (8-byte aligned), the device slots
+ *   (n_slots * blob_bytes, 256-byte aligned) and the pinned host blobs
+ *   (n_experts * blob_bytes, expert e at e * blob_bytes).
+ * fmoe_pool_init: empty pool; FMOE_ERR_INVALID_ARG for bad sizes/pointers.
+ * fmoe_pool_plan: for the n expert ids of one request (duplicates allowed),
+ *   the slot of each in slots[n]; each distinct expert not resident gets the
+ *   least recently used slot that neither this request nor the `keep`
+ *   requests before it used (an empty slot first, ties to the lower slot),
+ *   listed as (expert, slot) in loads[2*n_loads].  Slots of a request whose
+ *   compute may still be running must be kept (keep >= 1) or their loads
+ *   ordered after that compute.  FMOE_ERR_INVALID_ARG (nothing changed) for
+ *   an id outside [0, n_experts) or a request needing more slots than are
+ *   free to evict.
+ * fmoe_pool_load: the copies of `loads` on `stream`.
+ * fmoe_pool_slot_logits: slot_logits [T][n_slots] from logits [T][n_experts]
+ *   and the request's ids / slots [T][K] (all host).
+ * fmoe_pool_stats: distinct experts found resident (hits) and loaded
+ *   (misses) over all requests, and the number of requests.
+ * The write-ups' own reads go to SSD and the OS page cache; this pool is the
+ * HBM counterpart, not a port of either.
+ */
+size_t fmoe_pool_state_bytes(int n_slots, int n_experts);
+fmoe_status fmoe_pool_init(void* state /* host */, size_t state_bytes, int n_slots, int n_experts,
+                           size_t blob_bytes, void* slots_dev, const void* host_blobs);
+fmoe_status fmoe_pool_plan(void* state, const int32_t* ids /* host */, int n, int keep,
+                           int32_t* slots /* host */, int32_t* loads /* host [2n] */, int* n_loads);
+fmoe_status fmoe_pool_load(void* state, const int32_t* loads /* host */, int n_loads, void* stream);
+fmoe_status fmoe_pool_slot_logits(const void* state, const float* logits /* host */,
+                                  const int32_t* ids /* host */, const int32_t* slots /* host */, int T, int K,
+                                  float* slot_logits /* host */);
+fmoe_status fmoe_pool_stats(const void* state, uint64_t* hits, uint64_t* misses, uint64_t* requests);
 
 /* Static description of a status code (host). */
 const char* fmoe_status_string(fmoe_status s);

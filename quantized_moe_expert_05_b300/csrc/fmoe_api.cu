@@ -112,6 +112,31 @@ fmoe_status fmoe_route(const float* logits, int T, int E, int K, int32_t* ids, f
                                 static_cast<cudaStream_t>(stream)));
 }
 
+fmoe_status fmoe_router_logits(const uint16_t* w_router, const float* x, int T, int hidden, int E, float* logits,
+                               void* stream) {
+  if (!host_vec_ok(w_router) || !host_vec_ok(x) || logits == nullptr || !aligned(logits, 4))
+    return FMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > FMOE_MAX_TOKENS || E < 1 || E > FMOE_MAX_EXPERTS) return FMOE_ERR_INVALID_ARG;
+  if (hidden <= 0 || hidden % kGroup || hidden > FMOE_MAX_HIDDEN) return FMOE_ERR_INVALID_ARG;
+  const size_t lb = (size_t)T * E * 4;
+  if (host_overlap(logits, lb, x, (size_t)T * hidden * 4) || host_overlap(logits, lb, w_router, (size_t)E * hidden * 2))
+    return FMOE_ERR_INVALID_ARG;
+  return from_cuda(launch_router(w_router, x, T, hidden, E, logits, static_cast<cudaStream_t>(stream)));
+}
+
+fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, int hidden, int E, int K,
+                              const uint16_t* shared_gate_w, float* logits, int32_t* ids, float* weights, float* gate,
+                              void* stream) {
+  if (ids == nullptr || weights == nullptr || !aligned(ids, 4) || !aligned(weights, 4)) return FMOE_ERR_INVALID_ARG;
+  if (K < 1 || K > E || K > FMOE_MAX_TOPK) return FMOE_ERR_INVALID_ARG;
+  if ((shared_gate_w == nullptr) != (gate == nullptr)) return FMOE_ERR_INVALID_ARG;
+  if (shared_gate_w != nullptr && (!aligned(shared_gate_w, 2) || !aligned(gate, 4))) return FMOE_ERR_INVALID_ARG;
+  fmoe_status s = fmoe_router_logits(w_router, x, T, hidden, E, logits, stream);
+  if (s != FMOE_OK) return s;
+  return from_cuda(launch_route(logits, T, E, K, ids, weights, shared_gate_w, x, hidden, gate,
+                                static_cast<cudaStream_t>(stream)));
+}
+
 fmoe_status fmoe_expert_ffn(const fmoe_layer* layer, const int32_t* ids, int T, int K, const float* x, float* y,
                             void* ws, void* stream) {
   fmoe_status s = check_layer(layer, true);

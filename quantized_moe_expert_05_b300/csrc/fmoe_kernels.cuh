@@ -69,6 +69,8 @@ BatchGeom batch_geometry(int bits, int H, int I, int device);
 // per block (host arithmetic only).
 BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max);
 
+// logits[t][e] = w[e] . x[t] (fmoe_router.cu)
+cudaError_t launch_router(const uint16_t* w, const float* x, int T, int H, int E, float* logits, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights,
                          const uint16_t* wsg, const float* x, int H, float* gate, cudaStream_t st);
 // plan -> gate/up -> down into y (-> combine into a.out when non-null)

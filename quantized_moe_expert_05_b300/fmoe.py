@@ -54,6 +54,8 @@ def _load() -> ctypes.CDLL:
         "fmoe_workspace_bytes": (Z, [LP, I, I, I]),
         "fmoe_workspace_init": (I, [P, Z, P]),
         "fmoe_route": (I, [P, I, I, I, P, P, P]),
+        "fmoe_router_logits": (I, [P, P, I, I, I, P, P]),
+        "fmoe_route_from_x": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "fmoe_expert_ffn": (I, [LP, P, I, I, P, P, P, P]),
         "fmoe_moe_block": (I, [LP, P, P, P, P, I, I, P, P]),
         "fmoe_stack_decode": (I, [LP, I, P, P, I, F, P, P]),
@@ -66,6 +68,13 @@ def _load() -> ctypes.CDLL:
         "fmoe_moe_block_noalloc": (I, [LP, P, P, P, P, I, P, P]),
         "fmoe_debug_launch_geometry": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
         "fmoe_debug_block_pieces": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
+        "fmoe_pool_state_bytes": (Z, [I, I]),
+        "fmoe_pool_init": (I, [P, Z, I, I, Z, P, P]),
+        "fmoe_pool_plan": (I, [P, P, I, I, P, P, ctypes.POINTER(I)]),
+        "fmoe_pool_load": (I, [P, P, I, P]),
+        "fmoe_pool_slot_logits": (I, [P, P, P, P, I, I, P]),
+        "fmoe_pool_stats": (I, [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
+                                ctypes.POINTER(ctypes.c_uint64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -154,6 +163,33 @@ def route(logits: torch.Tensor, K: int, ids: Optional[torch.Tensor] = None,
         weights = torch.empty((T, K), dtype=torch.float32, device=logits.device)
     _check(lib.fmoe_route(_ptr(logits), T, E, K, _ptr(ids), _ptr(weights), _stream(stream)), "fmoe_route")
     return ids, weights
+
+
+def router_logits(w_router: torch.Tensor, x: torch.Tensor, logits: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """logits[t] = W_r x[t]; w_router int16/bfloat16 [E][H], x fp32 [T][H]."""
+    E, H = w_router.shape
+    T = x.shape[0]
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _check(lib.fmoe_router_logits(_ptr(w_router), _ptr(x), T, H, E, _ptr(logits), _stream(stream)),
+           "fmoe_router_logits")
+    return logits
+
+
+def route_from_x(w_router: torch.Tensor, x: torch.Tensor, K: int, shared_gate_w: Optional[torch.Tensor] = None,
+                 stream=None):
+    """(logits, ids, weights, gate or None): the router projection, then top-K + softmax."""
+    E, H = w_router.shape
+    T = x.shape[0]
+    dev = x.device
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    weights = torch.empty((T, K), dtype=torch.float32, device=dev)
+    gate = torch.empty((T,), dtype=torch.float32, device=dev) if shared_gate_w is not None else None
+    _check(lib.fmoe_route_from_x(_ptr(w_router), _ptr(x), T, H, E, K, _ptr(shared_gate_w), _ptr(logits), _ptr(ids),
+                                 _ptr(weights), _ptr(gate), _stream(stream)), "fmoe_route_from_x")
+    return logits, ids, weights, gate
 
 
 def expert_ffn(layer: Layer, ids: torch.Tensor, x: torch.Tensor, ws: torch.Tensor,
@@ -251,3 +287,61 @@ def moe_block_noalloc(layer: Layer, x: torch.Tensor, logits: torch.Tensor, resid
     _check(lib.fmoe_moe_block_noalloc(ctypes.byref(layer.c()), _ptr(x), _ptr(logits), _ptr(residual), _ptr(out),
                                       K, _ptr(device_error), _stream(stream)), "fmoe_moe_block_noalloc")
     return out
+
+
+class SlotPool:
+    """HBM slot pool over a copy of every expert blob in pinned host memory.
+
+    ``slots`` (device, n_slots * blob bytes) and ``host_blobs`` (pinned host,
+    n_experts * blob bytes) are owned by the caller; this object holds the
+    pool's host bookkeeping.  ``plan`` decides slots and loads for a request
+    (host only), ``load`` issues the copies, ``slot_logits`` maps router
+    logits onto the slots."""
+
+    def __init__(self, n_slots: int, n_experts: int, blob_bytes: int, slots_ptr: int, host_ptr: int):
+        n = int(lib.fmoe_pool_state_bytes(n_slots, n_experts))
+        if n == 0:
+            raise FmoeError(ERR_INVALID_ARG, "fmoe_pool_state_bytes")
+        self.n_slots, self.n_experts = n_slots, n_experts
+        self._state = (ctypes.c_uint64 * ((n + 7) // 8))()
+        _check(lib.fmoe_pool_init(ctypes.addressof(self._state), n, n_slots, n_experts, blob_bytes, slots_ptr,
+                                  host_ptr), "fmoe_pool_init")
+
+    @property
+    def state(self) -> int:
+        return ctypes.addressof(self._state)
+
+    def plan(self, ids, keep: int = 0):
+        """(slots, loads) for a request: ids a sequence of expert ids; loads a list of (expert, slot)."""
+        ids = [int(i) for i in ids]
+        n = len(ids)
+        a_ids = (ctypes.c_int32 * n)(*ids)
+        a_slots = (ctypes.c_int32 * n)()
+        a_loads = (ctypes.c_int32 * (2 * n))()
+        nl = ctypes.c_int(0)
+        _check(lib.fmoe_pool_plan(self.state, ctypes.addressof(a_ids), n, keep, ctypes.addressof(a_slots),
+                                  ctypes.addressof(a_loads), ctypes.byref(nl)), "fmoe_pool_plan")
+        loads = [(a_loads[2 * i], a_loads[2 * i + 1]) for i in range(nl.value)]
+        return list(a_slots), loads
+
+    def load(self, loads, stream=None) -> None:
+        flat = [v for pair in loads for v in pair]
+        arr = (ctypes.c_int32 * max(1, len(flat)))(*flat)
+        _check(lib.fmoe_pool_load(self.state, ctypes.addressof(arr), len(loads), _stream(stream)), "fmoe_pool_load")
+
+    def slot_logits(self, logits, ids, slots):
+        """logits [T][E] (host, fp32 numpy), ids and slots [T][K] -> slot logits [T][n_slots] (numpy)."""
+        import numpy as np
+        lg = np.ascontiguousarray(logits, dtype=np.float32)
+        i = np.ascontiguousarray(ids, dtype=np.int32)
+        sl = np.ascontiguousarray(slots, dtype=np.int32)
+        T, K = i.shape
+        out = np.empty((T, self.n_slots), dtype=np.float32)
+        _check(lib.fmoe_pool_slot_logits(self.state, lg.ctypes.data, i.ctypes.data, sl.ctypes.data, T, K,
+                                         out.ctypes.data), "fmoe_pool_slot_logits")
+        return out
+
+    def stats(self):
+        h, m, r = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+        _check(lib.fmoe_pool_stats(self.state, ctypes.byref(h), ctypes.byref(m), ctypes.byref(r)), "fmoe_pool_stats")
+        return {"hits": h.value, "misses": m.value, "requests": r.value}

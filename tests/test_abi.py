@@ -128,3 +128,15 @@ def test_new_entry_points_check_arguments(fm):
     assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), 16, 16, 16, 32, 9, None, None) == fm.ERR_INVALID_ARG
     assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), None, 16, 16, 32, 2, None, None) == fm.ERR_INVALID_ARG
     assert lib.fmoe_moe_block_noalloc(ctypes.byref(L), 16, 16, 16, 40, 2, None, None) == fm.ERR_INVALID_ARG
+    # router projection: null or misaligned matrix, T / E / H out of range, logits overlapping x
+    assert lib.fmoe_router_logits(None, 4096, 1, 512, 8, 8192, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_router_logits(8, 4096, 1, 512, 8, 8192, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_router_logits(16, 4096, 17, 512, 8, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_router_logits(16, 4096, 1, 500, 8, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_router_logits(16, 4096, 1, 512, 0, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_router_logits(16, 1 << 20, 1, 512, 8, (1 << 20) + 64, None) == fm.ERR_INVALID_ARG
+    # route from x: K > E, a gate pointer without the gate vector
+    assert lib.fmoe_route_from_x(16, 4096, 1, 512, 8, 9, None, 1 << 20, 1 << 21, 1 << 22, None,
+                                 None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_route_from_x(16, 4096, 1, 512, 8, 2, None, 1 << 20, 1 << 21, 1 << 22, 1 << 23,
+                                 None) == fm.ERR_INVALID_ARG

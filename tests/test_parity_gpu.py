@@ -77,6 +77,81 @@ def test_route_matches_oracle(fm, E, K):
             assert_close(w[t].cpu().numpy(), rw, what="weights")
 
 
+@pytest.mark.parametrize("T,E,H", [(1, 8, 512), (3, 100, 192), (1, 512, 4096), (5, 512, 4096), (16, 512, 4096),
+                                   (16, 512, 2048)])
+def test_router_projection_matches_oracle(fm, T, E, H):
+    shape = dataclasses.replace(synth.TINY, hidden=H, n_experts=E)
+    w = synth.router_matrix(shape, layer=T)
+    x = synth.normal(7, T, (T, H))
+    wsg = synth.shared_gate_vector(shape, layer=T)
+    K = min(4, E)
+    logits, ids, weights, gate = fm.route_from_x(w.cuda(), x.cuda(), K, wsg.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.router_logits(w.numpy().view(np.uint16), x.numpy())
+    got = logits.cpu().numpy()
+    for t in range(T):
+        assert_close(got[t], ref[t], what=f"logits token {t}")
+        # the routing decision is taken on the GPU's own fp32 logits, so the
+        # oracle routes those exactly
+        rid, rw = oracle.route(got[t], K)
+        assert ids[t].cpu().tolist() == rid.tolist()
+        assert_close(weights[t].cpu().numpy(), rw, what="weights")
+        assert_close(gate[t:t + 1].cpu().numpy(), [oracle.shared_gate(wsg.numpy().view(np.uint16), x[t].numpy())],
+                     what="shared gate")
+    # the projection alone writes the same logits, bit for bit (fixed summation order)
+    again = fm.router_logits(w.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(again.cpu(), logits.cpu())
+
+
+def test_slot_pool_zipf_routing_matches_oracle(fm):
+    """A quarter of the experts in HBM slots, the rest copied in from pinned
+    host memory as the routing asks (Zipf(1.1) popularity); the block runs
+    against the slots with logits remapped to them.  Ids (mapped back from
+    slots) exact, outputs within 2e-3 of the oracle on the full expert set, at
+    T = 1 (single launch) and T = 4 (batched path)."""
+    shape = dataclasses.replace(synth.QWEN_Q4, name="pool_h1024_e64_top4_shared_i512_q4", hidden=1024, inter=512,
+                                n_experts=64)
+    K, S = shape.top_k, 16
+    nw = synth.blob_bytes(shape.bits, shape.hidden, shape.inter) // 4
+    host = torch.empty(shape.n_experts * nw, dtype=torch.int32, pin_memory=True)
+    host.copy_(gpu_pool(shape, 0, shape.n_experts).cpu())
+    slots = torch.zeros(S * nw, dtype=torch.int32, device="cuda")
+    shared = gpu_pool(shape, 0, 1, first=shape.n_experts)
+    wsg = synth.shared_gate_vector(shape, 0).cuda()
+    pool = fm.SlotPool(S, shape.n_experts, nw * 4, slots.data_ptr(), host.data_ptr())
+    layer = fm.Layer(shape.bits, shape.hidden, shape.inter, S, slots, shared, wsg)
+    copy = torch.cuda.Stream()
+    step = 0
+    for T, n_steps in ((1, 12), (4, 4)):
+        ws = fm.new_workspace(layer, T, K)
+        for _ in range(n_steps):
+            step += 1
+            logits = synth.zipf_logits(shape.seed, 500 + step, T, shape.n_experts, 1.1)
+            x = synth.normal(shape.seed, 600 + step, (T, shape.hidden))
+            res = synth.normal(shape.seed, 700 + step, (T, shape.hidden))
+            ids_dev, _ = fm.route(logits.cuda(), K)
+            ids = ids_dev.cpu().numpy()
+            sl_of, loads = pool.plan(ids.flatten().tolist(), keep=0)
+            pool.load(loads, stream=copy)
+            done = torch.cuda.Event()
+            done.record(copy)
+            torch.cuda.current_stream().wait_event(done)
+            slot_ids = np.array(sl_of, dtype=np.int32).reshape(T, K)
+            slot_logits = torch.from_numpy(pool.slot_logits(logits.numpy(), ids, slot_ids)).cuda()
+            out = fm.moe_block(layer, x.cuda(), slot_logits, res.cuda(), K, ws)
+            torch.cuda.synchronize()
+            assert fm.last_device_error(ws) == fm.OK
+            expert_of = {int(sl): int(e) for e, sl in zip(ids.flatten(), sl_of)}
+            got_slots = fm.ws_routing(ws, layer, T, K)["ids"].cpu().numpy()
+            for t in range(T):
+                ref = oracle_block(shape, 0, x[t:t + 1].numpy(), logits[t:t + 1].numpy(), res[t:t + 1].numpy(), K)
+                assert [expert_of[int(v)] for v in got_slots[t]] == list(ref["ids"][0]), (step, t)
+                assert_close(out[t].cpu().numpy(), ref["out"][0], what=f"pool step {step} token {t}")
+    st = pool.stats()
+    assert st["misses"] > S and st["hits"] > 0, st
+
+
 # ---------------------------------------------------------------------------
 # tiny block (every output, several draws, fused single-launch path)
 # ---------------------------------------------------------------------------
