@@ -413,6 +413,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
         // thread's additions (the fence waits here, off the critical path)
         mbar_wait(bar_zero, lpar, tmo, p.err, s_abort);
         fence_acq_rel_gpu();
+        // where each piece's expert blob is (the layer's routing was published
+        // before its input was complete, hence before bar_zero)
+        const int* ids_d = s_ids + (size_t)(l & 1) * kMaxSlots;
+        auto piece_blob = [&](int slot) -> const uint8_t* {
+          if (p.S && slot == 0) return lp.shared;
+          return lp.experts + (size_t)ids_d[slot] * p.blob;
+        };
+        if (kFusedSbGlobal && dact) {
+          for (int pidx = 0; pidx < np; ++pidx) {
+            const Piece pc = s_pc[pidx];
+            const uint8_t* sb0 = piece_blob(pc.slot) + lay.dsb_off + (size_t)pc.g0 * lay.dsb_group + (size_t)wb * RW * 4;
+            for (int gi = 0; gi < pc.ng; ++gi)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(sb0 + (size_t)gi * lay.dsb_group));
+          }
+        }
         mbar_wait(bar_dfull, lpar, tmo, p.err, s_abort);
         const uint32_t hd_base = (uint32_t)l * (uint32_t)nstg;
         int seen = 0;                                          // stages of this layer known finalised
@@ -465,8 +480,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
             }
             // the group's scale and bias per row: out += s * 2^64 * acc + b * sum(h)
             if (dact) {
-              const uint4* sbw = reinterpret_cast<const uint4*>(darea + pc.sb_off + (size_t)gi * lay.dsb_group +
-                                                                (size_t)wb * RW * 4);
+              const uint4* sbw = reinterpret_cast<const uint4*>(
+                  (kFusedSbGlobal ? piece_blob(pc.slot) + lay.dsb_off + (size_t)pc.g0 * lay.dsb_group
+                                  : darea + pc.sb_off) +
+                  (size_t)gi * lay.dsb_group + (size_t)wb * RW * 4);
 #pragma unroll
               for (int j = 0; j < MW; ++j) {
 #pragma unroll
@@ -551,7 +568,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
         // the previous layer's down work is done with the area
         if (l > 0) mbar_wait(bar_ddone, (uint32_t)((l - 1) & 1), tmo, p.err, s_abort);
         uint32_t total = 0;
-        for (int q = 0; q < np; ++q) total += (uint32_t)(s_pc[q].cnt * lay.dcol + s_pc[q].ng * lay.dsb_group);
+        for (int q = 0; q < np; ++q)
+          total += (uint32_t)(s_pc[q].cnt * lay.dcol + (kFusedSbGlobal ? 0 : s_pc[q].ng * lay.dsb_group));
         if (aborted()) {
           if (lane == 0) mbar_arrive_expect_tx(bar_dfull, 0);
           return;
@@ -565,8 +583,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
           const uint8_t* b = slot_blob(pc.slot);
           copy(darea + pc.col_off, b + lay.dq_off + (size_t)pc.i0 * lay.dcol, (uint32_t)(pc.cnt * lay.dcol),
                bar_dfull);
-          copy(darea + pc.sb_off, b + lay.dsb_off + (size_t)pc.g0 * lay.dsb_group,
-               (uint32_t)(pc.ng * lay.dsb_group), bar_dfull);
+          if (!kFusedSbGlobal)
+            copy(darea + pc.sb_off, b + lay.dsb_off + (size_t)pc.g0 * lay.dsb_group,
+                 (uint32_t)(pc.ng * lay.dsb_group), bar_dfull);
         }
       };
       bool darea_issued = false;

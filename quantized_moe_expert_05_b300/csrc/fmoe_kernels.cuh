@@ -118,12 +118,20 @@ constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, redu
 #ifndef FMOE_POLL_NS
 #define FMOE_POLL_NS 64
 #endif
+#ifndef FMOE_FUSED_SB_GLOBAL
+#define FMOE_FUSED_SB_GLOBAL 0
+#endif
 
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
 constexpr int kFusedDareaAfter = FMOE_FUSED_DAREA_AFTER;
 constexpr uint32_t kFusedCopyBytes = FMOE_FUSED_COPY_BYTES;
 constexpr int kFusedIssueLanes = FMOE_FUSED_ISSUE_LANES;
 constexpr unsigned kPollNs = FMOE_POLL_NS;
+// 1: the down groups' (scale,bias) words are read from L2 at each group's
+// fold (asked into L2 when the layer starts) instead of being copied into
+// shared memory, and the ring gets the space (4 stages instead of 3 at the
+// Qwen shape); measured 1 % slower, so off
+constexpr bool kFusedSbGlobal = FMOE_FUSED_SB_GLOBAL != 0;
 
 // A block's intermediate columns within one slot: columns [i0, i0+cnt) of
 // slot `slot`, local indices [loc, loc+cnt); in the block's down area its
@@ -149,7 +157,7 @@ __host__ __device__ inline int block_pieces(int NS, int I, int c, int n, const B
     const int g0 = i0 / kGroup, ng = (i0 + cnt - 1) / kGroup - g0 + 1;
     const int cb = (int)round_up((size_t)cnt * lay.dcol, 128), sbb = (int)round_up((size_t)ng * lay.dsb_group, 128);
     if (np < max_pieces) pc[np] = Piece{slot, i0, cnt, u, off, off + cb, g0, ng};
-    off += cb + sbb;
+    off += cb + (kFusedSbGlobal ? 0 : sbb);
     u += cnt;
     v += cnt;
     ++np;
