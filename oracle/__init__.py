@@ -29,7 +29,10 @@ What is computed (all in fp64; fp32 and bf16 inputs are widened exactly):
               shared expert", shader list "MoE combine + residual + sigmoid gate")
 * combine     out = residual + sum_k w_k y_k + g y_shared
 * RMSNorm     x / sqrt(mean(x^2) + eps), unit weight (shader list: two-stage
-              RMS normalisation), used pre-norm between stacked blocks
+              RMS normalisation), used pre-norm between stacked blocks; times
+              a learned weight vector when one is given
+* o_proj      y = W x (+ residual) for a dense quantised matrix in row records
+              (same write-up, "per-layer pipeline": CMD2's o_proj)
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (hand-worked examples, closed forms, brute force and invariants); see the
@@ -53,5 +56,8 @@ from .moe import (  # noqa: F401
     combine,
     moe_block,
     rms_norm,
+    dense_record_words,
+    dense_weights,
+    dense_matvec,
     stack_decode,
 )

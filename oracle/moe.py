@@ -198,6 +198,32 @@ def shared_gate(wsg_bf16: np.ndarray, x: np.ndarray) -> float:
     return float(sigmoid(w @ np.asarray(x, dtype=np.float64)))
 
 
+def dense_record_words(bits: int, hidden: int) -> tuple:
+    """A dense quantised matrix (o_proj) is N row records, each the row's
+    codes (hidden*bits/32 words, lowest bits first) then its (scale,bias)
+    words (one per 64 columns), padded to a multiple of 16 bytes.  Returns
+    (code words, scale words, words per record)."""
+    qw = hidden * bits // 32
+    sw = hidden // GROUP
+    return qw, sw, -(-(qw + sw) * 4 // 16) * 16 // 4
+
+
+def dense_weights(words: np.ndarray, bits: int, n_rows: int, hidden: int) -> np.ndarray:
+    """W [N][H] fp64 of a dense quantised matrix given as uint32 words.
+    Pinned by records built field by field from random codes and dyadic
+    scales/biases, read back exactly."""
+    qw, sw, rw = dense_record_words(bits, hidden)
+    rec = np.asarray(words, dtype=np.uint32).reshape(n_rows, rw)
+    return dequantize(rec[:, :qw], rec[:, qw:qw + sw], bits)
+
+
+def dense_matvec(w: np.ndarray, x: np.ndarray, residual=None) -> np.ndarray:
+    """y = W x (+ residual) for one token [H] or T tokens [T][H]: the o_proj
+    of [FM] "per-layer pipeline" (CMD2), a dense 4-bit matvec."""
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+    return y if residual is None else y + np.asarray(residual, dtype=np.float64)
+
+
 def router_logits(w_router_bf16: np.ndarray, x: np.ndarray) -> np.ndarray:
     """Router logits l = W_r x of one token (x [H] -> [E]) or of T tokens
     (x [T][H] -> [T][E]), W_r [E][H] given as bf16 bit patterns.
@@ -265,10 +291,14 @@ def moe_block(get_expert, x, logits, residual, k, shared=None, wsg=None):
 # ---------------------------------------------------------------------------
 # stacked decode
 # ---------------------------------------------------------------------------
-def rms_norm(h, eps: float):
-    """h / sqrt(mean(h^2) + eps), unit weight ([FM] shader list: RMSNorm)."""
+def rms_norm(h, eps: float, weight=None):
+    """h / sqrt(mean(h^2) + eps), times a learned weight vector when one is
+    given ([FM] shader list: RMSNorm; "per-layer pipeline": the norm of CMD2).
+    Pinned by constant vectors, unit-weight identity and linearity in the
+    weight."""
     h = np.asarray(h, dtype=np.float64)
-    return h / np.sqrt(np.mean(h * h) + eps)
+    x = h / np.sqrt(np.mean(h * h) + eps)
+    return x if weight is None else x * np.asarray(weight, dtype=np.float64)
 
 
 def stack_decode(get_expert_l, h0, logits, k, eps, shared_l=None, wsg_l=None):

@@ -273,6 +273,29 @@ def shared_gate_vector(shape: BlockShape, layer: int = 0, seed: Optional[int] = 
     return w.to(torch.bfloat16).view(torch.int16)
 
 
+def dense_matrix(n_rows: int, hidden: int, bits: int, seed: int, tag: int = 0, scale=(0.002, 0.02),
+                 bias=(-0.1, 0.0), device="cpu") -> torch.Tensor:
+    """A dense quantised matrix (o_proj) as int32 words: n_rows records of the
+    row's codes, then its (scale,bias) words (one per 64 columns), padded to
+    16 bytes; codes uniform, scale U(scale), bias U(bias) as bf16."""
+    qw, sw = hidden * bits // 32, hidden // GROUP
+    rw = _round_up((qw + sw) * 4, 16) // 4
+    rows = torch.arange(n_rows, dtype=torch.int64, device=device).reshape(-1, 1)
+    words = torch.zeros((n_rows, rw), dtype=torch.int64, device=device)
+    words[:, :qw] = _word_hash(_stream_key(seed, tag, 7, 0), rows,
+                               torch.arange(qw, dtype=torch.int64, device=device).reshape(1, -1))
+    gi = torch.arange(sw, dtype=torch.int64, device=device).reshape(1, -1)
+    s = _uniform_bf16_bits(_word_hash(_stream_key(seed, tag, 7, 1), rows, gi), scale[0], scale[1])
+    b = _uniform_bf16_bits(_word_hash(_stream_key(seed, tag, 7, 2), rows, gi), bias[0], bias[1])
+    words[:, qw:qw + sw] = s | (b << 16)
+    return (words - ((words >> 31) << 32)).to(torch.int32).reshape(-1)
+
+
+def norm_weight(hidden: int, seed: int, tag: int = 0) -> torch.Tensor:
+    """A learned RMSNorm weight stand-in: fp32 1 + N(0, 0.1^2)."""
+    return 1.0 + normal(seed, 200 + tag, (hidden,), std=0.1)
+
+
 def router_matrix(shape: BlockShape, layer: int = 0, seed: Optional[int] = None) -> torch.Tensor:
     """bf16 bit patterns (int16 tensor [E][H]) of W_r ~ N(0, 1/H): with x ~ N(0, 1)
     the logits are about N(0, 1), as the workloads' router logits."""

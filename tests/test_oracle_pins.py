@@ -436,10 +436,46 @@ def pin_router_logits():
     assert abs(om.shared_gate(Wr[0], X[0]) - float(om.sigmoid(om.router_logits(Wr[:1], X[0])[0]))) < 1e-15
 
 
+def pin_dense_records():
+    rng = np.random.default_rng(21)
+    for bits, N, H in ((4, 5, 128), (2, 3, 192)):
+        codes = rng.integers(0, 1 << bits, size=(N, H))
+        scales = rng.choice([0.25, 0.5, 1.0, 2.0, 0.125], size=(N, H // 64))
+        biases = rng.choice([-1.0, -0.5, 0.0, 0.25, 3.0], size=(N, H // 64))
+        q = pack(codes, bits)
+        sbw = np.array([[bf16(s) | (bf16(b) << 16) for s, b in zip(rs, rb)] for rs, rb in zip(scales, biases)],
+                       dtype=np.uint32)
+        rec = _up((q.shape[1] + sbw.shape[1]) * 4, 16) // 4
+        words = np.zeros((N, rec), dtype=np.uint32)
+        words[:, :q.shape[1]] = q
+        words[:, q.shape[1]:q.shape[1] + sbw.shape[1]] = sbw
+        W = om.dense_weights(words.reshape(-1), bits, N, H)
+        want = codes * np.repeat(scales, 64, axis=1) + np.repeat(biases, 64, axis=1)
+        assert np.array_equal(W, want)
+        # integer inputs: every product and sum is exact in fp64
+        x = rng.integers(-20, 21, size=H)
+        res = rng.integers(-5, 6, size=N)
+        exact = [sum(Fraction(float(want[r, c])) * int(x[c]) for c in range(H)) + int(res[r]) for r in range(N)]
+        assert list(om.dense_matvec(W, x.astype(float), res.astype(float))) == [float(v) for v in exact]
+
+
+def pin_rms_weight():
+    rng = np.random.default_rng(22)
+    h = rng.standard_normal(64)
+    w = rng.standard_normal(64)
+    assert np.array_equal(om.rms_norm(h, 1e-6, np.ones(64)), om.rms_norm(h, 1e-6))
+    assert np.array_equal(om.rms_norm(h, 1e-6, 2 * w), 2 * om.rms_norm(h, 1e-6, w))
+    # constant input c: every element is sign(c) / sqrt(1 + eps / c^2), times its weight
+    c, eps = -0.75, 1e-6
+    want = -1.0 / math.sqrt(1.0 + eps / (c * c)) * w
+    assert np.allclose(om.rms_norm(np.full(64, c), eps, w), want, rtol=1e-14)
+
+
 PINS = [pin_unpack_golden, pin_dequant_golden, pin_two_groups, pin_fma_identity,
         pin_group_decomposition, pin_random_blob_fields, pin_constant_rows, pin_route_bruteforce,
         pin_route_weights, pin_special_values, pin_zero_weight, pin_page_sizes,
-        pin_layout_matches_generator, pin_block_closed_form, pin_stack_closed_form, pin_router_logits]
+        pin_layout_matches_generator, pin_block_closed_form, pin_stack_closed_form, pin_router_logits,
+        pin_dense_records, pin_rms_weight]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -557,6 +593,22 @@ def _router_transposed(w, x):
     return np.asarray(x, dtype=np.float64) @ om.bf16_to_f64(w)
 
 
+def _dense_scales_first(words, bits, n_rows, hidden):
+    qw, sw, rw = om.dense_record_words(bits, hidden)
+    rec = np.asarray(words, dtype=np.uint32).reshape(n_rows, rw)
+    return om.dequantize(rec[:, sw:sw + qw], rec[:, :sw], bits)
+
+
+def _dense_no_padding(words, bits, n_rows, hidden):
+    qw, sw, _ = om.dense_record_words(bits, hidden)
+    rec = np.asarray(words, dtype=np.uint32)[:n_rows * (qw + sw)].reshape(n_rows, qw + sw)
+    return om.dequantize(rec[:, :qw], rec[:, qw:], bits)
+
+
+def _rms_weight_ignored(h, eps, weight=None):
+    return _ORIG["rms_norm"](h, eps)
+
+
 def _combine_no_residual(residual, routed_y, weights, shared_y=None, g=None):
     return _ORIG["combine"](np.zeros_like(np.asarray(residual, dtype=np.float64)),
                             routed_y, weights, shared_y, g)
@@ -566,18 +618,20 @@ def _combine_unweighted_shared(residual, routed_y, weights, shared_y=None, g=Non
     return _ORIG["combine"](residual, routed_y, weights, shared_y, None if g is None else 1.0)
 
 
-def _rms_eps_outside(h, eps):
+def _rms_eps_outside(h, eps, weight=None):
     h = np.asarray(h, dtype=np.float64)
-    return h / (np.sqrt(np.mean(h * h)) + eps)
+    x = h / (np.sqrt(np.mean(h * h)) + eps)
+    return x if weight is None else x * weight
 
 
-def _rms_sum(h, eps):
+def _rms_sum(h, eps, weight=None):
     h = np.asarray(h, dtype=np.float64)
-    return h / np.sqrt(np.sum(h * h) + eps)
+    x = h / np.sqrt(np.sum(h * h) + eps)
+    return x if weight is None else x * weight
 
 
 _ORIG = {n: getattr(om, n) for n in ("unpack_codes", "dequantize", "route", "combine", "layout",
-                                      "expert_weights", "router_logits")}
+                                      "expert_weights", "router_logits", "rms_norm")}
 
 MUTANTS = [
     ("unpack_codes", _unpack_msb_first),
@@ -598,6 +652,9 @@ MUTANTS = [
     ("router_logits", _router_low_half),
     ("router_logits", _router_rows_shifted),
     ("router_logits", _router_transposed),
+    ("dense_weights", _dense_scales_first),
+    ("dense_weights", _dense_no_padding),
+    ("rms_norm", _rms_weight_ignored),
     ("combine", _combine_no_residual),
     ("combine", _combine_unweighted_shared),
     ("rms_norm", _rms_eps_outside),
