@@ -584,6 +584,48 @@ def measure_pool(n_tokens, warmup, dev, n_slots=128):
             "routing": "Zipf(1.1) over 512 experts, top-4 + shared (shared expert resident)"}
 
 
+def measure_dense(H, bits, T, steps, warmup, dev, n_mat=8):
+    """The o_proj: y = residual + W x for a dense quantised H x H matrix (row
+    records), T tokens; one graph holds n_mat launches over n_mat different
+    matrices, each read from HBM once per step (L2 flushed before every step,
+    outside the events).  Returns GB/s of matrix bytes and us per call."""
+    import torch
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    ws = [synth.dense_matrix(H, H, bits, seed=31, tag=i, device=dev) for i in range(n_mat)]
+    x = synth.normal(31, 900 + T, (T, H)).to(dev)
+    res = synth.normal(31, 901 + T, (T, H)).to(dev)
+    out = torch.empty((n_mat, T, H), dtype=torch.float32, device=dev)
+    for i in range(n_mat):
+        fm.dense_gemv(ws[i], bits, H, x, residual=res, y=out[i])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_mat):
+            fm.dense_gemv(ws[i], bits, H, x, residual=res, y=out[i])
+    flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.sum()
+        evs[i][0].record(stream)
+        g.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)[steps // 2]        # median step
+    nbytes = n_mat * H * fm.dense_row_bytes(bits, H)
+    value = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = load_peaks()
+    del ws, flush, g
+    torch.cuda.empty_cache()
+    return {"T": T, "H": H, "bits": bits, "gbs": value, "frac": value / peak, "us_per_call": ms * 1e3 / n_mat,
+            "bytes_per_call": nbytes // n_mat}
+
+
 def run_batch(args):
     """--workload qwen_q4_zipf: the batched block at --tokens T; value =
     distinct experts' bytes (routed + shared) per second."""
@@ -877,6 +919,7 @@ def main():
         for nm, sh in (("qwen", synth.QWEN_Q4), ("stack48", synth.STACK48)):
             for T in (1, 16):
                 cfgs["router_projection"][f"{nm}_T{T}"] = measure_router(sh, T, 50, 3, dev)
+        cfgs["o_proj_dense_q4"] = {f"T{T}": measure_dense(4096, 4, T, 50, 3, dev) for T in (1, 16)}
         line["configs"] = cfgs
     if world == 1 and not args.no_cpu_baseline:
         n = 16 if shape.hidden >= 4096 else 32

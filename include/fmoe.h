@@ -168,6 +168,30 @@ fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, i
                               float* gate, void* stream);
 
 /*
+ * The MoE-adjacent steps of a layer (flash-moe "per-layer pipeline": CMD2
+ * runs o_proj and the norm on the GPU before the routing).
+ *
+ * fmoe_dense_row_bytes: bytes of one row record of a dense quantised matrix:
+ *   the row's codes (hidden*bits/8 bytes, lowest bits first within each
+ *   32-bit word), then one (scale,bias) word per 64 columns (scale bf16 in
+ *   bits 0..15, bias bf16 in bits 16..31), padded to a multiple of 16 bytes.
+ *   0 for a bad shape.
+ * fmoe_dense_gemv: y[t][r] = sum_j (q[r][j]*s + b) * x[t][j] (+ residual[t][r])
+ *   for a dense matrix of N row records (the o_proj: N = H); bits 4 or 2.
+ *   w 16-byte aligned, N row records; x fp32 [T][H]; residual fp32 [T][N] or
+ *   NULL, may be y (in-place residual add); y fp32 [T][N] must not overlap
+ *   x or w.  1 <= T <= FMOE_MAX_TOKENS, H a multiple of 64 up to
+ *   FMOE_MAX_HIDDEN, N >= 1.  Deterministic (fixed summation order).
+ * fmoe_rmsnorm: x[t] = h[t] / sqrt(mean(h[t]^2) + eps) * weight (weight fp32
+ *   [H], or NULL for unit weight); x may be h.
+ */
+size_t fmoe_dense_row_bytes(int bits, int hidden);
+fmoe_status fmoe_dense_gemv(const void* w, int bits, int N, int hidden, const float* x, int T,
+                            const float* residual, float* y, void* stream);
+fmoe_status fmoe_rmsnorm(const float* h, const float* weight, int T, int hidden, float eps, float* x,
+                         void* stream);
+
+/*
  * Expert forward for given ids (flash-moe CMD3 "expert forward", without the
  * combine): for token t and slot k < K, y[t][k] = Wd (silu(Wg x_t) * (Wu x_t))
  * of routed expert ids[t][k]; if layer->has_shared, slot K holds the shared

@@ -137,6 +137,35 @@ fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, i
                                 static_cast<cudaStream_t>(stream)));
 }
 
+size_t fmoe_dense_row_bytes(int bits, int hidden) {
+  if ((bits != 4 && bits != 2) || hidden <= 0 || hidden % kGroup || hidden > FMOE_MAX_HIDDEN) return 0;
+  return (size_t)dense_row_bytes(bits, hidden);
+}
+
+fmoe_status fmoe_dense_gemv(const void* w, int bits, int N, int hidden, const float* x, int T, const float* residual,
+                            float* y, void* stream) {
+  if (fmoe_dense_row_bytes(bits, hidden) == 0 || N < 1 || T < 1 || T > FMOE_MAX_TOKENS) return FMOE_ERR_INVALID_ARG;
+  if (!host_vec_ok(w) || !host_vec_ok(x) || y == nullptr || !aligned(y, 4)) return FMOE_ERR_INVALID_ARG;
+  if (residual != nullptr && !aligned(residual, 4)) return FMOE_ERR_INVALID_ARG;
+  const size_t yb = (size_t)T * N * 4;
+  if (host_overlap(y, yb, x, (size_t)T * hidden * 4) ||
+      host_overlap(y, yb, w, (size_t)N * dense_row_bytes(bits, hidden)))
+    return FMOE_ERR_INVALID_ARG;
+  if (residual != nullptr && residual != y && host_overlap(y, yb, residual, yb)) return FMOE_ERR_INVALID_ARG;
+  return from_cuda(launch_dense_gemv(static_cast<const uint8_t*>(w), bits, N, hidden, x, T, residual, y,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+fmoe_status fmoe_rmsnorm(const float* h, const float* weight, int T, int hidden, float eps, float* x, void* stream) {
+  if (h == nullptr || x == nullptr || !aligned(h, 4) || !aligned(x, 4)) return FMOE_ERR_INVALID_ARG;
+  if (weight != nullptr && !aligned(weight, 4)) return FMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > FMOE_MAX_TOKENS || hidden < 1 || hidden > FMOE_MAX_HIDDEN || !(eps >= 0.f))
+    return FMOE_ERR_INVALID_ARG;
+  const size_t hb = (size_t)T * hidden * 4;
+  if (x != h && host_overlap(x, hb, h, hb)) return FMOE_ERR_INVALID_ARG;
+  return from_cuda(launch_rmsnorm_w(h, weight, T, hidden, eps, x, static_cast<cudaStream_t>(stream)));
+}
+
 fmoe_status fmoe_expert_ffn(const fmoe_layer* layer, const int32_t* ids, int T, int K, const float* x, float* y,
                             void* ws, void* stream) {
   fmoe_status s = check_layer(layer, true);

@@ -936,34 +936,10 @@ __global__ void batch_combine_kernel(BatchArgs a) {
   reinterpret_cast<float4*>(a.out)[idx] = acc;
 }
 
-// x = h / sqrt(mean(h^2) + eps) (unit weight): one block, a fixed summation
-// order (the general path of a stack; the persistent kernel normalises in
-// its own prologue)
-constexpr int kNormThreads = 1024;
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ h, float* __restrict__ x,
-                                                               int H, float eps) {
-  __shared__ float s_part[kNormThreads / 32];
-  __shared__ float s_rinv;
-  float ss = 0.f;
-  for (int j = threadIdx.x; j < H; j += kNormThreads) {
-    const float v = __ldcg(h + j);
-    ss += v * v;
-  }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kNormThreads / 32; ++w) t += s_part[w];
-    s_rinv = 1.0f / sqrtf(t / (float)H + eps);
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < H; j += kNormThreads) x[j] = __ldcg(h + j) * s_rinv;
-}
-
+// x = h / sqrt(mean(h^2) + eps) (unit weight), one token: the general path
+// of a stack (the persistent kernel normalises in its own input phase)
 cudaError_t launch_rmsnorm(const float* h, float* x, int H, float eps, cudaStream_t st) {
-  rmsnorm_kernel<<<1, kNormThreads, 0, st>>>(h, x, H, eps);
-  return cudaGetLastError();
+  return launch_rmsnorm_w(h, nullptr, 1, H, eps, x, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,161 @@
+// The MoE-adjacent steps of a layer: the dense quantised matrix-vector
+// product of the attention output projection (o_proj), with the residual
+// added, and RMSNorm with a learned weight.
+//
+// flash-moe write-up (discuss.pytorch.kr), section "per-layer pipeline": the
+// second command buffer runs o_proj, the norm, the routing logits and the
+// shared expert on the GPU; section "hand-written Metal compute shaders": a
+// two-stage RMS normalisation and the 4-bit dequant matvec.
+//
+// A dense matrix is N row records (the row's codes, then one (scale,bias)
+// word per 64 columns, padded to 16 bytes).  One warp computes one output row
+// for all T <= 16 tokens (held in registers: the kernel is instantiated for
+// 1, 2, 4, 8 and 16): lane l takes code word l of every 128-byte span of the
+// row (coalesced loads of codes and of the inputs they meet), issues eight
+// such loads before their arithmetic, unpacks each word once and meets every
+// token's inputs with it, adding s * sum(q * x) + b * sum(x) with the word's
+// group scale and bias.  Sums are taken in a fixed order (words in order
+// within a lane, then a shuffle tree), so results are deterministic.
+#include "fmoe_kernels.cuh"
+
+namespace fmoe {
+
+namespace {
+
+constexpr int kDgWarps = 8;
+constexpr int kDgThreads = 32 * kDgWarps;
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// NT: tokens held in registers, the smallest of 1, 2, 4, 8, 16 that is >= T.
+// Lane l takes code word l of every 128-byte span of the row, so that the
+// warp's loads of codes and of the inputs they meet are both coalesced.
+template <int BITS, int NT>
+__global__ void __launch_bounds__(kDgThreads) dense_gemv_kernel(const uint8_t* __restrict__ w, int N, int H, int rec,
+                                                              const float* __restrict__ x, int T,
+                                                              const float* residual, float* y) {
+  constexpr int CPW = 32 / BITS;                        // columns per 32-bit word
+  constexpr int PASS = 8;                               // words per lane loaded before their arithmetic
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kDgWarps + warp;
+  if (row >= N) return;                                 // whole warps only: no barrier below
+  const uint8_t* r = w + (size_t)row * rec;
+  const uint32_t* codes = reinterpret_cast<const uint32_t*>(r);
+  const uint32_t* sbw = reinterpret_cast<const uint32_t*>(r + (size_t)H * BITS / 8);
+  const int nw = H / CPW / 32;                          // words per lane (H is a multiple of 64)
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int p0 = 0; p0 < nw; p0 += PASS) {
+    uint32_t q[PASS];
+#pragma unroll
+    for (int j = 0; j < PASS; ++j) q[j] = p0 + j < nw ? ld_stream_u32(codes + 32 * (p0 + j) + lane) : 0u;
+#pragma unroll
+    for (int j = 0; j < PASS; ++j) {
+      if (p0 + j < nw) {
+        const int c0 = (32 * (p0 + j) + lane) * CPW;     // the word's first column
+        const uint32_t sb = __ldg(sbw + c0 / kGroup);
+        float qv[CPW];
+#pragma unroll
+        for (int i = 0; i < CPW; ++i) qv[i] = (float)((q[j] >> (BITS * i)) & ((1u << BITS) - 1u));
+        const float s = bf16lo(sb), b = bf16hi(sb);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t < T) {
+            const float4* xp = reinterpret_cast<const float4*>(x + (size_t)t * H + c0);
+            float sq = 0.f, sx = 0.f;
+#pragma unroll
+            for (int v = 0; v < CPW / 4; ++v) {
+              const float4 a = __ldg(xp + v);
+              sq = fmaf(qv[4 * v], a.x, sq);
+              sq = fmaf(qv[4 * v + 1], a.y, sq);
+              sq = fmaf(qv[4 * v + 2], a.z, sq);
+              sq = fmaf(qv[4 * v + 3], a.w, sq);
+              sx += (a.x + a.y) + (a.z + a.w);
+            }
+            acc[t] = fmaf(s, sq, fmaf(b, sx, acc[t]));
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    if (t < T) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) {
+        const size_t o = (size_t)t * N + row;
+        y[o] = residual != nullptr ? residual[o] + v : v;
+      }
+    }
+  }
+}
+
+// One block per token: x = h / sqrt(mean(h^2) + eps) (* w when given); the
+// sum of squares in a fixed order (strided per thread, shuffle tree per
+// warp, warps in order).  x may be h.
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_w_kernel(const float* h, const float* __restrict__ w, int H,
+                                                                float eps, float* x) {
+  __shared__ float s_part[kNormThreads / 32];
+  __shared__ float s_rinv;
+  const float* ht = h + (size_t)blockIdx.x * H;
+  float* xt = x + (size_t)blockIdx.x * H;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < H; j += kNormThreads) {
+    const float v = __ldcg(ht + j);
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < kNormThreads / 32; ++k) t += s_part[k];
+    s_rinv = 1.0f / sqrtf(t / (float)H + eps);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < H; j += kNormThreads) {
+    const float v = __ldcg(ht + j) * s_rinv;
+    xt[j] = w != nullptr ? v * __ldg(w + j) : v;
+  }
+}
+
+}  // namespace
+
+int dense_row_bytes(int bits, int H) {
+  const int qb = H * bits / 8, sb = H / kGroup * 4;
+  return (qb + sb + 15) / 16 * 16;
+}
+
+cudaError_t launch_dense_gemv(const uint8_t* w, int bits, int N, int H, const float* x, int T, const float* residual,
+                              float* y, cudaStream_t st) {
+  const int blocks = (N + kDgWarps - 1) / kDgWarps;
+  const int rec = dense_row_bytes(bits, H);
+#define FMOE_DG(B, NT) dense_gemv_kernel<B, NT><<<blocks, kDgThreads, 0, st>>>(w, N, H, rec, x, T, residual, y)
+  if (bits == 4) {
+    if (T <= 1) FMOE_DG(4, 1);
+    else if (T <= 2) FMOE_DG(4, 2);
+    else if (T <= 4) FMOE_DG(4, 4);
+    else if (T <= 8) FMOE_DG(4, 8);
+    else FMOE_DG(4, 16);
+  } else {
+    if (T <= 1) FMOE_DG(2, 1);
+    else if (T <= 2) FMOE_DG(2, 2);
+    else if (T <= 4) FMOE_DG(2, 4);
+    else if (T <= 8) FMOE_DG(2, 8);
+    else FMOE_DG(2, 16);
+  }
+#undef FMOE_DG
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_w(const float* h, const float* w, int T, int H, float eps, float* x, cudaStream_t st) {
+  rmsnorm_w_kernel<<<T, kNormThreads, 0, st>>>(h, w, H, eps, x);
+  return cudaGetLastError();
+}
+
+}  // namespace fmoe

@@ -69,6 +69,15 @@ BatchGeom batch_geometry(int bits, int H, int I, int device);
 // per block (host arithmetic only).
 BatchGeom batch_geometry_for(int bits, int H, int I, int sms, int smem_max);
 
+// RMSNorm block size (fmoe_dense.cu)
+constexpr int kNormThreads = 1024;
+// record bytes of a dense quantised row; y[t] = W x[t] (+ residual[t]) for
+// a dense matrix of N row records; x = RMSNorm(h) (* w) for T tokens
+// (fmoe_dense.cu)
+int dense_row_bytes(int bits, int H);
+cudaError_t launch_dense_gemv(const uint8_t* w, int bits, int N, int H, const float* x, int T, const float* residual,
+                              float* y, cudaStream_t st);
+cudaError_t launch_rmsnorm_w(const float* h, const float* w, int T, int H, float eps, float* x, cudaStream_t st);
 // logits[t][e] = w[e] . x[t] (fmoe_router.cu)
 cudaError_t launch_router(const uint16_t* w, const float* x, int T, int H, int E, float* logits, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights,

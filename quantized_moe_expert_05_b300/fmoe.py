@@ -68,6 +68,9 @@ def _load() -> ctypes.CDLL:
         "fmoe_moe_block_noalloc": (I, [LP, P, P, P, P, I, P, P]),
         "fmoe_debug_launch_geometry": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
         "fmoe_debug_block_pieces": (I, [I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64), I]),
+        "fmoe_dense_row_bytes": (Z, [I, I]),
+        "fmoe_dense_gemv": (I, [P, I, I, I, P, I, P, P, P]),
+        "fmoe_rmsnorm": (I, [P, P, I, I, F, P, P]),
         "fmoe_pool_state_bytes": (Z, [I, I]),
         "fmoe_pool_init": (I, [P, Z, I, I, Z, P, P]),
         "fmoe_pool_plan": (I, [P, P, I, I, P, P, ctypes.POINTER(I)]),
@@ -163,6 +166,31 @@ def route(logits: torch.Tensor, K: int, ids: Optional[torch.Tensor] = None,
         weights = torch.empty((T, K), dtype=torch.float32, device=logits.device)
     _check(lib.fmoe_route(_ptr(logits), T, E, K, _ptr(ids), _ptr(weights), _stream(stream)), "fmoe_route")
     return ids, weights
+
+
+def dense_row_bytes(bits: int, hidden: int) -> int:
+    return int(lib.fmoe_dense_row_bytes(bits, hidden))
+
+
+def dense_gemv(w: torch.Tensor, bits: int, n_rows: int, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+               y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[t] = W x[t] (+ residual[t]) for a dense quantised matrix of n_rows row records."""
+    T, H = x.shape
+    if y is None:
+        y = torch.empty((T, n_rows), dtype=torch.float32, device=x.device)
+    _check(lib.fmoe_dense_gemv(_ptr(w), bits, n_rows, H, _ptr(x), T, _ptr(residual), _ptr(y), _stream(stream)),
+           "fmoe_dense_gemv")
+    return y
+
+
+def rmsnorm(h: torch.Tensor, eps: float, weight: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    """x[t] = h[t] / sqrt(mean(h[t]^2) + eps) (* weight)."""
+    T, H = h.shape
+    if x is None:
+        x = torch.empty_like(h)
+    _check(lib.fmoe_rmsnorm(_ptr(h), _ptr(weight), T, H, eps, _ptr(x), _stream(stream)), "fmoe_rmsnorm")
+    return x
 
 
 def router_logits(w_router: torch.Tensor, x: torch.Tensor, logits: Optional[torch.Tensor] = None,

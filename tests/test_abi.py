@@ -135,6 +135,20 @@ def test_new_entry_points_check_arguments(fm):
     assert lib.fmoe_router_logits(16, 4096, 1, 500, 8, 1 << 20, None) == fm.ERR_INVALID_ARG
     assert lib.fmoe_router_logits(16, 4096, 1, 512, 0, 1 << 20, None) == fm.ERR_INVALID_ARG
     assert lib.fmoe_router_logits(16, 1 << 20, 1, 512, 8, (1 << 20) + 64, None) == fm.ERR_INVALID_ARG
+    # dense matrix rows: the record size is the oracle's, bad shapes are refused
+    import oracle
+    for bits in (4, 2):
+        for H in (64, 192, 512, 2048, 4096, 8192):
+            assert lib.fmoe_dense_row_bytes(bits, H) == oracle.dense_record_words(bits, H)[2] * 4
+    assert lib.fmoe_dense_row_bytes(3, 512) == 0 and lib.fmoe_dense_row_bytes(4, 500) == 0
+    # dense matvec: bad bits, T out of range, y overlapping x
+    assert lib.fmoe_dense_gemv(16, 3, 8, 512, 4096, 1, None, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_dense_gemv(16, 4, 8, 512, 4096, 17, None, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_dense_gemv(16, 4, 8, 512, 4096, 1, None, 4096 + 64, None) == fm.ERR_INVALID_ARG
+    # rmsnorm: T out of range, negative eps, x overlapping h without being h
+    assert lib.fmoe_rmsnorm(4096, None, 0, 512, 1e-6, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_rmsnorm(4096, None, 1, 512, -1.0, 1 << 20, None) == fm.ERR_INVALID_ARG
+    assert lib.fmoe_rmsnorm(4096, None, 2, 512, 1e-6, 4096 + 64, None) == fm.ERR_INVALID_ARG
     # route from x: K > E, a gate pointer without the gate vector
     assert lib.fmoe_route_from_x(16, 4096, 1, 512, 8, 9, None, 1 << 20, 1 << 21, 1 << 22, None,
                                  None) == fm.ERR_INVALID_ARG

@@ -104,6 +104,40 @@ def test_router_projection_matches_oracle(fm, T, E, H):
     assert torch.equal(again.cpu(), logits.cpu())
 
 
+@pytest.mark.parametrize("bits,N,H,T", [(4, 4096, 4096, 1), (4, 4096, 4096, 16), (2, 192, 512, 3), (4, 1000, 2048, 5),
+                                         (2, 2048, 2048, 1)])
+def test_dense_gemv_matches_oracle(fm, bits, N, H, T):
+    w = synth.dense_matrix(N, H, bits, seed=9, tag=bits * 100 + T)
+    x = synth.normal(9, 10 + T, (T, H))
+    res = synth.normal(9, 20 + T, (T, N))
+    W = oracle.dense_weights(w.numpy().view(np.uint32), bits, N, H)
+    ref = oracle.dense_matvec(W, x.numpy(), res.numpy())
+    wd = w.cuda()
+    y = fm.dense_gemv(wd, bits, N, x.cuda(), residual=res.cuda())
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert_close(y[t].cpu().numpy(), ref[t], what=f"o_proj token {t}")
+    # in place: residual and output the same buffer, and bit for bit the same result
+    y2 = res.cuda()
+    fm.dense_gemv(wd, bits, N, x.cuda(), residual=y2, y=y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y2.cpu(), y.cpu())
+
+
+@pytest.mark.parametrize("T,H", [(1, 4096), (16, 4096), (3, 2048), (2, 192)])
+def test_rmsnorm_weight_matches_oracle(fm, T, H):
+    h = synth.normal(11, T, (T, H)) * 3.0
+    wn = synth.norm_weight(H, 11, T)
+    x = fm.rmsnorm(h.cuda(), 1e-6, wn.cuda())
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert_close(x[t].cpu().numpy(), oracle.rms_norm(h[t].numpy(), 1e-6, wn.numpy()), what=f"rmsnorm token {t}")
+    hd = h.cuda()
+    fm.rmsnorm(hd, 1e-6, wn.cuda(), x=hd)            # in place
+    torch.cuda.synchronize()
+    assert torch.equal(hd.cpu(), x.cpu())
+
+
 def test_slot_pool_zipf_routing_matches_oracle(fm):
     """A quarter of the experts in HBM slots, the rest copied in from pinned
     host memory as the routing asks (Zipf(1.1) popularity); the block runs
