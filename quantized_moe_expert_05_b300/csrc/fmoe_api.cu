@@ -355,7 +355,7 @@ fmoe_status fmoe_debug_block_pieces(int bits, int hidden, int inter, int K, int 
   const BlobLayout lay = blob_layout(bits, hidden, inter);
   Piece pc[kMaxPieces];
   int darea = 0;
-  const int np = block_pieces(K + has_shared, inter, block, sms, lay, pc, kMaxPieces, darea);
+  const int np = block_pieces(K + has_shared, inter, has_shared, block, sms, lay, pc, kMaxPieces, darea);
   for (int i = 0; i < 1 + 8 * kMaxPieces; ++i) out[i] = 0;
   out[0] = np;
   for (int q = 0; q < np && q < kMaxPieces; ++q) {

@@ -226,8 +226,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
   const int tl = H / kSlice;
   const int R = pl.R, nparts = pl.nparts, hb = pl.hb;
   const int gw = tl < 32 ? tl : 32;                          // reduction width of a gate/up row
-  const long long V = (long long)NS * I;
-  const int len = (int)(V * (c + 1) / n - V * c / n);       // columns of this block
+  long long bv0, bv1;
+  block_bounds(NS, I, p.S, c, n, bv0, bv1);
+  const int len = (int)(bv1 - bv0);                         // columns of this block
   const int nstg = (len + R - 1) / R;
   const int ja = (int)((long long)H * c / n);               // accumulator slice this block clears
   const int nd = (int)((long long)H * (c + 1) / n) - ja;
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
     mbar_init(bar_dfull, 1);
     mbar_init(bar_ddone, kDnWarps);
     int dbytes = 0;
-    *s_np = block_pieces(NS, I, c, n, lay, s_pc, kMaxPieces, dbytes);
+    *s_np = block_pieces(NS, I, p.S, c, n, lay, s_pc, kMaxPieces, dbytes);
     *s_abort = 0;
     *s_hdone = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -782,14 +783,16 @@ FusedPlan fused_plan_for(int bits, int H, int I, int K, int S, int sms, int smem
   pl.R = R;
   pl.nparts = nparts;
   pl.stage_bytes = round_up_i((long long)R * lay.gu_row, 128);
-  const long long V = (long long)NS * I;
-  pl.len_max = (int)((V + grid - 1) / grid);
+  pl.len_max = 0;
   int darea = 0;
   for (int c = 0; c < grid; ++c) {
     Piece pc[kMaxPieces];
     int b = 0;
-    if (block_pieces(NS, I, c, grid, lay, pc, kMaxPieces, b) > kMaxPieces) return pl;
+    if (block_pieces(NS, I, S, c, grid, lay, pc, kMaxPieces, b) > kMaxPieces) return pl;
     darea = b > darea ? b : darea;
+    long long v0, v1;
+    block_bounds(NS, I, S, c, grid, v0, v1);
+    pl.len_max = (int)(v1 - v0) > pl.len_max ? (int)(v1 - v0) : pl.len_max;
   }
   pl.darea_bytes = round_up_i(darea > 128 ? darea : 128, 128);
   pl.hb = bits == 4 ? 8 : 12;

@@ -130,6 +130,9 @@ constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, redu
 #ifndef FMOE_FUSED_SB_GLOBAL
 #define FMOE_FUSED_SB_GLOBAL 0
 #endif
+#ifndef FMOE_FUSED_SHARED_WEIGHT
+#define FMOE_FUSED_SHARED_WEIGHT 100
+#endif
 
 constexpr int kFusedStageCap = FMOE_FUSED_STAGE_CAP < kMaxStages ? FMOE_FUSED_STAGE_CAP : kMaxStages;
 constexpr int kFusedDareaAfter = FMOE_FUSED_DAREA_AFTER;
@@ -141,6 +144,11 @@ constexpr unsigned kPollNs = FMOE_POLL_NS;
 // shared memory, and the ring gets the space (4 stages instead of 3 at the
 // Qwen shape); measured 1 % slower, so off
 constexpr bool kFusedSbGlobal = FMOE_FUSED_SB_GLOBAL != 0;
+// cost of a shared-expert column against a routed one, in percent, when the
+// blocks' columns are split: the shared expert needs no routing and is
+// streamed during the previous layer's exchange, so a lower cost gives its
+// blocks more columns and every routed block fewer
+constexpr int kFusedSharedWeight = FMOE_FUSED_SHARED_WEIGHT;
 
 // A block's intermediate columns within one slot: columns [i0, i0+cnt) of
 // slot `slot`, local indices [loc, loc+cnt); in the block's down area its
@@ -150,15 +158,25 @@ struct Piece {
   int slot, i0, cnt, loc, col_off, sb_off, g0, ng;
 };
 
-// Columns of block c of n: the virtual columns [V*c/n, V*(c+1)/n) of the
-// slot-major sequence (slot 0 = the shared expert when there is one), split
-// at slot boundaries.  Returns the number of pieces (at most max_pieces are
-// written) and the down-area bytes they need.
-__host__ __device__ inline int block_pieces(int NS, int I, int c, int n, const BlobLayout& lay, Piece* pc,
+// The virtual columns [v0, v1) of block c of n in the slot-major sequence
+// (slot 0 = the shared expert when S = 1): equal shares of the total cost,
+// a shared column costing kFusedSharedWeight percent of a routed one.
+__host__ __device__ inline void block_bounds(int NS, int I, int S, int c, int n, long long& v0, long long& v1) {
+  const long long ws = S ? kFusedSharedWeight : 100;
+  const long long cs = (long long)S * I * ws;                       // cost of the shared columns
+  const long long C = cs + (long long)(NS - S) * I * 100;
+  auto col = [&](long long x) -> long long { return x <= cs ? x / ws : (long long)S * I + (x - cs) / 100; };
+  v0 = col(C * c / n);
+  v1 = col(C * (c + 1) / n);
+}
+
+// Columns of block c of n (block_bounds), split at slot boundaries.  Returns
+// the number of pieces (at most max_pieces are written) and the down-area
+// bytes they need.
+__host__ __device__ inline int block_pieces(int NS, int I, int S, int c, int n, const BlobLayout& lay, Piece* pc,
                                             int max_pieces, int& darea_bytes) {
-  const long long V = (long long)NS * I;
-  long long v = V * c / n;
-  const long long v1 = V * (c + 1) / n;
+  long long v, v1;
+  block_bounds(NS, I, S, c, n, v, v1);
   int np = 0, off = 0, u = 0;
   while (v < v1) {
     const int slot = (int)(v / I), i0 = (int)(v % I);
