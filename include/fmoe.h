@@ -161,7 +161,8 @@ fmoe_status fmoe_router_logits(const uint16_t* w_router, const float* x, int T, 
  * (two launches on `stream`).
  *   logits  fp32 [T][E]   out (kept: the routing decisions are taken on them)
  *   ids, weights          out, as fmoe_route
- *   shared_gate_w bf16 [H] or NULL; gate fp32 [T] out (NULL when shared_gate_w is)
+ *   shared_gate_w bf16 [H] (16-byte aligned) or NULL; gate fp32 [T] out (NULL
+ *                 when shared_gate_w is)
  */
 fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, int hidden, int E, int K,
                               const uint16_t* shared_gate_w, float* logits, int32_t* ids, float* weights,

@@ -130,7 +130,7 @@ fmoe_status fmoe_route_from_x(const uint16_t* w_router, const float* x, int T, i
   if (ids == nullptr || weights == nullptr || !aligned(ids, 4) || !aligned(weights, 4)) return FMOE_ERR_INVALID_ARG;
   if (K < 1 || K > E || K > FMOE_MAX_TOPK) return FMOE_ERR_INVALID_ARG;
   if ((shared_gate_w == nullptr) != (gate == nullptr)) return FMOE_ERR_INVALID_ARG;
-  if (shared_gate_w != nullptr && (!aligned(shared_gate_w, 2) || !aligned(gate, 4))) return FMOE_ERR_INVALID_ARG;
+  if (shared_gate_w != nullptr && (!aligned(shared_gate_w, 16) || !aligned(gate, 4))) return FMOE_ERR_INVALID_ARG;
   fmoe_status s = fmoe_router_logits(w_router, x, T, hidden, E, logits, stream);
   if (s != FMOE_OK) return s;
   return from_cuda(launch_route(logits, T, E, K, ids, weights, shared_gate_w, x, hidden, gate,

@@ -59,7 +59,15 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
   if (gate != nullptr) {
     float acc = 0.f;
     if (wsg != nullptr) {
-      for (int c = lane; c < H; c += 32) acc += bf16v(wsg[c]) * x[(size_t)t * H + c];
+      // eight columns per lane and step (H is a multiple of 64)
+      const uint4* w8 = reinterpret_cast<const uint4*>(wsg);
+      const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)t * H);
+      for (int c = lane; c < H / 8; c += 32) {
+        const uint4 wb = __ldg(w8 + c);
+        const float4 a = __ldg(x4 + 2 * c), b = __ldg(x4 + 2 * c + 1);
+        acc += (bf16lo(wb.x) * a.x + bf16hi(wb.x) * a.y) + (bf16lo(wb.y) * a.z + bf16hi(wb.y) * a.w);
+        acc += (bf16lo(wb.z) * b.x + bf16hi(wb.z) * b.y) + (bf16lo(wb.w) * b.z + bf16hi(wb.w) * b.w);
+      }
       acc = warp_sum(acc);
     }
     if (lane == 0) gate[t] = (wsg != nullptr) ? sigmoid_f(acc) : 0.f;
