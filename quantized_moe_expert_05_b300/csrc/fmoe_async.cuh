@@ -107,20 +107,6 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, u
   }
 }
 
-// Asynchronous global -> shared copy of N bytes (4, 8 or 16) through the
-// load/store path; completion per thread by commit groups.
-template <int N>
-__device__ __forceinline__ void cp_async_bytes(void* dst, const void* src) {
-  static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
-  if constexpr (N == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src), "n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Wait for an mbarrier phase for at most timeout_ns whether or not the block
 // has given up: used before a block exits, so that no bulk copy still in
 // flight writes its shared memory afterwards.
