@@ -902,19 +902,23 @@ __global__ void __launch_bounds__(kBdThreads, 1) batch_down_kernel(BatchArgs a, 
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[st]);
     }
-    // the eight warps' partial sums, added in warp order
+    // the eight warps' partial sums, added in warp order; a warp's buffer is
+    // [row within the lane's word][token][lane], so that both the writes and
+    // the reads below touch 32 consecutive words (no bank conflicts)
     float* xb = xbuf + (size_t)warp * RB * G;
 #pragma unroll
     for (int r = 0; r < RW; ++r)
 #pragma unroll
-      for (int t = 0; t < G; ++t) xb[(RW * lane + r) * G + t] = outp[r][t];
+      for (int t = 0; t < G; ++t) xb[(r * G + t) * 32 + lane] = outp[r][t];
     if (!cons_sync()) break;
     for (int idx = tid; idx < RB * n; idx += kBdWarps * 32) {
-      const int row = idx / n, t = idx - row * n;
+      const int ln = idx & 31, rest = idx >> 5;
+      const int r = rest % RW, t = rest / RW;
+      const int row = RW * ln + r;
       if (r0 + row < H) {
         float v = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < kBdWarps; ++w2) v += xbuf[((size_t)w2 * RB + row) * G + t];
+        for (int w2 = 0; w2 < kBdWarps; ++w2) v += xbuf[(size_t)w2 * RB * G + (r * G + t) * 32 + ln];
         const int pr = ctl->item[2 + t];
         y[((size_t)(pr >> 8) * NS + (pr & 255)) * H + r0 + row] = v;
       }
