@@ -138,12 +138,14 @@ __device__ __forceinline__ bool poll8(const unsigned long long* p, int need, flo
 }
 
 // Wait (bounded) until a release counter in shared memory reaches `target`,
-// spinning (the waiting warps resume as soon as the counter moves).
+// pausing kWaitNs between checks so that the waiting warps leave the issue
+// slots to the warps doing the arithmetic.
 __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, unsigned long long timeout_ns,
                                            uint32_t* err, volatile int* abort) {
   if (ld_acquire_shared(ctr) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
+    if (kWaitNs) __nanosleep(kWaitNs);
     if (ld_acquire_shared(ctr) >= target) return true;
     if ((it & 255u) == 0u) {
       if (*abort) return false;
@@ -665,7 +667,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_moe_kernel(const __gri
       const bool last = (l == p.L - 1) && p.hmid != nullptr;
       for (int k = 0; k < nstg; ++k) {
         const uint32_t ps = g_cons % (2u * pl.nstage);
-        mbar_wait_spin(&bar_gudone[ps], (g_cons / (2u * pl.nstage)) & 1u, tmo, p.err, s_abort);
+        if (kFinalSpin)
+          mbar_wait_spin(&bar_gudone[ps], (g_cons / (2u * pl.nstage)) & 1u, tmo, p.err, s_abort);
+        else
+          mbar_wait(&bar_gudone[ps], (g_cons / (2u * pl.nstage)) & 1u, tmo, p.err, s_abort);
         ++g_cons;
         const int nrec = min(R, len - k * R);
         for (int r = lane; r < nrec; r += 32) {

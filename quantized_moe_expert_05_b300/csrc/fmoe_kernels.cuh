@@ -127,6 +127,12 @@ constexpr int kCtrlBytes = 2048;       // barriers, pieces, routing result, redu
 #ifndef FMOE_POLL_NS
 #define FMOE_POLL_NS 64
 #endif
+#ifndef FMOE_WAIT_NS
+#define FMOE_WAIT_NS 32
+#endif
+#ifndef FMOE_FINAL_SPIN
+#define FMOE_FINAL_SPIN 0
+#endif
 #ifndef FMOE_FUSED_SB_GLOBAL
 #define FMOE_FUSED_SB_GLOBAL 0
 #endif
@@ -144,6 +150,14 @@ constexpr unsigned kPollNs = FMOE_POLL_NS;
 // shared memory, and the ring gets the space (4 stages instead of 3 at the
 // Qwen shape); measured 1 % slower, so off
 constexpr bool kFusedSbGlobal = FMOE_FUSED_SB_GLOBAL != 0;
+// pause between two checks of a counter the down warps wait on (0: spin):
+// spinning warps take issue slots and shared-memory bandwidth from the
+// gate/up warps, which set the pace of the ring (32 ns measured 1 % faster
+// than spinning at the Qwen 4-bit shape)
+constexpr unsigned kWaitNs = FMOE_WAIT_NS;
+// 1: the finaliser spins on the gate/up warps' partial sums; 0: it waits
+// suspended in the barrier unit (measured no slower, and it frees issue slots)
+constexpr bool kFinalSpin = FMOE_FINAL_SPIN != 0;
 // cost of a shared-expert column against a routed one, in percent, when the
 // blocks' columns are split: the shared expert needs no routing and is
 // streamed during the previous layer's exchange, so a lower cost gives its
