@@ -8,21 +8,22 @@
 // two-stage RMS normalisation and the 4-bit dequant matvec.
 //
 // A dense matrix is N row records (the row's codes, then one (scale,bias)
-// word per 64 columns, padded to 16 bytes).  One warp computes one output row
-// for all T <= 16 tokens (held in registers: the kernel is instantiated for
-// 1, 2, 4, 8 and 16): lane l takes code word l of every 128-byte span of the
-// row (coalesced loads of codes and of the inputs they meet), issues eight
-// such loads before their arithmetic, unpacks each word once and meets every
-// token's inputs with it, adding s * sum(q * x) + b * sum(x) with the word's
-// group scale and bias.  Sums are taken in a fixed order (words in order
-// within a lane, then a shuffle tree), so results are deterministic.
+// word per 64 columns, padded to 16 bytes).  One warp computes RPW output
+// rows for all T <= 16 tokens (the kernel is instantiated for 1, 2, 4, 8 and
+// 16 tokens held in registers): lane l takes code word l of every 128-byte
+// span of its rows (coalesced loads of codes and of the inputs they meet),
+// issues several words of every row before their arithmetic, unpacks each
+// word once, and meets each token's inputs, loaded once, with all RPW rows,
+// adding s * sum(q * x) + b * sum(x) with the word's group scale and bias.
+// Sums are taken in a fixed order (words in order within a lane, then a
+// shuffle tree), so results are deterministic.
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
 
 namespace {
 
-constexpr int kDgWarps = 8;
+constexpr int kDgWarps = 4;
 constexpr int kDgThreads = 32 * kDgWarps;
 
 __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
@@ -31,65 +32,103 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
   return v;
 }
 
+// rows per warp: two for one or two tokens (more warps in flight for a
+// latency-bound read), four for 4-bit codes and more tokens, where every
+// input load then serves four rows (measured at H 4096: T 16 from 112 to
+// 88 us, T 4 from 30 to 26 us; four rows at T 2 ran slower, 15 against 12 us)
+template <int BITS, int NT>
+__host__ __device__ constexpr int dg_rows() {
+  return NT <= 2 ? 2 : (BITS == 4 ? 4 : 2);
+}
+
 // NT: tokens held in registers, the smallest of 1, 2, 4, 8, 16 that is >= T.
-// Lane l takes code word l of every 128-byte span of the row, so that the
-// warp's loads of codes and of the inputs they meet are both coalesced.
 template <int BITS, int NT>
 __global__ void __launch_bounds__(kDgThreads) dense_gemv_kernel(const uint8_t* __restrict__ w, int N, int H, int rec,
                                                               const float* __restrict__ x, int T,
                                                               const float* residual, float* y) {
   constexpr int CPW = 32 / BITS;                        // columns per 32-bit word
-  constexpr int PASS = 8;                               // words per lane loaded before their arithmetic
+  constexpr int RPW = dg_rows<BITS, NT>();              // rows per warp
+  constexpr int PASS = NT >= 4 ? 4 : 8;                 // words per lane and row loaded before their arithmetic
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kDgWarps + warp;
-  if (row >= N) return;                                 // whole warps only: no barrier below
-  const uint8_t* r = w + (size_t)row * rec;
-  const uint32_t* codes = reinterpret_cast<const uint32_t*>(r);
-  const uint32_t* sbw = reinterpret_cast<const uint32_t*>(r + (size_t)H * BITS / 8);
-  const int nw = H / CPW / 32;                          // words per lane (H is a multiple of 64)
-  float acc[NT];
+  const int row0 = (blockIdx.x * kDgWarps + warp) * RPW;
+  if (row0 >= N) return;                                // whole warps only: no barrier below
+  const uint32_t* codes[RPW];
+  const uint32_t* sbw[RPW];
 #pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int r = 0; r < RPW; ++r) {
+    // a row past the last is read as the last row again; its sums are dropped
+    const uint8_t* rp = w + (size_t)min(row0 + r, N - 1) * rec;
+    codes[r] = reinterpret_cast<const uint32_t*>(rp);
+    sbw[r] = reinterpret_cast<const uint32_t*>(rp + (size_t)H * BITS / 8);
+  }
+  const int nwt = H / CPW;                              // code words of a row (H is a multiple of 64)
+  const int nw = (nwt + 31) / 32;                       // rounds of 32 words
+  float acc[RPW][NT];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
   for (int p0 = 0; p0 < nw; p0 += PASS) {
-    uint32_t q[PASS];
+    uint32_t q[PASS][RPW];
 #pragma unroll
-    for (int j = 0; j < PASS; ++j) q[j] = p0 + j < nw ? ld_stream_u32(codes + 32 * (p0 + j) + lane) : 0u;
+    for (int j = 0; j < PASS; ++j)
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        const int wi = 32 * (p0 + j) + lane;
+        q[j][r] = wi < nwt ? ld_stream_u32(codes[r] + wi) : 0u;
+      }
 #pragma unroll
     for (int j = 0; j < PASS; ++j) {
-      if (p0 + j < nw) {
+      if (32 * (p0 + j) + lane < nwt) {
         const int c0 = (32 * (p0 + j) + lane) * CPW;     // the word's first column
-        const uint32_t sb = __ldg(sbw + c0 / kGroup);
-        float qv[CPW];
+        float s[RPW], b[RPW], qv[RPW][CPW];
 #pragma unroll
-        for (int i = 0; i < CPW; ++i) qv[i] = (float)((q[j] >> (BITS * i)) & ((1u << BITS) - 1u));
-        const float s = bf16lo(sb), b = bf16hi(sb);
+        for (int r = 0; r < RPW; ++r) {
+          const uint32_t sb = __ldg(sbw[r] + c0 / kGroup);
+          s[r] = bf16lo(sb);
+          b[r] = bf16hi(sb);
+#pragma unroll
+          for (int i = 0; i < CPW; ++i) qv[r][i] = (float)((q[j][r] >> (BITS * i)) & ((1u << BITS) - 1u));
+        }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (t < T) {
             const float4* xp = reinterpret_cast<const float4*>(x + (size_t)t * H + c0);
-            float sq = 0.f, sx = 0.f;
+            float xv[CPW];
 #pragma unroll
             for (int v = 0; v < CPW / 4; ++v) {
               const float4 a = __ldg(xp + v);
-              sq = fmaf(qv[4 * v], a.x, sq);
-              sq = fmaf(qv[4 * v + 1], a.y, sq);
-              sq = fmaf(qv[4 * v + 2], a.z, sq);
-              sq = fmaf(qv[4 * v + 3], a.w, sq);
-              sx += (a.x + a.y) + (a.z + a.w);
+              xv[4 * v] = a.x;
+              xv[4 * v + 1] = a.y;
+              xv[4 * v + 2] = a.z;
+              xv[4 * v + 3] = a.w;
             }
-            acc[t] = fmaf(s, sq, fmaf(b, sx, acc[t]));
+            float sx = 0.f;
+#pragma unroll
+            for (int v = 0; v < CPW / 4; ++v) sx += (xv[4 * v] + xv[4 * v + 1]) + (xv[4 * v + 2] + xv[4 * v + 3]);
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+              float sq = 0.f;
+#pragma unroll
+              for (int i = 0; i < CPW; ++i) sq = fmaf(qv[r][i], xv[i], sq);
+              acc[r][t] = fmaf(s[r], sq, fmaf(b[r], sx, acc[r][t]));
+            }
           }
         }
       }
     }
   }
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    if (t < T) {
-      const float v = warp_sum(acc[t]);
-      if (lane == 0) {
-        const size_t o = (size_t)t * N + row;
-        y[o] = residual != nullptr ? residual[o] + v : v;
+  for (int r = 0; r < RPW; ++r) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < T) {
+        const float v = warp_sum(acc[r][t]);
+        const int row = row0 + r;
+        if (lane == 0 && row < N) {
+          const size_t o = (size_t)t * N + row;
+          y[o] = residual != nullptr ? residual[o] + v : v;
+        }
       }
     }
   }
@@ -133,9 +172,10 @@ int dense_row_bytes(int bits, int H) {
 
 cudaError_t launch_dense_gemv(const uint8_t* w, int bits, int N, int H, const float* x, int T, const float* residual,
                               float* y, cudaStream_t st) {
-  const int blocks = (N + kDgWarps - 1) / kDgWarps;
   const int rec = dense_row_bytes(bits, H);
-#define FMOE_DG(B, NT) dense_gemv_kernel<B, NT><<<blocks, kDgThreads, 0, st>>>(w, N, H, rec, x, T, residual, y)
+#define FMOE_DG(B, NT)                                                                      \
+  dense_gemv_kernel<B, NT><<<(N + kDgWarps * dg_rows<B, NT>() - 1) / (kDgWarps * dg_rows<B, NT>()), kDgThreads, 0, \
+                             st>>>(w, N, H, rec, x, T, residual, y)
   if (bits == 4) {
     if (T <= 1) FMOE_DG(4, 1);
     else if (T <= 2) FMOE_DG(4, 2);

@@ -105,7 +105,7 @@ def test_router_projection_matches_oracle(fm, T, E, H):
 
 
 @pytest.mark.parametrize("bits,N,H,T", [(4, 4096, 4096, 1), (4, 4096, 4096, 16), (2, 192, 512, 3), (4, 1000, 2048, 5),
-                                         (2, 2048, 2048, 1)])
+                                         (2, 2048, 2048, 1), (4, 101, 320, 2), (2, 67, 192, 7), (4, 33, 64, 16)])
 def test_dense_gemv_matches_oracle(fm, bits, N, H, T):
     w = synth.dense_matrix(N, H, bits, seed=9, tag=bits * 100 + T)
     x = synth.normal(9, 10 + T, (T, H))
