@@ -8,13 +8,14 @@
 // two-stage RMS normalisation and the 4-bit dequant matvec.
 //
 // A dense matrix is N row records (the row's codes, then one (scale,bias)
-// word per 64 columns, padded to 16 bytes).  One warp computes RPW output
-// rows for all T <= 16 tokens (the kernel is instantiated for 1, 2, 4, 8 and
-// 16 tokens held in registers): lane l takes code word l of every 128-byte
-// span of its rows (coalesced loads of codes and of the inputs they meet),
-// issues several words of every row before their arithmetic, unpacks each
-// word once, and meets each token's inputs, loaded once, with all RPW rows,
-// adding s * sum(q * x) + b * sum(x) with the word's group scale and bias.
+// word per 64 columns, padded to 16 bytes).  One warp computes RPW (1, 2 or
+// 4) output rows for all T <= 16 tokens (the kernel is instantiated for 1,
+// 2, 4, 8 and 16 tokens held in registers): lane l takes code word l of
+// every 128-byte span of its rows (coalesced loads of codes and of the
+// inputs they meet), issues several words of every row before their
+// arithmetic, unpacks each word once, and meets each token's inputs, loaded
+// once, with all RPW rows, adding s * sum(q * x) + b * sum(x) with the
+// word's group scale and bias.
 // Sums are taken in a fixed order (words in order within a lane, then a
 // shuffle tree), so results are deterministic.
 #include "fmoe_kernels.cuh"
@@ -32,13 +33,16 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
   return v;
 }
 
-// rows per warp: two for one or two tokens (more warps in flight for a
-// latency-bound read), four for 4-bit codes and more tokens, where every
-// input load then serves four rows (measured at H 4096: T 16 from 112 to
-// 88 us, T 4 from 30 to 26 us; four rows at T 2 ran slower, 15 against 12 us)
+// rows per warp, measured at H 4096 (8 o_proj launches in one graph):
+// 4-bit, one row for one or two tokens (T 2: 12.0 us against 13.9 with two
+// rows; T 1 the same, 8.5 us) and four rows from four tokens on, where every
+// input load serves four rows (T 16: 88 us against 112 with one row); 2-bit,
+// two rows throughout (T 1: 8.2 against 11.4 us; T 16: 76 against 144 us).
+// Loading sixteen words per row before the arithmetic at T 1 instead of
+// eight was slower (8.7 and 9.0 us).
 template <int BITS, int NT>
 __host__ __device__ constexpr int dg_rows() {
-  return NT <= 2 ? 2 : (BITS == 4 ? 4 : 2);
+  return BITS == 4 ? (NT <= 2 ? 1 : 4) : 2;
 }
 
 // NT: tokens held in registers, the smallest of 1, 2, 4, 8, 16 that is >= T.
