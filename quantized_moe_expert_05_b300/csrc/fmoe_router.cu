@@ -4,23 +4,24 @@
 // flash-moe write-up (discuss.pytorch.kr), section "per-layer pipeline": the
 // second command buffer computes the routing logits on the GPU before the
 // softmax + top-K.  The projection reads E*H*2 bytes once (4 MiB for E 512,
-// H 4096) and is bound by HBM latency at this size: each router row is read
-// by four warps (a quarter of H each), two rows per block, so that E = 512
-// spreads over 256 blocks; a lane issues all its 16-byte streaming loads of
-// the row before any arithmetic (up to 8 in flight), and every loaded row
-// chunk meets all T tokens from registers.  The sums are taken in a fixed
-// order (lane, shuffle tree, then the four quarters), so the logits do not
-// depend on scheduling.
+// H 4096).  Each group of RPW router rows is read by four warps (a quarter
+// of H each), two groups per block; a lane issues its 16-byte streaming
+// loads of a pass (all of them for one row, two chunks of every row for
+// several) before any arithmetic, and every token's inputs, loaded once,
+// meet all RPW rows from registers.  The sums are taken in a fixed order
+// (lane, shuffle tree, then the four quarters), so the logits do not depend
+// on scheduling.
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
 
 namespace {
 
-constexpr int kRtRowsPerBlock = 2;
+constexpr int kRtGroupsPerBlock = 2;
 constexpr int kRtWarpsPerRow = 4;
-constexpr int kRtChunks = FMOE_MAX_HIDDEN / 8 / kRtWarpsPerRow / 32;   // 16-byte loads per lane, at most
-constexpr int kRtThreads = 32 * kRtRowsPerBlock * kRtWarpsPerRow;
+constexpr int kRtChunks = FMOE_MAX_HIDDEN / 8 / kRtWarpsPerRow / 32;   // 16-byte loads per lane and row, at most
+constexpr int kRtThreads = 32 * kRtGroupsPerBlock * kRtWarpsPerRow;
+constexpr int kRtMaxRows = 4;                              // bound on rt_rows()
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -30,68 +31,105 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-__global__ void __launch_bounds__(kRtThreads) router_kernel(const uint16_t* __restrict__ w, const float* __restrict__ x,
+// rows of a group, measured at E 512, H 4096 (8 projections in one graph,
+// against a kernel holding 16 tokens always, one row per group): one row
+// (256 blocks for E 512) takes T 1 from 6.5 to 3.3 us, T 4 from 8.5 to 6.2
+// and T 16 from 17.2 to 16.2; at two tokens, two rows (128 blocks) sharing
+// each input load take 5.5 us against 7.4.  Two rows from four tokens on
+// ran slower (T 16: 21.2 us), four rows (64 blocks) slower still (25.4).
+__host__ __device__ constexpr int rt_rows(int NT) { return NT == 2 ? 2 : 1; }
+
+// NT: tokens held in registers, the smallest of 1, 2, 4, 8, 16 that is >= T.
+template <int NT>
+__global__ void __launch_bounds__(kRtThreads, 1) router_kernel(const uint16_t* __restrict__ w, const float* __restrict__ x,
                                                           int T, int H, int E, float* __restrict__ logits) {
-  __shared__ float s_part[kRtRowsPerBlock][kRtWarpsPerRow][FMOE_MAX_TOKENS];
+  constexpr int RPW = rt_rows(NT);
+  constexpr int PASS = RPW == 1 ? kRtChunks : 2;          // chunks per lane and row loaded before their arithmetic
+  __shared__ float s_part[kRtGroupsPerBlock][kRtWarpsPerRow][kRtMaxRows][NT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rl = warp / kRtWarpsPerRow, part = warp % kRtWarpsPerRow;
-  const int row = blockIdx.x * kRtRowsPerBlock + rl;
-  float acc[FMOE_MAX_TOKENS];
+  const int rg = warp / kRtWarpsPerRow, part = warp % kRtWarpsPerRow;
+  const int row0 = (blockIdx.x * kRtGroupsPerBlock + rg) * RPW;
+  float acc[RPW][NT];
 #pragma unroll
-  for (int t = 0; t < FMOE_MAX_TOKENS; ++t) acc[t] = 0.f;
-  if (row < E) {
+  for (int r = 0; r < RPW; ++r)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+  if (row0 < E) {
     const int n8 = H / 8;                                   // 16-byte chunks of a row
     const int c0 = n8 * part / kRtWarpsPerRow, c1 = n8 * (part + 1) / kRtWarpsPerRow;
-    const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)row * H);
+    const uint4* wr[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)   // a row past the last is read as the last again; its sums are dropped
+      wr[r] = reinterpret_cast<const uint4*>(w + (size_t)min(row0 + r, E - 1) * H);
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    uint4 q[kRtChunks];
 #pragma unroll
-    for (int j = 0; j < kRtChunks; ++j) {
-      const int c = c0 + lane + 32 * j;
-      q[j] = c < c1 ? ld_stream(wr + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int j0 = 0; j0 < kRtChunks; j0 += PASS) {
+      uint4 q[PASS][RPW];
 #pragma unroll
-    for (int j = 0; j < kRtChunks; ++j) {
-      const int c = c0 + lane + 32 * j;
-      if (c < c1) {
-        const float w0 = bf16lo(q[j].x), w1 = bf16hi(q[j].x), w2 = bf16lo(q[j].y), w3 = bf16hi(q[j].y);
-        const float w4 = bf16lo(q[j].z), w5 = bf16hi(q[j].z), w6 = bf16lo(q[j].w), w7 = bf16hi(q[j].w);
+      for (int j = 0; j < PASS; ++j) {
+        const int c = c0 + lane + 32 * (j0 + j);
 #pragma unroll
-        for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
-          if (t < T) {
-            const float4 a = __ldg(x4 + ((size_t)t * H >> 2) + 2 * c);
-            const float4 b = __ldg(x4 + ((size_t)t * H >> 2) + 2 * c + 1);
-            float s = acc[t];
-            s = fmaf(w0, a.x, s);
-            s = fmaf(w1, a.y, s);
-            s = fmaf(w2, a.z, s);
-            s = fmaf(w3, a.w, s);
-            s = fmaf(w4, b.x, s);
-            s = fmaf(w5, b.y, s);
-            s = fmaf(w6, b.z, s);
-            s = fmaf(w7, b.w, s);
-            acc[t] = s;
+        for (int r = 0; r < RPW; ++r) q[j][r] = c < c1 ? ld_stream(wr[r] + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < PASS; ++j) {
+        const int c = c0 + lane + 32 * (j0 + j);
+        if (c < c1) {
+          float wv[RPW][8];
+#pragma unroll
+          for (int r = 0; r < RPW; ++r) {
+            wv[r][0] = bf16lo(q[j][r].x);
+            wv[r][1] = bf16hi(q[j][r].x);
+            wv[r][2] = bf16lo(q[j][r].y);
+            wv[r][3] = bf16hi(q[j][r].y);
+            wv[r][4] = bf16lo(q[j][r].z);
+            wv[r][5] = bf16hi(q[j][r].z);
+            wv[r][6] = bf16lo(q[j][r].w);
+            wv[r][7] = bf16hi(q[j][r].w);
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t < T) {
+              const float4 a = __ldg(x4 + ((size_t)t * H >> 2) + 2 * c);
+              const float4 b = __ldg(x4 + ((size_t)t * H >> 2) + 2 * c + 1);
+#pragma unroll
+              for (int r = 0; r < RPW; ++r) {
+                float v = acc[r][t];
+                v = fmaf(wv[r][0], a.x, v);
+                v = fmaf(wv[r][1], a.y, v);
+                v = fmaf(wv[r][2], a.z, v);
+                v = fmaf(wv[r][3], a.w, v);
+                v = fmaf(wv[r][4], b.x, v);
+                v = fmaf(wv[r][5], b.y, v);
+                v = fmaf(wv[r][6], b.z, v);
+                v = fmaf(wv[r][7], b.w, v);
+                acc[r][t] = v;
+              }
+            }
           }
         }
       }
     }
   }
 #pragma unroll
-  for (int t = 0; t < FMOE_MAX_TOKENS; ++t) {
-    if (t < T) {
-      const float v = warp_sum(acc[t]);
-      if (lane == 0) s_part[rl][part][t] = v;
+  for (int r = 0; r < RPW; ++r) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < T) {
+        const float v = warp_sum(acc[r][t]);
+        if (lane == 0) s_part[rg][part][r][t] = v;
+      }
     }
   }
   __syncthreads();
-  const int i = threadIdx.x;
-  if (i < kRtRowsPerBlock * T) {
-    const int r = i / T, t = i - r * T;
-    const int e = blockIdx.x * kRtRowsPerBlock + r;
+  for (int i = threadIdx.x; i < kRtGroupsPerBlock * RPW * T; i += kRtThreads) {
+    const int t = i % T, rr = i / T;
+    const int g = rr / RPW, r = rr % RPW;
+    const int e = (blockIdx.x * kRtGroupsPerBlock + g) * RPW + r;
     if (e < E) {
       float v = 0.f;
 #pragma unroll
-      for (int h2 = 0; h2 < kRtWarpsPerRow; ++h2) v += s_part[r][h2][t];
+      for (int h2 = 0; h2 < kRtWarpsPerRow; ++h2) v += s_part[g][h2][r][t];
       logits[(size_t)t * E + e] = v;
     }
   }
@@ -100,8 +138,15 @@ __global__ void __launch_bounds__(kRtThreads) router_kernel(const uint16_t* __re
 }  // namespace
 
 cudaError_t launch_router(const uint16_t* w, const float* x, int T, int H, int E, float* logits, cudaStream_t st) {
-  const int blocks = (E + kRtRowsPerBlock - 1) / kRtRowsPerBlock;
-  router_kernel<<<blocks, kRtThreads, 0, st>>>(w, x, T, H, E, logits);
+#define FMOE_RT(NT)                                                                                  \
+  router_kernel<NT><<<(E + kRtGroupsPerBlock * rt_rows(NT) - 1) / (kRtGroupsPerBlock * rt_rows(NT)), kRtThreads, 0, \
+                      st>>>(w, x, T, H, E, logits)
+  if (T <= 1) FMOE_RT(1);
+  else if (T <= 2) FMOE_RT(2);
+  else if (T <= 4) FMOE_RT(4);
+  else if (T <= 8) FMOE_RT(8);
+  else FMOE_RT(16);
+#undef FMOE_RT
   return cudaGetLastError();
 }
 

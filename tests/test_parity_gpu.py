@@ -78,7 +78,7 @@ def test_route_matches_oracle(fm, E, K):
 
 
 @pytest.mark.parametrize("T,E,H", [(1, 8, 512), (3, 100, 192), (1, 512, 4096), (5, 512, 4096), (16, 512, 4096),
-                                   (16, 512, 2048)])
+                                   (16, 512, 2048), (2, 7, 256), (8, 37, 1024), (4, 1, 64)])
 def test_router_projection_matches_oracle(fm, T, E, H):
     shape = dataclasses.replace(synth.TINY, hidden=H, n_experts=E)
     w = synth.router_matrix(shape, layer=T)
