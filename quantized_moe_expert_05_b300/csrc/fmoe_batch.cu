@@ -1041,8 +1041,8 @@ static cudaError_t allow_smem(Kern k, size_t bytes, size_t& done) {
 static size_t g_smem_set[64][4];
 static std::mutex g_smem_mu;
 
-// The driver's tensor-map encoder, looked up once through the runtime (no
-// link against the driver library).
+// cuTensorMapEncodeTiled (a CUDA driver API entry point), looked up once
+// through the runtime, so that the library need not link libcuda.
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::once_flag once;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
