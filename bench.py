@@ -56,6 +56,9 @@ def parse():
                     help="skip the other configurations measured with the default workload")
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="run only this many steps (for an ncu launch list); prints no JSON")
+    ap.add_argument("--profile-next", type=int, default=0,
+                    help="run only this many launches each of the router projection and the o_proj "
+                         "(Qwen shape, T = 1 and 16) inside an NVTX range 'next' (for ncu); prints no JSON")
     return ap.parse_args()
 
 
@@ -822,10 +825,41 @@ def chain_summary(shape, n_layers, r):
             "tokens_per_s_per_block": n_layers * 1e3 / r["ms_per_step"]}
 
 
+def profile_next(n, dev):
+    """n launches each of the router projection (E 512, H 4096, bf16) and the
+    4-bit o_proj (4096 x 4096) at T = 1 and T = 16, inside an NVTX range
+    'next', on freshly generated matrices (for an ncu capture, whose default
+    cache control flushes L2 before every captured launch)."""
+    import torch
+    from quantized_moe_expert_05_b300 import build
+    build.build()
+    from quantized_moe_expert_05_b300 import fmoe as fm
+    import synth
+
+    wr = synth.router_matrix(synth.QWEN_Q4, layer=0).to(dev)
+    wd = synth.dense_matrix(4096, 4096, 4, seed=31, tag=0, device=dev)
+    xs = {T: synth.normal(31, 900 + T, (T, 4096)).to(dev) for T in (1, 16)}
+    res = {T: synth.normal(31, 901 + T, (T, 4096)).to(dev) for T in (1, 16)}
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("next")
+    for T in (1, 16):
+        for _ in range(n):
+            fm.router_logits(wr, xs[T])
+        for _ in range(n):
+            fm.dense_gemv(wd, 4, 4096, xs[T], residual=res[T])
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_next:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        return profile_next(args.profile_next, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
     if args.workload == "qwen_q4_zipf":
         return run_batch(args)
 
