@@ -15,9 +15,8 @@
 // inputs they meet), issues several words of every row before their
 // arithmetic, unpacks each word once, and meets each token's inputs, loaded
 // once, with all RPW rows, adding s * sum(q * x) + b * sum(x) with the
-// word's group scale and bias.
-// Sums are taken in a fixed order (words in order within a lane, then a
-// shuffle tree), so results are deterministic.
+// word's group scale and bias.  Sums are taken in a fixed order (words in
+// order within a lane, then a shuffle tree), so results are deterministic.
 #include "fmoe_kernels.cuh"
 
 namespace fmoe {
