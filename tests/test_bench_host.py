@@ -69,3 +69,22 @@ def test_reference_arm_prints_the_contract_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["e2e"]["value"] == line["value"]
+
+
+def test_committed_traffic_only_while_the_kernel_sources_match(monkeypatch, tmp_path):
+    """roofline.traffic comes from the committed ncu record only while the
+    hashed kernel sources are the ones it was captured on; otherwise null."""
+    srcs = ["a.cu", "b.cuh"]
+    for name in srcs:
+        (tmp_path / name).write_text(f"// {name}\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", srcs)
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "ncu_traffic.txt").write_text(
+        f"# workload bytes hash\nqwen_q4 123456 {h}\nqwen_q2 999 0000000000000000\n")
+    assert bench.committed_traffic("qwen_q4") == 123456.0
+    assert bench.committed_traffic("qwen_q2") is None          # captured on other sources
+    assert bench.committed_traffic("stack48") is None          # no record
+    (tmp_path / "b.cuh").write_text("// b.cuh, changed\n")
+    assert bench.committed_traffic("qwen_q4") is None
